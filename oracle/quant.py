@@ -1,0 +1,171 @@
+"""amax, scales, the scaled cast, overflow/underflow counters, fine-grained units and
+delayed scaling (oracle; test infrastructure).
+
+Sources:
+* "FP8 stability guardrails" page, "Why FP8 is tempting and why it is fragile":
+  values beyond the format maximum overflow or saturate, tiny ones underflow to zero;
+  the first paragraph names "overflow telemetry" as a guardrail.
+* Same page, "Real products, models, and research": fine-grained tile and block
+  scaling factors (DeepSeek-V3) and delayed scaling with amax history tracking
+  (Transformer Engine).
+* "#84 FP8 Precision" page, "Explanation": weights are divided by a scale before the
+  E4M3 cast so that no value overflows the exponent range.
+
+Definitions (readings where the pages leave a step open):
+* amax = max |x| over the scaling unit, NaN ignored, -0 counts as 0; 0 when empty.
+* current scaling: s = fl32(FP8_MAX / amax), d = fl32(amax / FP8_MAX) if amax is
+  finite and > 0, else s = d = 1.  Dividing by the scale d is taken as multiplying by
+  s, so the cast is q = cast(fl32(float(x) * s)).
+* units: the whole tensor; a 1x128 row tile along the contraction dimension; a
+  128x128 block.  Dimensions that are not multiples of 128 are not tiled.
+* overflow = number of non-NaN inputs with |fl32(x * s)| > FP8_MAX (infinite inputs
+  included); underflow = number of non-zero non-NaN inputs whose code is +-0.
+* delayed scaling: a ring of ``hist_len`` fp32 amaxes and a push count n.  A cast uses
+  amax_eff = max of the filled entries when n > 0, else (bootstrap) the current amax.
+  Each cast records its own current amax; ``commit`` pushes it at index n % hist_len.
+
+Parity: amax, scales, codes and counters are pinned by brute-force tests on small
+arrays (tests/test_oracle_quant.py).  The delayed-scaling state machine is "parity
+unpinned" by the pages beyond those invariants (the pages name the technique only).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import fp8
+
+TILE = 128
+
+
+def widen_bf16(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float32 values, exactly."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def amax(x_bits: np.ndarray) -> np.float32:
+    v = np.abs(widen_bf16(x_bits)).reshape(-1)
+    v = v[~np.isnan(v)]
+    if v.size == 0:
+        return np.float32(0.0)
+    return np.float32(v.max())
+
+
+def scales_from_amax(a, fmt: str):
+    """(s, d) as float32 from an amax, per the current-scaling rule."""
+    a = np.float32(a)
+    mx = np.float32(fp8.fp8_max(fmt))
+    if np.isfinite(a) and a > 0:
+        return np.float32(mx / a), np.float32(a / mx)
+    return np.float32(1.0), np.float32(1.0)
+
+
+def cast_with_scale(x_bits: np.ndarray, s, fmt: str):
+    """codes, overflow count, underflow count for q = cast(fl32(x * s))."""
+    x = widen_bf16(x_bits)
+    v = (x * np.float32(s)).astype(np.float32)            # one fp32 multiply, RNE
+    q = fp8.cast(v, fmt)
+    mx = fp8.fp8_max(fmt)
+    notnan = ~np.isnan(x)
+    overflow = int(np.count_nonzero(notnan & (np.abs(v.astype(np.float64)) > mx)))
+    underflow = int(np.count_nonzero(notnan & (x != 0) & ((q & 0x7F) == 0)))
+    return q, overflow, underflow
+
+
+def quantize_tensor(x_bits: np.ndarray, fmt: str):
+    """Per-tensor current scaling.  Returns dict(q, qT, amax, s, d, overflow, underflow)."""
+    a = amax(x_bits)
+    s, d = scales_from_amax(a, fmt)
+    q, ov, un = cast_with_scale(x_bits, s, fmt)
+    out = dict(q=q, amax=a, s=s, d=d, overflow=ov, underflow=un)
+    if q.ndim == 2:
+        out["qT"] = np.ascontiguousarray(q.T)
+    return out
+
+
+def quantize_tile_1x128(x_bits: np.ndarray, fmt: str):
+    """One scale per (row, 128-column tile).  Returns dict(q, d[R, C/128], amax, s, overflow, underflow)."""
+    R, C = x_bits.shape
+    assert C % TILE == 0
+    T = C // TILE
+    q = np.empty((R, C), dtype=np.uint8)
+    d = np.empty((R, T), dtype=np.float32)
+    s = np.empty((R, T), dtype=np.float32)
+    am = np.empty((R, T), dtype=np.float32)
+    ov = un = 0
+    for i in range(R):
+        for t in range(T):
+            unit = x_bits[i, t * TILE:(t + 1) * TILE]
+            a = amax(unit)
+            si, di = scales_from_amax(a, fmt)
+            qi, o, u = cast_with_scale(unit, si, fmt)
+            q[i, t * TILE:(t + 1) * TILE] = qi
+            d[i, t], s[i, t], am[i, t] = di, si, a
+            ov += o
+            un += u
+    return dict(q=q, d=d, s=s, amax=am, overflow=ov, underflow=un)
+
+
+def quantize_block_128x128(w_bits: np.ndarray, fmt: str):
+    """One scale per 128x128 block.  Returns dict(q, qT, d[R/128, C/128], amax, s, overflow, underflow)."""
+    R, C = w_bits.shape
+    assert R % TILE == 0 and C % TILE == 0
+    A, B = R // TILE, C // TILE
+    q = np.empty((R, C), dtype=np.uint8)
+    d = np.empty((A, B), dtype=np.float32)
+    s = np.empty((A, B), dtype=np.float32)
+    am = np.empty((A, B), dtype=np.float32)
+    ov = un = 0
+    for a in range(A):
+        for b in range(B):
+            unit = w_bits[a * TILE:(a + 1) * TILE, b * TILE:(b + 1) * TILE]
+            m = amax(unit)
+            si, di = scales_from_amax(m, fmt)
+            qi, o, u = cast_with_scale(unit, si, fmt)
+            q[a * TILE:(a + 1) * TILE, b * TILE:(b + 1) * TILE] = qi
+            d[a, b], s[a, b], am[a, b] = di, si, m
+            ov += o
+            un += u
+    return dict(q=q, qT=np.ascontiguousarray(q.T), d=d, s=s, amax=am, overflow=ov, underflow=un)
+
+
+class DelayedState:
+    """Per-tensor scaling state of one tensor role (x, W or dy) of one layer."""
+
+    def __init__(self, hist_len: int = 16):
+        self.hist_len = hist_len
+        self.hist = np.zeros(hist_len, dtype=np.float32)
+        self.count = 0
+        self.scale = np.float32(1.0)
+        self.scale_inv = np.float32(1.0)
+        self.amax_cur = np.float32(0.0)
+        self.overflow = 0
+        self.underflow = 0
+
+    def amax_eff(self):
+        n = min(self.count, self.hist_len)
+        if n == 0:
+            return None
+        return np.float32(self.hist[:n].max())
+
+    def quantize(self, x_bits: np.ndarray, fmt: str, delayed: bool = True):
+        """Cast with the delayed scale (or the current one in bootstrap / current mode)."""
+        cur = amax(x_bits)
+        eff = self.amax_eff() if delayed else None
+        a = cur if eff is None else eff
+        s, d = scales_from_amax(a, fmt)
+        q, ov, un = cast_with_scale(x_bits, s, fmt)
+        self.scale, self.scale_inv, self.amax_cur = s, d, cur
+        self.overflow += ov
+        self.underflow += un
+        out = dict(q=q, s=s, d=d, amax=cur, overflow=ov, underflow=un)
+        if q.ndim == 2:
+            out["qT"] = np.ascontiguousarray(q.T)
+        return out
+
+    def commit(self):
+        self.hist[self.count % self.hist_len] = self.amax_cur
+        self.count += 1
+
+    def snapshot(self):
+        return dict(hist=self.hist.copy(), count=self.count, scale=self.scale, scale_inv=self.scale_inv,
+                    amax_cur=self.amax_cur, overflow=self.overflow, underflow=self.underflow)
