@@ -1,0 +1,362 @@
+// api.cu -- the C ABI declared in include/fp8gb.h: argument validation, the order of
+// launches of each entry point, and the device error word.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fp8gb.h"
+#include "kernels.h"
+
+namespace fp8gb {
+
+// Bit set by any bounded wait that ran out (one word per device that loads the library).
+__device__ uint32_t g_device_error_word;
+
+namespace {
+
+thread_local char g_detail[512] = "";
+std::atomic<unsigned long long> g_wait_limit_ns{4000000000ull};
+
+fp8_status_t fail(fp8_status_t s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+fp8_status_t cuda_fail(cudaError_t e, const char* where) {
+  return fail(FP8_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDev = 64;
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+QuantState to_qs(const fp8_tensor_state_t* st) {
+  QuantState q{};
+  if (st != nullptr) {
+    q.hist = st->amax_history;
+    q.hist_count = st->hist_count;
+    q.scale = st->scale;
+    q.scale_inv = st->scale_inv;
+    q.amax_cur = st->amax_cur;
+    q.counters = st->counters;
+    q.hist_len = st->hist_len;
+  }
+  return q;
+}
+
+fp8_status_t check_state(const fp8_tensor_state_t* st, fp8_scaling_t mode, const char* who) {
+  if (st == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: scaling state is required", who);
+  if (!st->scale || !st->scale_inv || !st->amax_cur || !st->counters)
+    return fail(FP8_ERR_INVALID_ARG, "%s: state has a null scale, scale_inv, amax_cur or counters", who);
+  if (mode == FP8_SCALE_DELAYED && (!st->amax_history || !st->hist_count || st->hist_len <= 0))
+    return fail(FP8_ERR_INVALID_ARG, "%s: delayed scaling needs amax_history, hist_count and hist_len > 0", who);
+  return FP8_OK;
+}
+
+}  // namespace
+
+int num_sms() {
+  static int cache[kMaxDev] = {};
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDev) return 148;
+  if (cache[d] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0) n = 148;
+    cache[d] = n;
+  }
+  return cache[d];
+}
+
+WaitCtl wait_ctl() {
+  static uint32_t* ptr[kMaxDev] = {};
+  static std::mutex mu;
+  const int d = current_device();
+  WaitCtl w{nullptr, g_wait_limit_ns.load()};
+  if (d < 0 || d >= kMaxDev) return w;
+  std::lock_guard<std::mutex> lk(mu);
+  if (ptr[d] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error_word) == cudaSuccess) ptr[d] = static_cast<uint32_t*>(p);
+  }
+  w.err = ptr[d];
+  return w;
+}
+
+}  // namespace fp8gb
+
+using namespace fp8gb;
+
+namespace {
+
+fp8_status_t validate_common(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, const char* who) {
+  if (rows < 0 || cols < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
+  if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_INVALID_ARG, "%s: unknown format %d", who, fmt);
+  if (rows * cols > 0 && x == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: null input", who);
+  if (ld < cols) return fail(FP8_ERR_INVALID_ARG, "%s: ld (%lld) < cols (%lld)", who, (long long)ld, (long long)cols);
+  if (rows > (1ll << 31) || cols > (1ll << 31)) return fail(FP8_ERR_UNSUPPORTED, "%s: dimension beyond 2^31", who);
+  return FP8_OK;
+}
+
+fp8_status_t quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld, fp8_format_t fmt, fp8_gran_t gran,
+                           fp8_scaling_t mode, const fp8_tensor_state_t* st, void* q, void* qT, float* unit_si,
+                           cudaStream_t stream) {
+  const char* who = "fp8_quantize";
+  fp8_status_t s = validate_common(x, rows, cols, ld, fmt, who);
+  if (s != FP8_OK) return s;
+  if (gran != FP8_GRAN_TENSOR && gran != FP8_GRAN_TILE_1x128 && gran != FP8_GRAN_BLOCK_128x128)
+    return fail(FP8_ERR_INVALID_ARG, "%s: unknown granularity %d", who, (int)gran);
+  if (mode != FP8_SCALE_CURRENT && mode != FP8_SCALE_DELAYED)
+    return fail(FP8_ERR_INVALID_ARG, "%s: unknown scaling mode %d", who, (int)mode);
+  const int64_t n = rows * cols;
+  if (n > 0 && q == nullptr && qT == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: no output", who);
+  if (!aligned16(x) || !aligned16(q) || !aligned16(qT))
+    return fail(FP8_ERR_ALIGNMENT, "%s: x, q_out and qT_out must be 16-byte aligned", who);
+  const bool contiguous = (ld == cols);
+  const bool tiled = (qT != nullptr) || gran != FP8_GRAN_TENSOR;
+  if (tiled && n > 0) {
+    if (cols % 8 != 0 || ld % 8 != 0 || rows % 8 != 0)
+      return fail(FP8_ERR_UNSUPPORTED, "%s: this layout needs rows, cols and ld multiples of 8", who);
+    if (qT != nullptr && rows % 16 != 0)
+      return fail(FP8_ERR_UNSUPPORTED, "%s: the transposed output needs rows %% 16 == 0", who);
+  }
+  const QuantState qs = to_qs(st);
+  cudaError_t e = cudaSuccess;
+
+  if (gran == FP8_GRAN_TENSOR) {
+    if ((s = check_state(st, mode, who)) != FP8_OK) return s;
+    if ((e = cudaMemsetAsync(st->amax_cur, 0, sizeof(float), stream)) != cudaSuccess) return cuda_fail(e, who);
+    if (n > 0) {
+      e = launch_amax(x, rows, cols, ld, st->amax_cur, mode == FP8_SCALE_DELAYED ? st->hist_count : nullptr, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "amax kernel");
+    }
+    if (!tiled || n == 0) {
+      if (!contiguous && n > 0 && q == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: no output", who);
+      e = launch_cast_flat(fmt, mode == FP8_SCALE_DELAYED, x, rows, cols, ld, q, qs, stream);
+    } else {
+      e = launch_cast_tiles(fmt, mode == FP8_SCALE_DELAYED ? 1 : 0, x, rows, cols, ld, q, qT, nullptr, qs, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "cast kernel");
+    return FP8_OK;
+  }
+
+  if (mode != FP8_SCALE_CURRENT)
+    return fail(FP8_ERR_UNSUPPORTED, "%s: tile and block scales support current scaling only", who);
+  if (unit_si == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: unit_scale_inv is required", who);
+  if (st != nullptr && st->amax_cur != nullptr) {
+    if ((e = cudaMemsetAsync(st->amax_cur, 0, sizeof(float), stream)) != cudaSuccess) return cuda_fail(e, who);
+  }
+  if (gran == FP8_GRAN_TILE_1x128) {
+    if (cols % 128 != 0) return fail(FP8_ERR_UNSUPPORTED, "%s: 1x128 tiles need cols %% 128 == 0", who);
+    if (qT != nullptr) return fail(FP8_ERR_UNSUPPORTED, "%s: 1x128 tiles write no transposed copy", who);
+    if (q == nullptr && n > 0) return fail(FP8_ERR_INVALID_ARG, "%s: q_out is required", who);
+    if (n == 0) return FP8_OK;
+    e = launch_cast_1x128(fmt, x, rows, cols, ld, q, unit_si, qs, stream);
+  } else {
+    if (rows % 128 != 0 || cols % 128 != 0)
+      return fail(FP8_ERR_UNSUPPORTED, "%s: 128x128 blocks need rows and cols multiples of 128", who);
+    if (n == 0) return FP8_OK;
+    e = launch_cast_tiles(fmt, 2, x, rows, cols, ld, q, qT, unit_si, qs, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "cast kernel");
+  return FP8_OK;
+}
+
+fp8_status_t scaled_mm_impl(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb, int64_t M, int64_t N,
+                            int64_t K, int64_t lda, int64_t ldb, fp8_gran_t gran, const float* sa, const float* sb,
+                            void* C, int64_t ldc, cudaStream_t stream) {
+  const char* who = "fp8_scaled_mm";
+  if (M < 0 || N < 0 || K < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
+  if ((fa != FP8_E4M3 && fa != FP8_E5M2) || (fb != FP8_E4M3 && fb != FP8_E5M2))
+    return fail(FP8_ERR_INVALID_ARG, "%s: unknown format", who);
+  if (gran != FP8_GRAN_TENSOR && gran != FP8_GRAN_BLOCK_128x128)
+    return fail(FP8_ERR_INVALID_ARG, "%s: granularity must be TENSOR or BLOCK_128x128", who);
+  if (M == 0 || N == 0) return FP8_OK;
+  if (C == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: null C", who);
+  if (ldc < N) return fail(FP8_ERR_INVALID_ARG, "%s: ldc < N", who);
+  if (!aligned16(C) || ldc % 8 != 0) return fail(FP8_ERR_ALIGNMENT, "%s: C must be 16-byte aligned, ldc %% 8 == 0", who);
+  if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31)) return fail(FP8_ERR_UNSUPPORTED, "%s: size >= 2^31", who);
+  if (K == 0) {
+    cudaError_t e = cudaMemset2DAsync(C, ldc * 2, 0, N * 2, M, stream);
+    return e == cudaSuccess ? FP8_OK : cuda_fail(e, who);
+  }
+  if (A == nullptr || B == nullptr || sa == nullptr || sb == nullptr)
+    return fail(FP8_ERR_INVALID_ARG, "%s: null A, B or scale", who);
+  if (lda < K || ldb < K) return fail(FP8_ERR_INVALID_ARG, "%s: lda or ldb < K", who);
+  if (!aligned16(A) || !aligned16(B) || lda % 16 != 0 || ldb % 16 != 0)
+    return fail(FP8_ERR_ALIGNMENT, "%s: A and B must be 16-byte aligned with lda, ldb multiples of 16", who);
+  if (gran == FP8_GRAN_BLOCK_128x128 && (K % 128 != 0 || N % 128 != 0))
+    return fail(FP8_ERR_UNSUPPORTED, "%s: block scaling needs K and N multiples of 128", who);
+  GemmArgs g{A, B, C, M, N, K, lda, ldb, ldc, (int)fa, (int)fb, sa, sb, gran == FP8_GRAN_BLOCK_128x128};
+  const char* why = "launch";
+  cudaError_t e = launch_gemm(g, stream, &why);
+  if (e != cudaSuccess) return cuda_fail(e, why);
+  return FP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8_status_t fp8_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld, fp8_format_t fmt,
+                          fp8_gran_t gran, fp8_scaling_t mode, const fp8_tensor_state_t* st, void* q_out,
+                          void* qT_out, float* unit_scale_inv, void* stream) {
+  return quantize_impl(x_bf16, rows, cols, ld, fmt, gran, mode, st, q_out, qT_out, unit_scale_inv,
+                       static_cast<cudaStream_t>(stream));
+}
+
+fp8_status_t fp8_scaled_mm(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb, int64_t M, int64_t N,
+                           int64_t K, int64_t lda, int64_t ldb, fp8_gran_t gran, const float* scale_inv_a,
+                           const float* scale_inv_b, void* C_bf16, int64_t ldc, void* stream) {
+  return scaled_mm_impl(A, fa, B, fb, M, N, K, lda, ldb, gran, scale_inv_a, scale_inv_b, C_bf16, ldc,
+                        static_cast<cudaStream_t>(stream));
+}
+
+fp8_status_t fp8_requantize_weights(const void* w_master_bf16, int64_t K, int64_t N, fp8_gran_t gran,
+                                    fp8_scaling_t mode, const fp8_tensor_state_t* st, void* wq_kn, void* wqT_nk,
+                                    float* block_scale_inv, void* stream) {
+  if (gran == FP8_GRAN_TILE_1x128)
+    return fail(FP8_ERR_INVALID_ARG, "fp8_requantize_weights: weights take TENSOR or BLOCK_128x128 scales");
+  if (wq_kn == nullptr && wqT_nk == nullptr && K * N > 0)
+    return fail(FP8_ERR_INVALID_ARG, "fp8_requantize_weights: no output");
+  return quantize_impl(w_master_bf16, K, N, N, FP8_E4M3, gran, mode, st, wq_kn, wqT_nk, block_scale_inv,
+                       static_cast<cudaStream_t>(stream));
+}
+
+fp8_status_t fp8_linear_fwd(const void* x_bf16, int64_t M, int64_t K, int64_t N, const void* wqT_nk,
+                            const fp8_tensor_state_t* w_st, const float* w_block_scale_inv,
+                            const fp8_tensor_state_t* x_st, fp8_gran_t gran, fp8_scaling_t mode, void* xq_save,
+                            void* xqT_save, float* x_tile_scale_inv, void* y_bf16, void* stream) {
+  const char* who = "fp8_linear_fwd";
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M < 0 || K < 0 || N < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
+  if (xq_save == nullptr || y_bf16 == nullptr || wqT_nk == nullptr)
+    return fail(FP8_ERR_INVALID_ARG, "%s: xq_save, y and wqT are required", who);
+  fp8_status_t st;
+  if (gran == FP8_GRAN_TENSOR) {
+    if (w_st == nullptr || w_st->scale_inv == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: w_st->scale_inv is required", who);
+    if (x_st == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: x_st is required", who);
+    st = quantize_impl(x_bf16, M, K, K, FP8_E4M3, FP8_GRAN_TENSOR, mode, x_st, xq_save, xqT_save, nullptr, s);
+    if (st != FP8_OK) return st;
+    return scaled_mm_impl(xq_save, FP8_E4M3, wqT_nk, FP8_E4M3, M, N, K, K, K, FP8_GRAN_TENSOR, x_st->scale_inv,
+                          w_st->scale_inv, y_bf16, N, s);
+  }
+  if (gran == FP8_GRAN_BLOCK_128x128) {
+    if (mode != FP8_SCALE_CURRENT) return fail(FP8_ERR_UNSUPPORTED, "%s: block scaling uses current scaling", who);
+    if (xqT_save != nullptr) return fail(FP8_ERR_UNSUPPORTED, "%s: no transposed copy with 1x128 tiles", who);
+    if (w_block_scale_inv == nullptr || x_tile_scale_inv == nullptr)
+      return fail(FP8_ERR_INVALID_ARG, "%s: block scaling needs w_block_scale_inv and x_tile_scale_inv", who);
+    st = quantize_impl(x_bf16, M, K, K, FP8_E4M3, FP8_GRAN_TILE_1x128, FP8_SCALE_CURRENT, x_st, xq_save, nullptr,
+                       x_tile_scale_inv, s);
+    if (st != FP8_OK) return st;
+    return scaled_mm_impl(xq_save, FP8_E4M3, wqT_nk, FP8_E4M3, M, N, K, K, K, FP8_GRAN_BLOCK_128x128,
+                          x_tile_scale_inv, w_block_scale_inv, y_bf16, N, s);
+  }
+  return fail(FP8_ERR_INVALID_ARG, "%s: granularity must be TENSOR or BLOCK_128x128", who);
+}
+
+fp8_status_t fp8_linear_bwd(const void* dy_bf16, int64_t M, int64_t K, int64_t N, const void* xqT_save,
+                            const fp8_tensor_state_t* x_st, const void* wq_kn, const fp8_tensor_state_t* w_st,
+                            fp8_tensor_state_t* dy_st, fp8_scaling_t mode, void* dyq_ws, void* dyqT_ws, void* dx_bf16,
+                            void* dw_bf16, void* stream) {
+  const char* who = "fp8_linear_bwd";
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M < 0 || K < 0 || N < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
+  if (M % 16 || K % 16 || N % 16) return fail(FP8_ERR_UNSUPPORTED, "%s: M, K and N must be multiples of 16", who);
+  if (dyq_ws == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: dyq_ws is required", who);
+  if (dw_bf16 != nullptr && (dyqT_ws == nullptr || xqT_save == nullptr || x_st == nullptr || !x_st->scale_inv))
+    return fail(FP8_ERR_INVALID_ARG, "%s: wgrad needs dyqT_ws, xqT_save and x_st", who);
+  if (dx_bf16 != nullptr && (wq_kn == nullptr || w_st == nullptr || !w_st->scale_inv))
+    return fail(FP8_ERR_INVALID_ARG, "%s: dgrad needs wq_kn and w_st", who);
+  fp8_status_t st = quantize_impl(dy_bf16, M, N, N, FP8_E5M2, FP8_GRAN_TENSOR, mode, dy_st, dyq_ws,
+                                  dw_bf16 != nullptr ? dyqT_ws : nullptr, nullptr, s);
+  if (st != FP8_OK) return st;
+  if (dx_bf16 != nullptr) {
+    st = scaled_mm_impl(dyq_ws, FP8_E5M2, wq_kn, FP8_E4M3, M, K, N, N, N, FP8_GRAN_TENSOR, dy_st->scale_inv,
+                        w_st->scale_inv, dx_bf16, K, s);
+    if (st != FP8_OK) return st;
+  }
+  if (dw_bf16 != nullptr) {
+    st = scaled_mm_impl(xqT_save, FP8_E4M3, dyqT_ws, FP8_E5M2, K, N, M, M, M, FP8_GRAN_TENSOR, x_st->scale_inv,
+                        dy_st->scale_inv, dw_bf16, N, s);
+    if (st != FP8_OK) return st;
+  }
+  return FP8_OK;
+}
+
+fp8_status_t fp8_history_commit(const fp8_tensor_state_t* st, void* stream) {
+  if (st == nullptr || !st->amax_history || !st->hist_count || !st->amax_cur || st->hist_len <= 0)
+    return fail(FP8_ERR_INVALID_ARG, "fp8_history_commit: needs amax_history, hist_count, amax_cur, hist_len > 0");
+  cudaError_t e = launch_history_commit(to_qs(st), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FP8_OK : cuda_fail(e, "fp8_history_commit");
+}
+
+fp8_status_t fp8_poll_device_error(void) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_poll_device_error");
+  uint32_t v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_error_word, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_poll_device_error");
+  if (v == 0) return FP8_OK;
+  const uint32_t zero = 0;
+  cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(zero));
+  return fail(FP8_ERR_TIMEOUT, "a bounded wait ran out (device error bits 0x%x)", v);
+}
+
+fp8_status_t fp8_set_wait_limit_ns(unsigned long long ns) {
+  if (ns == 0) return fail(FP8_ERR_INVALID_ARG, "fp8_set_wait_limit_ns: limit must be > 0");
+  g_wait_limit_ns.store(ns);
+  return FP8_OK;
+}
+
+fp8_status_t fp8_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
+  WaitCtl w = wait_ctl();
+  if (w.err == nullptr) return fail(FP8_ERR_CUDA, "fp8_selftest_wait_timeout: no device error word");
+  w.limit_ns = limit_ns;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_selftest_wait(w, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_selftest_wait_timeout");
+  uint32_t v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_error_word, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "fp8_selftest_wait_timeout");
+  const uint32_t zero = 0;
+  cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(zero));
+  if (v & DEV_ERR_WAIT_SELFTEST) return fail(FP8_ERR_TIMEOUT, "self-test wait ran out as intended");
+  return fail(FP8_ERR_CUDA, "self-test wait did not report a timeout (bits 0x%x)", v);
+}
+
+fp8_status_t fp8_get_last_error_detail(char* buf, size_t n) {
+  if (buf != nullptr && n > 0) {
+    strncpy(buf, g_detail, n - 1);
+    buf[n - 1] = '\0';
+  }
+  return FP8_OK;
+}
+
+const char* fp8_status_string(fp8_status_t s) {
+  switch (s) {
+    case FP8_OK: return "FP8_OK";
+    case FP8_ERR_INVALID_ARG: return "FP8_ERR_INVALID_ARG";
+    case FP8_ERR_UNSUPPORTED: return "FP8_ERR_UNSUPPORTED";
+    case FP8_ERR_ALIGNMENT: return "FP8_ERR_ALIGNMENT";
+    case FP8_ERR_CUDA: return "FP8_ERR_CUDA";
+    case FP8_ERR_TIMEOUT: return "FP8_ERR_TIMEOUT";
+  }
+  return "FP8_ERR_UNKNOWN";
+}
+
+}  // extern "C"

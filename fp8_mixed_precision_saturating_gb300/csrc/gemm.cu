@@ -1,0 +1,444 @@
+// gemm.cu -- FP8 x FP8 -> bf16 GEMM on the sm_103a tensor cores (tcgen05, kind::f8f6f4).
+//
+// Source: "#84 FP8 Precision" page, "Explanation": the scaled FP8 matmul of the forward
+// pass, with one scale per operand and both operands contiguous along the contraction
+// dimension; "Hardware precision": FP8 tensor cores. "FP8 stability guardrails" page,
+// "Real products, models, and research": fine-grained 1x128 tile / 128x128 block scaling.
+//
+//   C[m, n] = bf16( d_a * d_b * sum_k A[m, k] B[n, k] )                    (per tensor)
+//   C[m, n] = bf16( sum_kb d_a[m, kb] d_b[kb, n/128] sum_{k in kb} A B )  (block scaled)
+//
+// Design (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0      one thread issues TMA loads of A [128 x 128] and B [256 x 128] (K-major,
+//               128-byte swizzle) into a 4-stage shared-memory ring;
+//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma (M=128, N=256,
+//               K=32) into a TMEM accumulator and frees ring slots with tcgen05.commit;
+//   warps 2..   epilogue: tcgen05.ld of the accumulator (each warp owns the 32 TMEM lanes
+//               its warp index selects), multiply by the scales, convert to bf16, stage
+//               128-byte rows through swizzled shared memory and write them with TMA.
+// Per tensor: two 256-column accumulators, so the epilogue of one tile overlaps the
+// mainloop of the next. Block scaled: every 128-deep K block gets a fresh accumulator
+// buffer (two, alternating), and 8 epilogue warps fold each block into fp32 registers
+// with its scale product before the next block lands.
+// Every mbarrier wait is bounded (see ptx.cuh); on a timeout the CTA stops issuing work,
+// drains what it issued and frees its TMEM.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fp8gb {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STG_BYTES = 32 * 128;  // one staging buffer: 32 rows x 64 bf16
+constexpr int GROUP_M = 16;          // tile raster: 16 M-blocks share each B tile
+constexpr uint32_t TMEM_COLS = 512;
+
+template <bool BLOCK>
+struct Cfg {
+  static constexpr int EPI_WARPS = BLOCK ? 8 : 4;
+  static constexpr int STG_PER_WARP = BLOCK ? 1 : 2;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int OFF_STG = STAGES * STAGE_BYTES;
+  static constexpr int OFF_BAR = OFF_STG + EPI_WARPS * STG_PER_WARP * STG_BYTES;
+  // full[S], empty[S], tfull[2], tempty[2], final
+  static constexpr int NBAR = 2 * STAGES + 5;
+  static constexpr int OFF_TMEM_SLOT = OFF_BAR + 8 * NBAR;
+  static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;  // + alignment slack
+};
+
+struct KParams {
+  int M, N, K;
+  int num_m, num_n, num_kb, num_tiles;
+  uint32_t idesc;
+  const float* sa;
+  const float* sb;
+  int sa_ld, sb_ld;
+  WaitCtl w;
+};
+
+__device__ __forceinline__ void tile_coords(int t, const KParams& p, int& mb, int& nb) {
+  const int per_group = GROUP_M * p.num_n;
+  const int g = t / per_group;
+  const int first_m = g * GROUP_M;
+  const int gsize = min(GROUP_M, p.num_m - first_m);
+  const int local = t - g * per_group;
+  mb = first_m + local % gsize;
+  nb = local / gsize;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Wait that ignores the error word (used only to drain work already issued).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// Stage 32 rows x 64 bf16 (this lane's row = 32 packed words) into a 128-byte-swizzled
+// buffer and store it with TMA at (c0, r0). Called by all 32 lanes of the warp.
+__device__ __forceinline__ void stage_and_store(uint8_t* stg, const uint32_t (&pk)[32], int lane,
+                                                const CUtensorMap* tmC, int c0, int r0) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) * 16)) =
+        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmC, smem_u32(stg), c0, r0);
+    bulk_commit_group();
+  }
+}
+
+template <bool BLOCK>
+__global__ void __launch_bounds__(Cfg<BLOCK>::THREADS, 1)
+    gemm_f8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const KParams p) {
+  using C = Cfg<BLOCK>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar_full = sbase + C::OFF_BAR;
+  const uint32_t bar_empty = bar_full + 8 * STAGES;
+  const uint32_t bar_tfull = bar_empty + 8 * STAGES;
+  const uint32_t bar_tempty = bar_tfull + 16;
+  const uint32_t bar_final = bar_tempty + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tempty + 8 * a, C::EPI_WARPS);
+    }
+    mbar_init(bar_final, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_phase = 0;  // per stage: issued?, parity of last issue
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, p, mb, nb);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.w, DEV_ERR_WAIT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full + 8 * stage;
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          tma_load_2d(sa, &tmA, fb, kb * BK, mb * BM);
+          tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, nb * BN);
+          issued_mask |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let every load already issued land before the CTA exits
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_mask & (1u << s)) mbar_wait_drain(bar_full + 8 * s, (issued_phase >> s) & 1u, 1000000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        if (!BLOCK) {
+          if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.w, DEV_ERR_WAIT_MMA)) break;
+          tc_fence_after();
+        }
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (BLOCK) {
+            if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.w, DEV_ERR_WAIT_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          if (!mbar_wait(bar_full + 8 * stage, phase, p.w, DEV_ERR_WAIT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          const uint64_t adesc = smem_desc_sw128(sa);
+          const uint64_t bdesc = smem_desc_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k) {
+            const uint32_t accumulate = BLOCK ? (k != 0) : ((kb | k) != 0);
+            mma_f8(d, adesc + 2 * k, bdesc + 2 * k, p.idesc, accumulate);
+          }
+          mma_commit(bar_empty + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (BLOCK) {
+            mma_commit(bar_tfull + 8 * acc);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+          }
+        }
+        if (!BLOCK && ok) {
+          mma_commit(bar_tfull + 8 * acc);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        }
+      }
+      // every MMA this thread issued has completed once this barrier flips
+      mma_commit(bar_final);
+      if (!mbar_wait_drain(bar_final, 0, 1000000000ull)) atomicOr(p.w.err, DEV_ERR_WAIT_TEARDOWN);
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int ew = warp - 2;             // 0 .. EPI_WARPS-1
+    const int q = warp & 3;              // TMEM lane quarter this warp may read
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    uint8_t* stg = smem + C::OFF_STG + ew * C::STG_PER_WARP * STG_BYTES;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    if constexpr (!BLOCK) {
+      const float dd = __fmul_rn(__ldg(p.sa), __ldg(p.sb));
+      int buf = 0;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, p, mb, nb);
+        if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE)) break;
+        __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the spin
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 64; ++ch) {
+          __syncwarp();
+          uint32_t r0[32], r1[32];
+          const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + ch * 64);
+          tmem_ld32(taddr, r0);
+          tmem_ld32(taddr + 32, r1);
+          tmem_ld_wait();
+          reg_fence(r0);
+          reg_fence(r1);
+          if (ch == BN / 64 - 1) {  // accumulator fully read: hand it back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+          }
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            pk[j] = pack_bf16x2(__fmul_rn(__uint_as_float(r0[2 * j]), dd), __fmul_rn(__uint_as_float(r0[2 * j + 1]), dd));
+            pk[16 + j] =
+                pack_bf16x2(__fmul_rn(__uint_as_float(r1[2 * j]), dd), __fmul_rn(__uint_as_float(r1[2 * j + 1]), dd));
+          }
+          if (lane == 0) bulk_wait_group_read<1>();  // the store that used this buffer has read it
+          __syncwarp();
+          stage_and_store(stg + buf * STG_BYTES, pk, lane, &tmC, nb * BN + ch * 64, mb * BM + q * 32);
+          buf ^= 1;
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+    } else {
+      const int h = ew >> 2;  // which 128-column half of the tile this warp folds
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, p, mb, nb);
+        const int row = mb * BM + q * 32 + lane;
+        const int nblk = nb * (BN / 128) + h;
+        const bool row_ok = row < p.M;
+        const bool col_ok = nblk * 128 < p.N;
+        float accum[128];
+#pragma unroll
+        for (int j = 0; j < 128; ++j) accum[j] = 0.0f;
+        float sa_next = row_ok ? __ldg(p.sa + (int64_t)row * p.sa_ld) : 0.0f;
+        float sb_next = col_ok ? __ldg(p.sb + nblk) : 0.0f;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          const float sc = __fmul_rn(sa_next, sb_next);
+          if (kb + 1 < p.num_kb) {
+            sa_next = row_ok ? __ldg(p.sa + (int64_t)row * p.sa_ld + kb + 1) : 0.0f;
+            sb_next = col_ok ? __ldg(p.sb + (int64_t)(kb + 1) * p.sb_ld + nblk) : 0.0f;
+          }
+          if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE)) {
+            ok = false;
+            break;
+          }
+          __syncwarp();
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + h * 128);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld32(taddr + 32 * c, r);
+            tmem_ld_wait();
+            reg_fence(r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) accum[32 * c + j] = fmaf(__uint_as_float(r[j]), sc, accum[32 * c + j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(accum[64 * ch + 2 * j], accum[64 * ch + 2 * j + 1]);
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+          stage_and_store(stg, pk, lane, &tmC, nb * BN + h * 128 + ch * 64, mb * BM + q * 32);
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t inner, uint64_t outer,
+              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool BLOCK>
+cudaError_t prepare_kernel() {
+  // the attribute is per device; remember which devices were configured
+  static bool done[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(gemm_f8_kernel<BLOCK>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BLOCK>::SMEM);
+  if (e == cudaSuccess && dev < 64) done[dev] = true;
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why) {
+  CUtensorMap ta, tb, tc;
+  if (!make_map(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.M, g.lda, BK, BM) ||
+      !make_map(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.N, g.ldb, BK, BN) ||
+      !make_map(&tc, g.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.N, g.M, g.ldc * 2, 64, 32)) {
+    *why = "cuTensorMapEncodeTiled failed (driver entry point missing or tensor map rejected)";
+    return cudaErrorInvalidValue;
+  }
+  KParams p;
+  p.M = static_cast<int>(g.M);
+  p.N = static_cast<int>(g.N);
+  p.K = static_cast<int>(g.K);
+  p.num_m = static_cast<int>((g.M + BM - 1) / BM);
+  p.num_n = static_cast<int>((g.N + BN - 1) / BN);
+  p.num_kb = static_cast<int>((g.K + BK - 1) / BK);
+  p.num_tiles = p.num_m * p.num_n;
+  p.idesc = idesc_f8(static_cast<uint32_t>(g.fa), static_cast<uint32_t>(g.fb), BM, BN);
+  p.sa = g.sa;
+  p.sb = g.sb;
+  p.sa_ld = static_cast<int>(g.K / 128);
+  p.sb_ld = static_cast<int>(g.N / 128);
+  p.w = wait_ctl();
+  if (p.w.err == nullptr) {
+    *why = "device error word unavailable";
+    return cudaErrorInvalidDevice;
+  }
+  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  cudaError_t e;
+  if (g.block_scaled) {
+    e = prepare_kernel<true>();
+    if (e != cudaSuccess) return e;
+    gemm_f8_kernel<true><<<grid, Cfg<true>::THREADS, Cfg<true>::SMEM, stream>>>(ta, tb, tc, p);
+  } else {
+    e = prepare_kernel<false>();
+    if (e != cudaSuccess) return e;
+    gemm_f8_kernel<false><<<grid, Cfg<false>::THREADS, Cfg<false>::SMEM, stream>>>(ta, tb, tc, p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fp8gb

@@ -1,0 +1,56 @@
+// kernels.h -- internal interface between the C ABI (api.cu) and the kernel launchers.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fp8gb {
+
+// Device pointers of one tensor role's scaling state (see fp8_tensor_state_t).
+struct QuantState {
+  float* hist;
+  int32_t* hist_count;
+  float* scale;
+  float* scale_inv;
+  float* amax_cur;
+  unsigned long long* counters;
+  int32_t hist_len;
+};
+
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms();
+
+// Device error word and wait limit for launches on the current device.
+WaitCtl wait_ctl();
+
+cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* amax_out,
+                        const int32_t* gate_count, cudaStream_t stream);
+cudaError_t launch_cast_flat(int fmt, bool delayed, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
+                             const QuantState& st, cudaStream_t stream);
+// scale_kind: 0 per-tensor current, 1 per-tensor delayed, 2 per 128x128 block.
+cudaError_t launch_cast_tiles(int fmt, int scale_kind, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
+                              void* qT, float* unit_scale_inv, const QuantState& st, cudaStream_t stream);
+cudaError_t launch_cast_1x128(int fmt, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
+                              float* unit_scale_inv, const QuantState& st, cudaStream_t stream);
+cudaError_t launch_history_commit(const QuantState& st, cudaStream_t stream);
+cudaError_t launch_selftest_wait(const WaitCtl& w, cudaStream_t stream);
+
+// GEMM: C [M,N] bf16 = A [M,K] * B [N,K]^T with per-tensor (block_scaled = false: sa, sb
+// point to one fp32 each) or fine-grained scales (block_scaled = true: sa [M, K/128],
+// sb [K/128, N/128]).
+struct GemmArgs {
+  const void* A;
+  const void* B;
+  void* C;
+  int64_t M, N, K, lda, ldb, ldc;
+  int fa, fb;
+  const float* sa;
+  const float* sb;
+  bool block_scaled;
+};
+// Returns cudaSuccess, or an error; `why` receives a static message for host-side failures.
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why);
+
+}  // namespace fp8gb

@@ -1,0 +1,212 @@
+/*
+ * fp8gb.h -- C ABI of the GB300 (sm_103a) FP8 up-projection library.
+ *
+ * The library implements FP8 training's quantise-then-scaled-matmul for a transformer
+ * MLP up-projection y = x W (x [M,K], W [K,N], row-major bf16):
+ *   - amax reductions that produce scales (per tensor, per 1x128 row tile, per 128x128
+ *     block, or from an amax history for delayed scaling),
+ *   - a saturating round-to-nearest-even cast of bf16 to E4M3 (max 448; forward
+ *     activations and weights) or E5M2 (max 57344; gradients), with overflow and
+ *     underflow counters,
+ *   - FP8 x FP8 GEMMs on the tcgen05 tensor cores with fp32 accumulation and an epilogue
+ *     that multiplies by the operands' inverse scales and writes bf16,
+ *   - the forward, dgrad and wgrad compositions and the FP8 weight cache refresh.
+ *
+ * Sources (three web pages on FP8 mixed-precision training):
+ *   [GUARD]  "FP8 stability guardrails" page (zenaique): section "Why FP8 is tempting and
+ *            why it is fragile" (format maxima, overflow / saturation, underflow);
+ *            "Real products, models, and research" (fine-grained tile / block scaling,
+ *            delayed scaling with amax history); "What an interviewer would ask next"
+ *            (E4M3 and E5M2 in one run).
+ *   [SPEED]  "#84 FP8 Precision" speedrun page (bubblnet): "Explanation" (weights divided
+ *            by a scale before the E4M3 cast; a scaled matmul with per-operand scales;
+ *            operands laid out contiguous along the contraction), "Hardware precision"
+ *            (bf16 master weights in the optimizer, FP8 compute copy re-quantised after
+ *            every optimizer step; FP8 only for the MLP up-projection).
+ *
+ * Conventions for every entry point:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; the library keeps no
+ *     pointer after a call returns and allocates no device memory in any call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). All
+ *     work is enqueued on it; no call synchronises the host except where stated.
+ *   - Scales, amaxes and counters stay on the device (fp8_tensor_state_t), so a call
+ *     never reads a device value back to the host.
+ *   - Arguments are validated before anything is enqueued: null pointers, negative
+ *     sizes, bad enums -> FP8_ERR_INVALID_ARG; shapes the kernels do not handle ->
+ *     FP8_ERR_UNSUPPORTED; pointers or leading dimensions that break the 16-byte rule of
+ *     the tensor-memory-accelerator copies -> FP8_ERR_ALIGNMENT. A CUDA error reported
+ *     after a launch -> FP8_ERR_CUDA. fp8_get_last_error_detail() gives a message.
+ *   - Matrices are row-major with a leading dimension `ld` (elements between rows).
+ *   - Codes are stored one byte per element (uint8), as the formats' bit patterns.
+ *   - No C++ exception crosses the boundary. There is no CPU fallback: without a
+ *     suitable GPU every compute entry point returns FP8_ERR_CUDA or FP8_ERR_UNSUPPORTED.
+ *   - Thread safety: calls are stateless apart from the caller's state structs and the
+ *     per-thread error message; concurrent calls on different streams are safe when they
+ *     touch disjoint caller buffers.
+ */
+#ifndef FP8GB_H
+#define FP8GB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP8_OK = 0,
+  FP8_ERR_INVALID_ARG = 1,
+  FP8_ERR_UNSUPPORTED = 2,
+  FP8_ERR_ALIGNMENT = 3,
+  FP8_ERR_CUDA = 4,
+  FP8_ERR_TIMEOUT = 5
+} fp8_status_t;
+
+/* [GUARD] "Why FP8 is tempting...": E4M3 (4 exponent, 3 mantissa bits, max 448) and
+ * E5M2 (5 exponent, 2 mantissa bits, max 57344). */
+typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format_t;
+
+/* [GUARD] "Real products...": per-tensor, fine-grained 1x128 tiles (one scale per row
+ * and 128 consecutive columns) and 128x128 blocks. */
+typedef enum { FP8_GRAN_TENSOR = 0, FP8_GRAN_TILE_1x128 = 1, FP8_GRAN_BLOCK_128x128 = 2 } fp8_gran_t;
+
+/* Current scaling takes the scale from this tensor's own amax; delayed scaling takes it
+ * from the maximum of an amax history ([GUARD] "Real products...": delayed scaling with
+ * amax history tracking). */
+typedef enum { FP8_SCALE_CURRENT = 0, FP8_SCALE_DELAYED = 1 } fp8_scaling_t;
+
+/* Scaling state of one tensor role (x, W or dy of one layer). Every pointer is caller-
+ * owned device memory; zero-initialise amax_history, hist_count and counters once.
+ *   amax_history [hist_len] fp32  ring of past amaxes (delayed scaling)
+ *   hist_count   int32            number of amaxes pushed so far; the next push goes to
+ *                                 amax_history[hist_count % hist_len]
+ *   scale        fp32             s = FP8_MAX / amax_eff of the most recent cast
+ *   scale_inv    fp32             d = amax_eff / FP8_MAX (what the GEMM multiplies by)
+ *   amax_cur     fp32             max |x| of the tensor of the most recent cast
+ *   counters     uint64 [2]       [0] saturated elements, [1] non-zero elements flushed to
+ *                                 zero; both accumulate until the caller clears them
+ * If amax_eff is zero or not finite, s = d = 1. */
+typedef struct {
+  float* amax_history;
+  int32_t* hist_count;
+  float* scale;
+  float* scale_inv;
+  float* amax_cur;
+  unsigned long long* counters;
+  int32_t hist_len;
+} fp8_tensor_state_t;
+
+/* Quantise a bf16 matrix x [rows, cols] (leading dimension ld) to FP8 codes.
+ *  [GUARD] "Why FP8 is tempting...": cast with saturation at +-FP8_MAX, round to nearest
+ *  even, NaN -> 0x7F, sign of zero kept; [SPEED] "Explanation": the tensor is divided by
+ *  its scale (multiplied by s = FP8_MAX / amax) before the cast.
+ *  gran = FP8_GRAN_TENSOR: one scale for the whole tensor, from x's own amax (mode
+ *    CURRENT; two passes over x) or from st's history (mode DELAYED; bootstrap with the
+ *    current amax while hist_count == 0). `st` is required; the call writes st->amax_cur,
+ *    st->scale, st->scale_inv and adds to st->counters. `unit_scale_inv` is ignored.
+ *  gran = FP8_GRAN_TILE_1x128: cols % 128 == 0; one scale per (row, 128 columns), the
+ *    inverse scales written to unit_scale_inv [rows, cols/128] (fp32, row-major). Mode
+ *    must be CURRENT. `st` may be NULL; if given, st->amax_cur receives the tensor amax and
+ *    the counters accumulate.
+ *  gran = FP8_GRAN_BLOCK_128x128: rows % 128 == 0 and cols % 128 == 0; one scale per
+ *    128x128 block, inverse scales in unit_scale_inv [rows/128, cols/128]. Mode CURRENT;
+ *    `st` as for tiles.
+ *  q_out [rows, cols] (leading dimension cols) receives the codes; may be NULL when
+ *    qT_out is given. qT_out [cols, rows] (leading dimension rows) receives the transposed
+ *    codes, or is NULL. With qT_out, rows % 16 == 0. With q_out and a GEMM consumer,
+ *    cols % 16 == 0 is needed by the GEMM, not by this call.
+ *  Alignment: x, q_out and qT_out 16-byte aligned; ld % 8 == 0 unless ld == cols. */
+fp8_status_t fp8_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld,
+                          fp8_format_t fmt, fp8_gran_t gran, fp8_scaling_t mode,
+                          const fp8_tensor_state_t* st, void* q_out, void* qT_out,
+                          float* unit_scale_inv, void* stream);
+
+/* C [M,N] (bf16, leading dimension ldc) = dequantised A [M,K] times B [N,K] transposed:
+ *   C_ij = bf16_rne( d_a * d_b * sum_k a_ik b_jk ),  fp32 accumulation.
+ *  [SPEED] "Explanation": the scaled FP8 matmul with one scale per operand, both operands
+ *  contiguous along the contraction dimension K (A row-major [M,K] with lda, B row-major
+ *  [N,K] with ldb). fa / fb: the codes' formats (any combination).
+ *  gran = FP8_GRAN_TENSOR: scale_inv_a and scale_inv_b point to one fp32 each (device).
+ *  gran = FP8_GRAN_BLOCK_128x128: [GUARD] "Real products...": fine-grained scaling; A has
+ *    1x128 tile scales scale_inv_a [M, K/128], B has 128x128 block scales
+ *    scale_inv_b [K/128, N/128] (indexed [k/128][n/128]); each 128-deep K block is
+ *    accumulated separately and added as C_ij += d_a[i,kb] * d_b[kb, j/128] * P_ij,kb.
+ *    Requires K % 128 == 0 and N % 128 == 0.
+ *  Any M, N >= 0 and K >= 0 (K == 0 writes zeros). A, B, C 16-byte aligned; lda and ldb
+ *  multiples of 16, ldc a multiple of 8. */
+fp8_status_t fp8_scaled_mm(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb,
+                           int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                           fp8_gran_t gran, const float* scale_inv_a, const float* scale_inv_b,
+                           void* C_bf16, int64_t ldc, void* stream);
+
+/* Refresh the FP8 weight cache from the bf16 master weight W [K,N] (contiguous).
+ *  [SPEED] "Hardware precision": after each optimizer step the bf16 master weights are
+ *  re-quantised to E4M3 and cached for the next forward. One pass over W writes
+ *  wq_kn [K,N] (for dgrad) and/or wqT_nk [N,K] (for the forward); either may be NULL but
+ *  not both. gran TENSOR (st required; CURRENT or DELAYED: delayed scaling uses the
+ *  history before this call's amax is pushed) or BLOCK_128x128 (block_scale_inv
+ *  [K/128, N/128]). Same rules as fp8_quantize. */
+fp8_status_t fp8_requantize_weights(const void* w_master_bf16, int64_t K, int64_t N,
+                                    fp8_gran_t gran, fp8_scaling_t mode,
+                                    const fp8_tensor_state_t* st, void* wq_kn, void* wqT_nk,
+                                    float* block_scale_inv, void* stream);
+
+/* Forward of the FP8 up-projection: y [M,N] = x [M,K] W [K,N].
+ *  Quantises x to E4M3 (per tensor into xq_save [M,K] with x_st, or per 1x128 tile into
+ *  xq_save with x_tile_scale_inv [M, K/128]) and runs the scaled GEMM against the cached
+ *  wqT_nk [N,K]. gran TENSOR uses w_st->scale_inv; gran BLOCK_128x128 (1x128 x tiles,
+ *  128x128 W blocks) uses w_block_scale_inv [K/128, N/128] and requires mode CURRENT.
+ *  xqT_save [K,M] (nullable, gran TENSOR only) keeps the transposed codes for wgrad.
+ *  x contiguous; K % 16 == 0 (K % 128 == 0 for gran BLOCK); M % 16 == 0 with xqT_save.
+ *  x_st is required for gran TENSOR and optional otherwise. */
+fp8_status_t fp8_linear_fwd(const void* x_bf16, int64_t M, int64_t K, int64_t N,
+                            const void* wqT_nk, const fp8_tensor_state_t* w_st,
+                            const float* w_block_scale_inv, const fp8_tensor_state_t* x_st,
+                            fp8_gran_t gran, fp8_scaling_t mode, void* xq_save, void* xqT_save,
+                            float* x_tile_scale_inv, void* y_bf16, void* stream);
+
+/* Backward of the FP8 up-projection (per-tensor scales).
+ *  [GUARD] "What an interviewer would ask next": the backward signal dy [M,N] is cast to
+ *  E5M2 for its range (per tensor, with dy_st, mode CURRENT or DELAYED) into the caller's
+ *  scratch dyq_ws [M,N] and dyqT_ws [N,M], then
+ *    dgrad  dx [M,K] = d_dy d_w  dyq  wq_kn^T      (contraction over N; wq_kn [K,N])
+ *    wgrad  dW [K,N] = d_x  d_dy xqT_save dyqT_ws^T (contraction over M; xqT_save [K,M])
+ *  dx and dw may each be NULL (that GEMM is skipped; dyqT_ws may then be NULL when dw is).
+ *  Needs M, N, K multiples of 16. dy contiguous. */
+fp8_status_t fp8_linear_bwd(const void* dy_bf16, int64_t M, int64_t K, int64_t N,
+                            const void* xqT_save, const fp8_tensor_state_t* x_st,
+                            const void* wq_kn, const fp8_tensor_state_t* w_st,
+                            fp8_tensor_state_t* dy_st, fp8_scaling_t mode,
+                            void* dyq_ws, void* dyqT_ws, void* dx_bf16, void* dw_bf16,
+                            void* stream);
+
+/* Push st->amax_cur into the history: amax_history[hist_count % hist_len] = amax_cur;
+ * hist_count += 1. [GUARD] "Real products...": amax history tracking. */
+fp8_status_t fp8_history_commit(const fp8_tensor_state_t* st, void* stream);
+
+/* Device-side error word. Every wait inside a kernel is bounded; a wait that runs out
+ * sets a bit in this word and its kernel returns early (its outputs are then undefined).
+ * fp8_poll_device_error synchronises the current device, returns FP8_ERR_TIMEOUT if any
+ * wait ran out since the last clear (and clears the word), else FP8_OK. */
+fp8_status_t fp8_poll_device_error(void);
+
+/* Limit in nanoseconds for every bounded wait in later launches (default 4e9 ns). */
+fp8_status_t fp8_set_wait_limit_ns(unsigned long long ns);
+
+/* Self-test of the bounded wait: launches one kernel whose thread waits on a barrier
+ * that nothing completes, for at most limit_ns; then synchronises the stream and returns
+ * FP8_ERR_TIMEOUT (the expected result) with the device word cleared again. */
+fp8_status_t fp8_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
+/* Copy the message of the last failed call on this thread into buf (at most n bytes,
+ * NUL-terminated). Returns FP8_OK. */
+fp8_status_t fp8_get_last_error_detail(char* buf, size_t n);
+
+/* Static name of a status code. */
+const char* fp8_status_string(fp8_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8GB_H */
