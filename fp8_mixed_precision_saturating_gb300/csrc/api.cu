@@ -127,7 +127,9 @@ fp8_status_t quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld
     return fail(FP8_ERR_ALIGNMENT, "%s: x, q_out and qT_out must be 16-byte aligned", who);
   const bool contiguous = (ld == cols);
   const bool tiled = (qT != nullptr) || gran != FP8_GRAN_TENSOR;
-  if (tiled && n > 0) {
+  if (gran == FP8_GRAN_TILE_1x128 && n > 0 && ld % 8 != 0)
+    return fail(FP8_ERR_UNSUPPORTED, "%s: 1x128 tiles need ld %% 8 == 0", who);
+  if (tiled && gran != FP8_GRAN_TILE_1x128 && n > 0) {
     if (cols % 8 != 0 || ld % 8 != 0 || rows % 8 != 0)
       return fail(FP8_ERR_UNSUPPORTED, "%s: this layout needs rows, cols and ld multiples of 8", who);
     if (qT != nullptr && rows % 16 != 0)

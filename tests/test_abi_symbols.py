@@ -18,9 +18,9 @@ def declared_functions():
 
 @pytest.fixture(scope="module")
 def libpath():
-    from fp8_mixed_precision_saturating_gb300 import _build
+    import __graft_entry__
     try:
-        return _build.build()
+        return __graft_entry__._build_module().build()
     except RuntimeError as e:
         pytest.skip(f"no CUDA toolkit to build with: {e}")
 

@@ -37,9 +37,9 @@ def rand_codes(rng, shape, fmt, spread=1.0):
 def run_mm(g, A, fa, B, fb, da, db, lda=None, ldb=None, ldc=None):
     M, K = A.shape
     N = B.shape[0]
-    lda = lda or K
-    ldb = ldb or K
-    ldc = ldc or N
+    lda = lda or -(-K // 16) * 16
+    ldb = ldb or -(-K // 16) * 16
+    ldc = ldc or -(-N // 8) * 8
     Ad = torch.zeros(M, lda, dtype=torch.uint8, device="cuda")
     Ad[:, :K] = dev_u8(A)
     Bd = torch.zeros(N, ldb, dtype=torch.uint8, device="cuda")
@@ -78,7 +78,7 @@ def test_scaled_mm_against_exact(g, M, N, K, fa, fb):
     da, db = np.float32(rng.uniform(0.001, 0.1)), np.float32(rng.uniform(0.001, 0.1))
     got = run_mm(g, A, fa, B, fb, da, db)
     ref, mag, _ = gemm.scaled_mm(A, FMT[fa], B, FMT[fb], da, db)
-    assert_close(got, ref, mag)
+    assert_close(got[:, :N], ref, mag)
 
 
 def test_padded_leading_dimensions(g):
@@ -102,7 +102,7 @@ def test_identity_operand_is_exact(g, fa, one):
     d = np.float32(0.01171875)  # 3 * 2^-8
     got = run_mm(g, A, fa, B, fa, d, 1.0)
     ref, _, _ = gemm.scaled_mm(A, FMT[fa], B, FMT[fa], d, 1.0)
-    assert np.array_equal(got, ref)
+    assert np.array_equal(got[:, :K], ref)
 
 
 def test_integer_sums_are_exact(g):
@@ -115,7 +115,7 @@ def test_integer_sums_are_exact(g):
     B = rng.choice(vals, size=(N, K))
     got = run_mm(g, A, 0, B, 0, 1.0, 1.0)
     ref, _, _ = gemm.scaled_mm(A, fp8.E4M3, B, fp8.E4M3, 1.0, 1.0)
-    assert np.array_equal(got, ref)
+    assert np.array_equal(got[:, :N], ref)
 
 
 def test_k_zero_writes_zeros(g):
