@@ -1,0 +1,468 @@
+#!/usr/bin/env python
+"""Benchmark of the FP8 up-projection training step on GB300.
+
+Workload (GPT-2-small-shaped MLP up-projection): x [8192 x 768] ~ N(0,1) with 0.1 % of
+the entries x100, W [768 x 3072] ~ N(0, 0.02), dy [8192 x 3072] log-normal (median 1e-4,
+sigma_log 2, random sign). One step = one pass of the whole hot path with per-tensor
+delayed scaling (amax history of 16):
+  requantise W (amax, scale, E4M3 cast into W_q [K,N] and W_q^T [N,K])
+  quantise x (E4M3, x_q and x_q^T)          forward GEMM  y  = x W         (tcgen05)
+  quantise dy (E5M2, dy_q and dy_q^T)       dgrad GEMM    dx = dy W^T
+                                            wgrad GEMM    dW = x^T dy
+  push the x, W and dy amaxes into their histories.
+Each stage is captured once into a CUDA graph; the timed loop replays the stages with
+CUDA events between them (per-stage times) and writes a 256 MiB buffer between steps to
+flush the 129 MB L2 (not timed). value = the step's GEMM FLOPs (3 x 2MNK) over the
+measured step time, summed over ranks (each rank its own batch: weak scaling).
+
+--impl reference times the CPU oracle (test infrastructure) on a bounded sample of the
+same step on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 up-proj GEMM TFLOP/s (% FP8 peak); quantize-cast GB/s (% HBM)"
+M, K, N = 8192, 768, 3072
+HIST = 16
+FLUSH_BYTES = 256 << 20
+# Peaks on this machine (measured): HBM copy GB/s and dense bf16 TFLOP/s (burst); the FP8
+# dense peak is the bf16 figure times the nominal fp8/bf16 ratio 4.5 / 2.25 = 2.
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return FALLBACK_PEAKS["hbm_gbs"], FALLBACK_PEAKS["bf16_tflops"], "fallback"
+
+
+def env_rank():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+# --------------------------------------------------------------------------------------
+# clocks sampler
+# --------------------------------------------------------------------------------------
+class Clocks:
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------------------
+def traffic_table():
+    """Per-launch DRAM bytes from the committed ncu summary, keyed by stage, valid only
+    while the kernel sources hash the same as when the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic_per_launch.txt")
+    out = {}
+    if not os.path.exists(path):
+        return out
+    h = source_hash()
+    for line in open(path):
+        line = line.split("#")[0].split()
+        if len(line) == 3 and line[2] == h:
+            out[line[0]] = float(line[1])
+    return out
+
+
+def source_hash():
+    d = os.path.join(ROOT, "fp8_mixed_precision_saturating_gb300", "csrc")
+    hsh = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        hsh.update(open(os.path.join(d, f), "rb").read())
+    return hsh.hexdigest()[:16]
+
+
+def rank_seeds(rank: int):
+    """Seeds of rank r's own batch (x, dy): rank 0 uses the workload's seeds."""
+    return (1000 * 2 + 0, 2002) if rank == 0 else (2000 + 10 * rank, 2002 + 10 * rank)
+
+
+def max_over_ranks(total_ms: float, world: int, device) -> float:
+    """The slowest rank's timed total (every rank calls this)."""
+    if world <= 1:
+        return total_ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(step_flops: float, steps: int, world: int, total_ms: float) -> float:
+    """TFLOP/s of the whole job: every rank ran `steps` steps of its own batch."""
+    return step_flops * steps * world / (total_ms * 1e-3) / 1e12
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    rank, local_rank, world = env_rank()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+    import fp8_mixed_precision_saturating_gb300 as g
+    from datagen import workload_inputs, lognormal_grad_bf16, outlier_normal_bf16
+
+    w = workload_inputs("gpt2s_upproj_fwd")
+    sx, sdy = rank_seeds(rank)
+    x_h = w["x"] if rank == 0 else outlier_normal_bf16(sx, (M, K))
+    w_h = w["w"]
+    dy_h = lognormal_grad_bf16(sdy, (M, N))
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+    x, wm, dy = dev(x_h), dev(w_h), dev(dy_h)
+    u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device="cuda")
+    bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
+    wst, xst, gst = g.TensorState(HIST), g.TensorState(HIST), g.TensorState(HIST)
+    wq, wqT, xq, xqT, dyq, dyqT = u8(K, N), u8(N, K), u8(M, K), u8(K, M), u8(M, N), u8(N, M)
+    y, dx, dw = bf(M, N), bf(M, K), bf(K, N)
+    D = g.FP8_SCALE_DELAYED
+    T = g.FP8_GRAN_TENSOR
+    gemm_flops = 2.0 * M * N * K
+
+    # (name, call, kernels launched, algorithmic flops, algorithmic bytes)
+    stages = [
+        ("requant_w", lambda: g.fp8_requantize_weights(wm, K, N, T, D, wst, wq, wqT), 2, 0.0, K * N * 4.0),
+        ("quant_x", lambda: g.fp8_quantize(x, M, K, K, g.FP8_E4M3, T, D, xst, xq, xqT), 2, 0.0, M * K * 4.0),
+        ("gemm_fwd", lambda: g.fp8_scaled_mm(xq, 0, wqT, 0, M, N, K, K, K, T, xst.scale_inv, wst.scale_inv, y, N),
+         1, gemm_flops, 0.0),
+        ("quant_dy", lambda: g.fp8_quantize(dy, M, N, N, g.FP8_E5M2, T, D, gst, dyq, dyqT), 2, 0.0, M * N * 4.0),
+        ("gemm_dgrad", lambda: g.fp8_scaled_mm(dyq, 1, wq, 0, M, K, N, N, N, T, gst.scale_inv, wst.scale_inv, dx, K),
+         1, gemm_flops, 0.0),
+        ("gemm_wgrad", lambda: g.fp8_scaled_mm(xqT, 0, dyqT, 1, K, N, M, M, M, T, xst.scale_inv, gst.scale_inv, dw, N),
+         1, gemm_flops, 0.0),
+        ("commit", lambda: (g.fp8_history_commit(wst), g.fp8_history_commit(xst), g.fp8_history_commit(gst)),
+         3, 0.0, 0.0),
+    ]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(stream):
+        for _, fn, *_ in stages:  # eager pass: sets kernel attributes and caches
+            fn()
+        torch.cuda.synchronize()
+        for _, fn, *_ in stages:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                fn()
+            graphs.append(gr)
+        for st in (wst, xst, gst):
+            st.reset()  # the delayed-scaling state starts empty (bootstrap step first)
+        torch.cuda.synchronize()
+
+        def step(ev=None):
+            flush.zero_()
+            if ev is not None:
+                ev[0].record(stream)
+            for i, gr in enumerate(graphs):
+                gr.replay()
+                if ev is not None:
+                    ev[i + 1].record(stream)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
+        clocks = Clocks(local_rank)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        clocks.start()
+        time.sleep(0.3)  # let the sampler see the first samples
+        wall0 = time.perf_counter()
+        for k in range(args.steps):
+            step(evs[k])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        if world > 1:
+            torch.distributed.barrier()
+        clk = clocks.stop()
+        g.fp8_poll_device_error()
+
+    step_ms = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)]
+    stage_ms = [sum(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)) / args.steps
+                for i in range(len(stages))]
+    total_ms = max_over_ranks(sum(step_ms), world, "cuda")
+    step_flops = sum(s[3] for s in stages)
+    value = weak_scaling_value(step_flops, args.steps, world, total_ms)
+
+    hbm, bf16_tf, peak_src = load_peaks()
+    fp8_peak = bf16_tf * 2.0
+    traffic = traffic_table()
+    kernels = {}
+    for (name, _, nk, fl, by), ms in zip(stages, stage_ms):
+        kd = {"ms": round(ms, 5), "launches": nk}
+        if fl:
+            kd.update(achieved=round(fl / (ms * 1e-3) / 1e12, 1), unit="TFLOP/s", frac=round(fl / (ms * 1e-3) / 1e12 / fp8_peak, 4))
+        elif by:
+            kd.update(achieved=round(by / (ms * 1e-3) / 1e9, 1), unit="GB/s", frac=round(by / (ms * 1e-3) / 1e9 / hbm, 4))
+        kernels[name] = kd
+    dom_i = max(range(len(stages)), key=lambda i: stage_ms[i] if (stages[i][3] or stages[i][4]) else -1)
+    dname, _, _, dfl, dby = stages[dom_i]
+    dms = stage_ms[dom_i]
+    if dfl:
+        roof = {"kernel": dname, "bound": "tensor", "achieved": round(dfl / (dms * 1e-3) / 1e12, 1),
+                "peak": round(fp8_peak, 1), "unit": "TFLOP/s"}
+    else:
+        roof = {"kernel": dname, "bound": "hbm", "achieved": round(dby / (dms * 1e-3) / 1e9, 1),
+                "peak": round(hbm, 1), "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = traffic.get(dname)
+    roof["peak_source"] = (f"{peak_src}: fp8 = 2 x bf16 burst {bf16_tf} TF/s" if dfl else f"{peak_src}: HBM copy {hbm} GB/s")
+
+    # block-scaled forward at the same shapes (1x128 x tiles, 128x128 W blocks), timed alone
+    blk = run_block_scaled(g, torch, x, wm, stream, flush, args.steps)
+    # end to end through the public API with host buffers
+    e2e = run_e2e(g, torch, x_h, w_h, dy_h, stream, args.steps, step_flops)
+
+    launches = sum(s[2] for s in stages) * args.steps
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/e5m2 x fp32-accumulate -> bf16", "data": "synthetic",
+        "config": {"workload": "gpt2s_upproj_train_step", "M_tokens": M, "d_model": K, "d_ff": N,
+                   "step": "requantise W, quantise x, fwd GEMM, quantise dy, dgrad, wgrad, 3 history commits",
+                   "scaling": "per-tensor delayed, amax history 16", "global_batch_tokens": M * world,
+                   "l2": "256 MiB buffer written between timed steps (flush)", "parallelism": f"dp{world} (independent batches)"},
+        "roofline": roof,
+        "kernels": kernels,
+        "block_scaled_fwd": blk,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "wall_s_timed": round(wall, 4),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_full_step()
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_block_scaled(g, torch, x, wm, stream, flush, steps):
+    u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device="cuda")
+    xq, wq, wqT = u8(M, K), u8(K, N), u8(N, K)
+    xsi = torch.empty(M, K // 128, dtype=torch.float32, device="cuda")
+    wsi = torch.empty(K // 128, N // 128, dtype=torch.float32, device="cuda")
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    B = g.FP8_GRAN_BLOCK_128x128
+    calls = [
+        ("requant_w_block", lambda: g.fp8_requantize_weights(wm, K, N, B, 0, None, wq, wqT, wsi), 0.0, K * N * 4.0),
+        ("quant_x_1x128", lambda: g.fp8_quantize(x, M, K, K, 0, g.FP8_GRAN_TILE_1x128, 0, None, xq, None, xsi),
+         0.0, M * K * 3.0 + M * K / 128 * 4),
+        ("gemm_fwd_block_scaled", lambda: g.fp8_scaled_mm(xq, 0, wqT, 0, M, N, K, K, K, B, xsi, wsi, y, N),
+         2.0 * M * N * K, 0.0),
+    ]
+    with torch.cuda.stream(stream):
+        for _, fn, _, _ in calls:
+            fn()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(steps)]
+        for k in range(steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            for i, (_, fn, _, _) in enumerate(calls):
+                fn()
+                ev[k][i + 1].record(stream)
+        torch.cuda.synchronize()
+    out = {}
+    hbm, bf16_tf, _ = load_peaks()
+    for i, (name, _, fl, by) in enumerate(calls):
+        ms = sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(steps)) / steps
+        d = {"ms": round(ms, 5)}
+        if fl:
+            d.update(achieved=round(fl / (ms * 1e-3) / 1e12, 1), unit="TFLOP/s", frac=round(fl / (ms * 1e-3) / 1e12 / (2 * bf16_tf), 4))
+        else:
+            d.update(achieved=round(by / (ms * 1e-3) / 1e9, 1), unit="GB/s", frac=round(by / (ms * 1e-3) / 1e9 / hbm, 4))
+        out[name] = d
+    return out
+
+
+def run_e2e(g, torch, x_h, w_h, dy_h, stream, steps, step_flops):
+    """The same step through the public API (requantise + linear forward + linear backward
+    + commits) with host inputs: pinned host -> device copies of x, W and dy and device ->
+    host copies of y, dx and dW inside the timed region."""
+    import numpy as np
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+    xh, wh, dyh = pin(x_h), pin(w_h), pin(dy_h)
+    bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
+    u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device="cuda")
+    x, wm, dy = bf(M, K), bf(K, N), bf(M, N)
+    y, dx, dw = bf(M, N), bf(M, K), bf(K, N)
+    yh, dxh, dwh = [torch.empty(*s, dtype=torch.bfloat16).pin_memory() for s in ((M, N), (M, K), (K, N))]
+    wq, wqT, xq, xqT, dyq, dyqT = u8(K, N), u8(N, K), u8(M, K), u8(K, M), u8(M, N), u8(N, M)
+    wst, xst, gst = g.TensorState(HIST), g.TensorState(HIST), g.TensorState(HIST)
+    D, T = g.FP8_SCALE_DELAYED, g.FP8_GRAN_TENSOR
+
+    def one():
+        x.copy_(xh, non_blocking=True)
+        wm.copy_(wh, non_blocking=True)
+        dy.copy_(dyh, non_blocking=True)
+        g.fp8_requantize_weights(wm, K, N, T, D, wst, wq, wqT)
+        g.fp8_linear_fwd(x, M, K, N, wqT, wst, None, xst, T, D, xq, xqT, None, y)
+        g.fp8_linear_bwd(dy, M, K, N, xqT, xst, wq, wst, gst, D, dyq, dyqT, dx, dw)
+        for st in (wst, xst, gst):
+            g.fp8_history_commit(st)
+        yh.copy_(y, non_blocking=True)
+        dxh.copy_(dx, non_blocking=True)
+        dwh.copy_(dw, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": round(step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(2 * (M * K + K * N + M * N)),
+            "d2h_bytes_per_step": int(2 * (M * N + M * K + K * N))}
+
+
+# --------------------------------------------------------------------------------------
+# CPU oracle arm
+# --------------------------------------------------------------------------------------
+def oracle_step(tokens: int):
+    """One oracle pass of the step's arithmetic on `tokens` of the M tokens (W in full).
+    Returns the GEMM FLOPs it covered."""
+    from datagen import workload_inputs, lognormal_grad_bf16
+    from oracle import fp8, gemm, quant
+    w = oracle_step.cache if hasattr(oracle_step, "cache") else None
+    if w is None:
+        w = workload_inputs("gpt2s_upproj_fwd")
+        w["dy"] = lognormal_grad_bf16(2002, (M, N))
+        oracle_step.cache = w
+    x, dy = w["x"][:tokens], w["dy"][:tokens]
+    ow = quant.quantize_tensor(w["w"], fp8.E4M3)
+    ox = quant.quantize_tensor(x, fp8.E4M3)
+    og = quant.quantize_tensor(dy, fp8.E5M2)
+    gemm.scaled_mm(ox["q"], fp8.E4M3, ow["qT"], fp8.E4M3, ox["d"], ow["d"])
+    gemm.scaled_mm(og["q"], fp8.E5M2, ow["q"], fp8.E4M3, og["d"], ow["d"])
+    gemm.scaled_mm(ox["qT"], fp8.E4M3, og["qT"], fp8.E5M2, ox["d"], og["d"])
+    return 3 * 2.0 * tokens * N * K
+
+
+def cpu_baseline_full_step():
+    oracle_step(64)  # load inputs
+    t0 = time.perf_counter()
+    fl = oracle_step(M)
+    dt = time.perf_counter() - t0
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"one full step ({M} tokens): numpy oracle casts (one thread) and fp64 BLAS matmuls "
+                      f"(all cores); {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank, _, world = env_rank()
+    if rank != 0:
+        return
+    tokens = 2048
+    for _ in range(args.warmup):
+        oracle_step(tokens)
+    t0 = time.perf_counter()
+    fl = 0.0
+    for _ in range(args.steps):
+        fl += oracle_step(tokens)
+    dt = time.perf_counter() - t0
+    value = fl / dt / 1e12
+    sample = f"{tokens} of {M} tokens per step (W in full), numpy oracle, fp64 BLAS matmuls"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": "gpt2s_upproj_train_step", "M_tokens": M, "d_model": K, "d_ff": N},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
