@@ -52,6 +52,7 @@ _SIGS = {
     "fp8_requantize_weights": [_P, _I64, _I64, _I, _I, _SP, _P, _P, _P, _P],
     "fp8_linear_fwd": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _I, _I, _P, _P, _P, _P, _P],
     "fp8_linear_bwd": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _SP, _I, _P, _P, _P, _P, _P],
+    "fp8_linear_bwd_noalloc": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _SP, _I, _P, _P, _P],
     "fp8_history_commit": [_SP, _P],
     "fp8_poll_device_error": [],
     "fp8_set_wait_limit_ns": [ctypes.c_ulonglong],
@@ -183,6 +184,13 @@ def fp8_linear_bwd(dy, M, K, N, xqT_save, x_st, wq_kn, w_st, dy_st, mode, dyq_ws
     return _check(lib.fp8_linear_bwd(_ptr(dy), M, K, N, _ptr(xqT_save), _state(x_st), _ptr(wq_kn), _state(w_st),
                                      _state(dy_st), mode, _ptr(dyq_ws), _ptr(dyqT_ws), _ptr(dx), _ptr(dw),
                                      _stream(stream)))
+
+
+def fp8_linear_bwd_noalloc(dy, M, K, N, xqT_save, x_st, wq_kn, w_st, dy_st, mode, dx, dw, stream=None):
+    """fp8_linear_bwd with the dy codes in the library's static device array (no scratch
+    arguments, no allocation by the call); see include/fp8gb.h for the size limit."""
+    return _check(lib.fp8_linear_bwd_noalloc(_ptr(dy), M, K, N, _ptr(xqT_save), _state(x_st), _ptr(wq_kn),
+                                             _state(w_st), _state(dy_st), mode, _ptr(dx), _ptr(dw), _stream(stream)))
 
 
 def fp8_history_commit(st, stream=None):

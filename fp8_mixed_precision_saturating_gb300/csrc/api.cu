@@ -299,6 +299,75 @@ fp8_status_t fp8_linear_bwd(const void* dy_bf16, int64_t M, int64_t K, int64_t N
   return FP8_OK;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free backward: fp8_linear_bwd with its dy-code scratch in a static array.
+// ---------------------------------------------------------------------------------------
+// The backward casts dy to E5M2 twice (row-major for dgrad, transposed for wgrad) before the
+// two GEMMs read the codes. fp8_linear_bwd takes those two buffers from the caller; this
+// array stands in for them. It is part of the loaded library image, so every GPU that loads
+// the library holds these 64 MiB until the process exits, whether or not it is used.
+static constexpr size_t kBwdScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) uint8_t g_bwd_scratch[kBwdScratchBytes];
+
+namespace {
+
+// Device address of g_bwd_scratch on the current device. The name g_bwd_scratch in host
+// code is only a host-side stand-in for the symbol, never a device pointer, so it is looked
+// up once per device (with that device current) and cached.
+uint8_t* bwd_scratch_address(fp8_status_t* status) {
+  static uint8_t* addr[kMaxDev] = {};
+  static std::mutex mu;
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDev) {
+    *status = fail(FP8_ERR_CUDA, "fp8_linear_bwd_noalloc: no usable current device");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (addr[d] == nullptr) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_bwd_scratch);
+    if (e != cudaSuccess || ptr == nullptr) {
+      *status = cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol,
+                          "fp8_linear_bwd_noalloc: cudaGetSymbolAddress of the static scratch");
+      return nullptr;
+    }
+    addr[d] = static_cast<uint8_t*>(ptr);
+  }
+  return addr[d];
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8_status_t fp8_linear_bwd_noalloc(const void* dy_bf16, int64_t M, int64_t K, int64_t N, const void* xqT_save,
+                                    const fp8_tensor_state_t* x_st, const void* wq_kn,
+                                    const fp8_tensor_state_t* w_st, fp8_tensor_state_t* dy_st, fp8_scaling_t mode,
+                                    void* dx_bf16, void* dw_bf16, void* stream) {
+  const char* who = "fp8_linear_bwd_noalloc";
+  if (M < 0 || K < 0 || N < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
+  if (M >= (1ll << 31) || N >= (1ll << 31)) return fail(FP8_ERR_UNSUPPORTED, "%s: dimension >= 2^31", who);
+  // dy codes [M,N], then (for wgrad) the transposed codes [N,M] at the next 256-byte boundary
+  const uint64_t codes = static_cast<uint64_t>(M) * static_cast<uint64_t>(N);
+  const uint64_t t_off = (codes + 255u) & ~uint64_t(255);
+  const uint64_t need = dw_bf16 != nullptr ? t_off + codes : codes;
+  if (need > kBwdScratchBytes)
+    return fail(FP8_ERR_UNSUPPORTED,
+                "%s: dy [%lld x %lld] needs %llu bytes of scratch for its FP8 codes%s, more than the %llu-byte "
+                "static array; use fp8_linear_bwd with caller-provided scratch",
+                who, (long long)M, (long long)N, (unsigned long long)need, dw_bf16 != nullptr ? " and their transpose" : "",
+                (unsigned long long)kBwdScratchBytes);
+  fp8_status_t st = FP8_OK;
+  uint8_t* base = bwd_scratch_address(&st);
+  if (base == nullptr) return st;
+  // Both regions are written in full by the dy cast before the GEMMs read them: nothing in
+  // the array has to start at zero.
+  return fp8_linear_bwd(dy_bf16, M, K, N, xqT_save, x_st, wq_kn, w_st, dy_st, mode, base,
+                        dw_bf16 != nullptr ? base + t_off : nullptr, dx_bf16, dw_bf16, stream);
+}
+
 fp8_status_t fp8_history_commit(const fp8_tensor_state_t* st, void* stream) {
   if (st == nullptr || !st->amax_history || !st->hist_count || !st->amax_cur || st->hist_len <= 0)
     return fail(FP8_ERR_INVALID_ARG, "fp8_history_commit: needs amax_history, hist_count, amax_cur, hist_len > 0");

@@ -181,6 +181,30 @@ fp8_status_t fp8_linear_bwd(const void* dy_bf16, int64_t M, int64_t K, int64_t N
                             void* dyq_ws, void* dyqT_ws, void* dx_bf16, void* dw_bf16,
                             void* stream);
 
+/* fp8_linear_bwd without caller scratch. The pages have no counterpart to this entry point:
+ * it exists for callers that cannot allocate device memory at the point of the call -- for
+ * example a host framework that hands the library only its input and output tensors and
+ * forbids side allocations, or a plain C program that links this library and keeps no
+ * device allocator of its own. Everything is as in fp8_linear_bwd (same arguments, same
+ * results, same validation) except that the E5M2 codes of dy and of dy^T live in a static
+ * 64 MiB device array inside the library instead of dyq_ws / dyqT_ws:
+ *   - size limit: M*N bytes when dw_bf16 is NULL, else M*N rounded up to 256 plus M*N
+ *     bytes, at most 64 MiB (e.g. M*N <= 32 Mi elements with wgrad); larger shapes return
+ *     FP8_ERR_UNSUPPORTED before anything is enqueued;
+ *   - the array is part of the loaded library: every GPU that loads the library holds the
+ *     64 MiB until the process exits;
+ *   - the first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current and caches it; make that first call before any stream capture;
+ *   - all calls share one array, so calls whose work overlaps on the GPU (different streams,
+ *     or threads without ordering) race on it and give wrong codes; order them on one stream;
+ *   - the call allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine;
+ *     the array's previous contents never matter because the dy cast overwrites what it uses. */
+fp8_status_t fp8_linear_bwd_noalloc(const void* dy_bf16, int64_t M, int64_t K, int64_t N,
+                                    const void* xqT_save, const fp8_tensor_state_t* x_st,
+                                    const void* wq_kn, const fp8_tensor_state_t* w_st,
+                                    fp8_tensor_state_t* dy_st, fp8_scaling_t mode,
+                                    void* dx_bf16, void* dw_bf16, void* stream);
+
 /* Push st->amax_cur into the history: amax_history[hist_count % hist_len] = amax_cur;
  * hist_count += 1. [GUARD] "Real products...": amax history tracking. */
 fp8_status_t fp8_history_commit(const fp8_tensor_state_t* st, void* stream);
