@@ -10,9 +10,9 @@ delayed scaling (amax history of 16):
   quantise dy (E5M2, dy_q and dy_q^T)       dgrad GEMM    dx = dy W^T
                                             wgrad GEMM    dW = x^T dy
   push the x, W and dy amaxes into their histories.
-Each stage is captured once into a CUDA graph; the timed loop replays the stages with
-CUDA events between them (per-stage times) and writes a 256 MiB buffer between steps to
-flush the 129 MB L2 (not timed). value = the step's GEMM FLOPs (3 x 2MNK) over the
+The step is captured once into a CUDA graph with external CUDA-event nodes between the
+stages (per-stage times); the timed loop replays it once per step and writes a 256 MiB
+buffer between steps to flush the 129 MB L2 (not timed). value = the step's GEMM FLOPs (3 x 2MNK) over the
 measured step time, summed over ranks (each rank its own batch: weak scaling).
 
 --impl reference times the CPU oracle (test infrastructure) on a bounded sample of the
@@ -203,33 +203,30 @@ def run_gpu(args):
     ]
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.Stream()
-    graphs = []
     with torch.cuda.stream(stream):
         for _, fn, *_ in stages:  # eager pass: sets kernel attributes and caches
             fn()
         torch.cuda.synchronize()
-        for _, fn, *_ in stages:
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=stream):
+        # the whole step is one CUDA graph; external event nodes between the stages time them
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(stages) + 1)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            ev[0].record(stream)
+            for i, (_, fn, *_) in enumerate(stages):
                 fn()
-            graphs.append(gr)
+                ev[i + 1].record(stream)
         for st in (wst, xst, gst):
             st.reset()  # the delayed-scaling state starts empty (bootstrap step first)
         torch.cuda.synchronize()
 
-        def step(ev=None):
-            flush.zero_()
-            if ev is not None:
-                ev[0].record(stream)
-            for i, gr in enumerate(graphs):
-                gr.replay()
-                if ev is not None:
-                    ev[i + 1].record(stream)
+        def step():
+            flush.zero_()  # L2 flush, outside the timed events
+            graph.replay()
+            torch.cuda.synchronize()
+            return [ev[i].elapsed_time(ev[i + 1]) for i in range(len(stages))]
 
         for _ in range(args.warmup):
             step()
-        torch.cuda.synchronize()
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
         clocks = Clocks(local_rank)
         if world > 1:
             torch.distributed.barrier()
@@ -237,8 +234,7 @@ def run_gpu(args):
         clocks.start()
         time.sleep(0.3)  # let the sampler see the first samples
         wall0 = time.perf_counter()
-        for k in range(args.steps):
-            step(evs[k])
+        per_step = [step() for _ in range(args.steps)]
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
         if world > 1:
@@ -246,9 +242,8 @@ def run_gpu(args):
         clk = clocks.stop()
         g.fp8_poll_device_error()
 
-    step_ms = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)]
-    stage_ms = [sum(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)) / args.steps
-                for i in range(len(stages))]
+    step_ms = [sum(t) for t in per_step]
+    stage_ms = [sum(t[i] for t in per_step) / args.steps for i in range(len(stages))]
     total_ms = max_over_ranks(sum(step_ms), world, "cuda")
     step_flops = sum(s[3] for s in stages)
     value = weak_scaling_value(step_flops, args.steps, world, total_ms)
@@ -391,6 +386,118 @@ def run_e2e(g, torch, x_h, w_h, dy_h, stream, steps, step_flops):
 
 
 # --------------------------------------------------------------------------------------
+# per-kernel sweep over the five workloads' shapes (not part of the bench line)
+# --------------------------------------------------------------------------------------
+# name, M, N, K, format of A, format of B, block scaled
+SWEEP_GEMMS = [
+    ("tiny_fwd", 256, 512, 128, 0, 0, False),
+    ("gpt2s_fwd", 8192, 3072, 768, 0, 0, False),
+    ("gpt2s_dgrad", 8192, 768, 3072, 1, 0, False),
+    ("gpt2s_wgrad", 768, 3072, 8192, 0, 1, False),
+    ("bwd_dgrad", 16384, 1024, 4096, 1, 0, False),
+    ("bwd_wgrad", 1024, 4096, 16384, 0, 1, False),
+    ("fine_fwd_block", 16384, 14336, 4096, 0, 0, True),
+    ("fine_fwd_tensor", 16384, 14336, 4096, 0, 0, False),
+    ("loop_fwd", 32768, 6144, 1536, 0, 0, False),
+    ("loop_dgrad", 32768, 1536, 6144, 1, 0, False),
+    ("loop_wgrad", 1536, 6144, 32768, 0, 1, False),
+]
+# name, rows, cols, format, granularity (0 tensor, 1 1x128, 2 128x128), transposed copy
+SWEEP_CASTS = [
+    ("gpt2s_dy_e5m2", 8192, 3072, 1, 0, True),
+    ("bwd_dy_e5m2", 16384, 4096, 1, 0, True),
+    ("bwd_x_e4m3", 16384, 1024, 0, 0, True),
+    ("bwd_dy_e5m2_rowmajor", 16384, 4096, 1, 0, False),
+    ("fine_x_1x128", 16384, 4096, 0, 1, False),
+    ("fine_w_128x128", 4096, 14336, 0, 2, True),
+    ("loop_dy_e5m2", 32768, 6144, 1, 0, True),
+]
+
+
+def run_sweep(args):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import fp8_mixed_precision_saturating_gb300 as g
+    torch.cuda.set_device(0)
+    hbm, bf16_tf, _ = load_peaks()
+    fp8_peak = 2 * bf16_tf
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    only = set(args.only.split(",")) if args.only else None
+
+    def codes(rows, cols, fmt):
+        # finite codes of either sign: magnitudes below the NaN / inf encodings
+        mag = torch.randint(0, 0x70, (rows, cols), generator=gen, device="cuda", dtype=torch.int32)
+        sgn = torch.randint(0, 2, (rows, cols), generator=gen, device="cuda", dtype=torch.int32) << 7
+        return (mag | sgn).to(torch.uint8)
+
+    def timed(fn, iters):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(iters):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    for name, m, n, k, fa, fb, blk in SWEEP_GEMMS:
+        if only and name not in only:
+            continue
+        A, B = codes(m, k, fa), codes(n, k, fb)
+        C = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+        if blk:
+            sa = torch.rand(m, k // 128, generator=gen, device="cuda") * 1e-2
+            sb = torch.rand(k // 128, n // 128, generator=gen, device="cuda") * 1e-2
+            gran = g.FP8_GRAN_BLOCK_128x128
+        else:
+            sa = torch.full((1,), 1e-2, device="cuda")
+            sb = torch.full((1,), 1e-2, device="cuda")
+            gran = g.FP8_GRAN_TENSOR
+        ms = timed(lambda: g.fp8_scaled_mm(A, fa, B, fb, m, n, k, k, k, gran, sa, sb, C, n), args.steps)
+        tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
+        print(json.dumps({"sweep": "gemm", "name": name, "M": m, "N": n, "K": k, "block_scaled": blk,
+                          "ms": round(ms, 5), "TFLOP/s": round(tf, 1), "frac_fp8_peak": round(tf / fp8_peak, 4)}))
+        del A, B, C
+    for name, r, c, fmt, gran, tr in SWEEP_CASTS:
+        if only and name not in only:
+            continue
+        x = torch.randn(r, c, generator=gen, device="cuda").to(torch.bfloat16)
+        q = torch.empty(r, c, dtype=torch.uint8, device="cuda")
+        qT = torch.empty(c, r, dtype=torch.uint8, device="cuda") if tr else None
+        st = g.TensorState()
+        if gran == 0:
+            fn = lambda: g.fp8_quantize(x, r, c, c, fmt, 0, g.FP8_SCALE_CURRENT, st, q, qT)
+            by = r * c * (3.0 + (1 if tr else 0))
+        elif gran == 1:
+            si = torch.empty(r, c // 128, device="cuda")
+            fn = lambda: g.fp8_quantize(x, r, c, c, fmt, 1, 0, None, q, None, si)
+            by = r * c * 3.0 + r * c / 128 * 4
+        else:
+            si = torch.empty(r // 128, c // 128, device="cuda")
+            fn = lambda: g.fp8_quantize(x, r, c, c, fmt, 2, 0, None, q, qT, si)
+            by = r * c * (3.0 + (1 if tr else 0)) + r * c / 16384 * 4
+        ms = timed(fn, args.steps)
+        gbs = by / (ms * 1e-3) / 1e9
+        out = {"sweep": "cast", "name": name, "rows": r, "cols": c, "ms": round(ms, 5),
+               "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
+        if gran == 0:  # the current-scaling amax pass re-reads x: not algorithmic, reported apart
+            st2 = g.TensorState(2)
+            st2.amax_history[0] = 1.0
+            st2.hist_count[0] = 1
+            ms_c = timed(lambda: g.fp8_quantize(x, r, c, c, fmt, 0, g.FP8_SCALE_DELAYED, st2, q, qT), args.steps)
+            out.update(ms_cast_only=round(ms_c, 5), cast_only_GB_s=round(by / (ms_c * 1e-3) / 1e9, 1))
+        print(json.dumps(out))
+        del x, q, qT
+    g.fp8_poll_device_error()
+
+
+# --------------------------------------------------------------------------------------
 # CPU oracle arm
 # --------------------------------------------------------------------------------------
 def oracle_step(tokens: int):
@@ -455,10 +562,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="time every workload's GEMM and cast shapes instead")
+    ap.add_argument("--only", default="", help="comma-separated sweep entries")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

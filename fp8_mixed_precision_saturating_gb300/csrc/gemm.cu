@@ -46,14 +46,17 @@ struct Cfg {
   static constexpr int B_BYTES = BN * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
-  static constexpr uint32_t TMEM_COLS = 2 * BN;          // two accumulators
-  static constexpr int EPI_WARPS = BLOCK ? 4 * (BN / 128) : 4;
-  static constexpr int STG_PER_WARP = BLOCK ? 1 : 2;
+  static constexpr int ACC = 512 / BN;                   // accumulator buffers in TMEM
+  static constexpr uint32_t TMEM_COLS = 512;
+  // per tensor: two warps per TMEM lane quarter, each draining half of the tile's columns;
+  // block scaled: one warp per lane quarter and 64 columns
+  static constexpr int EPI_WARPS = BLOCK ? 4 * (BN / 64) : 8;
+  static constexpr int STG_PER_WARP = 1;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int OFF_STG = STAGES * STAGE_BYTES;
   static constexpr int OFF_BAR = OFF_STG + EPI_WARPS * STG_PER_WARP * STG_BYTES;
-  // full[S], empty[S], tfull[2], tempty[2], final
-  static constexpr int NBAR = 2 * STAGES + 5;
+  // full[S], empty[S], tfull[ACC], tempty[ACC], final
+  static constexpr int NBAR = 2 * STAGES + 2 * ACC + 1;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + 8 * NBAR;
   static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;  // + alignment slack
   static_assert(SMEM <= 232448, "shared memory");
@@ -119,6 +122,7 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
   constexpr int STAGES = C::STAGES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
   constexpr uint32_t TMEM_COLS = C::TMEM_COLS;
+  constexpr int ACC = C::ACC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -126,8 +130,8 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
   const uint32_t bar_full = sbase + C::OFF_BAR;
   const uint32_t bar_empty = bar_full + 8 * STAGES;
   const uint32_t bar_tfull = bar_empty + 8 * STAGES;
-  const uint32_t bar_tempty = bar_tfull + 16;
-  const uint32_t bar_final = bar_tempty + 16;
+  const uint32_t bar_tempty = bar_tfull + 8 * ACC;
+  const uint32_t bar_final = bar_tempty + 8 * ACC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   if (threadIdx.x == 0) {
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < ACC; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
       mbar_init(bar_tempty + 8 * a, C::EPI_WARPS);
     }
@@ -229,13 +233,13 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
           }
           if (BLOCK) {
             mma_commit(bar_tfull + 8 * acc);
-            acc ^= 1;
+            acc = (acc + 1 == ACC) ? 0 : acc + 1;
             if (acc == 0) acc_phase ^= 1u;
           }
         }
         if (!BLOCK && ok) {
           mma_commit(bar_tfull + 8 * acc);
-          acc ^= 1;
+          acc = (acc + 1 == ACC) ? 0 : acc + 1;
           if (acc == 0) acc_phase ^= 1u;
         }
       }
@@ -254,7 +258,8 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
     bool ok = true;
     if constexpr (!BLOCK) {
       const float dd = __fmul_rn(__ldg(p.sa), __ldg(p.sb));
-      int buf = 0;
+      const int hc = ew >> 2;  // which half of the tile's columns this warp drains
+      constexpr int CHUNKS = BN / 128;  // 64-column chunks per warp
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
         int mb, nb;
         tile_coords(t, p, mb, nb);
@@ -262,16 +267,17 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
         __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the spin
         tc_fence_after();
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 64; ++ch) {
+        for (int ch = 0; ch < CHUNKS; ++ch) {
           __syncwarp();
           uint32_t r0[32], r1[32];
-          const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + ch * 64);
+          const int col = hc * (BN / 2) + ch * 64;
+          const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col);
           tmem_ld32(taddr, r0);
           tmem_ld32(taddr + 32, r1);
           tmem_ld_wait();
           reg_fence(r0);
           reg_fence(r1);
-          if (ch == BN / 64 - 1) {  // accumulator fully read: hand it back to the MMA warp
+          if (ch == CHUNKS - 1) {  // this warp's part of the accumulator is read: hand it back
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
@@ -283,26 +289,27 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
             pk[16 + j] =
                 pack_bf16x2(__fmul_rn(__uint_as_float(r1[2 * j]), dd), __fmul_rn(__uint_as_float(r1[2 * j + 1]), dd));
           }
-          if (lane == 0) bulk_wait_group_read<1>();  // the store that used this buffer has read it
+          if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the staging buffer
           __syncwarp();
-          stage_and_store(stg + buf * STG_BYTES, pk, lane, &tmC, nb * BN + ch * 64, mb * BM + q * 32);
-          buf ^= 1;
+          stage_and_store(stg, pk, lane, &tmC, nb * BN + col, mb * BM + q * 32);
         }
-        acc ^= 1;
+        acc = (acc + 1 == ACC) ? 0 : acc + 1;
         if (acc == 0) acc_phase ^= 1u;
       }
     } else {
-      const int h = ew >> 2;  // which 128-column half of the tile this warp folds
+      // each warp folds 64 columns (one 128-column scale block = BN / 128 ... of them) of its
+      // TMEM lane quarter: two x32 loads issued back to back, one wait, 64 FMAs
+      const int col0 = (ew >> 2) * 64;
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
         int mb, nb;
         tile_coords(t, p, mb, nb);
         const int row = mb * BM + q * 32 + lane;
-        const int nblk = nb * (BN / 128) + h;
+        const int nblk = (nb * BN + col0) / 128;
         const bool row_ok = row < p.M;
         const bool col_ok = nblk * 128 < p.N;
-        float accum[128];
+        float accum[64];
 #pragma unroll
-        for (int j = 0; j < 128; ++j) accum[j] = 0.0f;
+        for (int j = 0; j < 64; ++j) accum[j] = 0.0f;
         float sa_next = row_ok ? __ldg(p.sa + (int64_t)row * p.sa_ld) : 0.0f;
         float sb_next = col_ok ? __ldg(p.sb + nblk) : 0.0f;
         for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -317,32 +324,31 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
           }
           __syncwarp();
           tc_fence_after();
-          const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + h * 128);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld32(taddr + 32 * c, r);
-            tmem_ld_wait();
-            reg_fence(r);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) accum[32 * c + j] = fmaf(__uint_as_float(r[j]), sc, accum[32 * c + j]);
-          }
+          const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0);
+          uint32_t r0[32], r1[32];
+          tmem_ld32(taddr, r0);
+          tmem_ld32(taddr + 32, r1);
+          tmem_ld_wait();
+          reg_fence(r0);
+          reg_fence(r1);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
-          acc ^= 1;
+          if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);  // registers hold the block now
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            accum[j] = fmaf(__uint_as_float(r0[j]), sc, accum[j]);
+            accum[32 + j] = fmaf(__uint_as_float(r1[j]), sc, accum[32 + j]);
+          }
+          acc = (acc + 1 == ACC) ? 0 : acc + 1;
           if (acc == 0) acc_phase ^= 1u;
         }
         if (!ok) break;
+        uint32_t pk[32];
 #pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(accum[64 * ch + 2 * j], accum[64 * ch + 2 * j + 1]);
-          if (lane == 0) bulk_wait_group_read<0>();
-          __syncwarp();
-          stage_and_store(stg, pk, lane, &tmC, nb * BN + h * 128 + ch * 64, mb * BM + q * 32);
-        }
+        for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(accum[2 * j], accum[2 * j + 1]);
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+        stage_and_store(stg, pk, lane, &tmC, nb * BN + col0, mb * BM + q * 32);
       }
     }
     if (lane == 0) bulk_wait_group<0>();
@@ -440,7 +446,13 @@ cudaError_t launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const C
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why) {
-  const int bn = choose_bn(g.M, g.N, num_sms());
+  // block scaling folds every 128-deep K block out of TMEM: 128-wide tiles keep the fold's
+  // registers (64 fp32 per thread) and its four accumulator buffers within budget
+#ifdef FP8GB_FORCE_BN  // compile-time override of the tile-width heuristic, for tuning builds
+  const int bn = g.block_scaled ? 128 : FP8GB_FORCE_BN;
+#else
+  const int bn = g.block_scaled ? 128 : choose_bn(g.M, g.N, num_sms());
+#endif
   CUtensorMap ta, tb, tc;
   if (!make_map(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.M, g.lda, BK, BM) ||
       !make_map(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.N, g.ldb, BK, bn) ||
@@ -464,9 +476,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why
     *why = "device error word unavailable";
     return cudaErrorInvalidDevice;
   }
-  if (g.block_scaled) {
-    return bn == 256 ? launch_variant<true, 256>(ta, tb, tc, p, stream) : launch_variant<true, 128>(ta, tb, tc, p, stream);
-  }
+  if (g.block_scaled) return launch_variant<true, 128>(ta, tb, tc, p, stream);
   return bn == 256 ? launch_variant<false, 256>(ta, tb, tc, p, stream) : launch_variant<false, 128>(ta, tb, tc, p, stream);
 }
 
