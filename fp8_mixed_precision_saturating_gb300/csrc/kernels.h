@@ -8,6 +8,25 @@
 
 namespace fp8gb {
 
+// Launch `kernel` on `stream` with programmatic stream serialization: it may begin while the
+// previous kernel on the stream finishes; it waits for that kernel (pdl_wait) before it
+// reads or writes global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Device pointers of one tensor role's scaling state (see fp8_tensor_state_t).
 struct QuantState {
   float* hist;

@@ -33,6 +33,16 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 }
 
 // ---------------------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------------------
+// Every kernel of the library is launched so that the next kernel on the stream may start
+// before it ends. A kernel lets its dependent launch as soon as all its CTAs have started
+// (pdl_trigger) and waits, before its first global-memory access, until the kernel before it
+// has completed and its writes are visible (pdl_wait). Outside such a launch both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -7,14 +7,21 @@
 // divided by its scale before the cast).
 //
 // Arithmetic, identical in every kernel:
-//   amax  = max |x| over the unit, NaN ignored (integer max over the bf16 magnitude bits)
-//   s     = FP8_MAX / amax, d = amax / FP8_MAX (IEEE fp32 divisions), or 1, 1 when amax is
-//           zero or not finite
+//   amax  = max |x| over the unit, NaN ignored
+//   s     = FP8_MAX / amax, d = amax / FP8_MAX (IEEE fp32 divisions); 1, 1 when amax is
+//           zero or not finite, or when the quotient overflows fp32 (subnormal amax)
 //   code  = cvt.rn.satfinite(x * s) (one fp32 multiply), NaN -> 0x7F
 //   overflow  counts |x * s| > FP8_MAX; underflow counts x != 0 whose code is +-0.
+//
+// The casts are issue-bound if every element pays for its counter and NaN checks, so each
+// vector of 8 first compares its largest and smallest magnitude with two exact thresholds
+// (see make_scaler) and takes a check-free path when nothing in it can saturate, flush to
+// zero or be NaN.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -30,10 +37,12 @@ struct Fmt;
 template <>
 struct Fmt<0> {
   static constexpr float kMax = 448.0f;
+  static constexpr float kHalfMinSub = 9.765625e-4f;  // 2^-10: half the smallest subnormal
 };
 template <>
 struct Fmt<1> {
   static constexpr float kMax = 57344.0f;
+  static constexpr float kHalfMinSub = 7.62939453125e-6f;  // 2^-17
 };
 
 // Two fp32 values -> two codes, byte 0 from `lo`, byte 1 from `hi`.
@@ -49,25 +58,45 @@ __device__ __forceinline__ uint32_t cvt2(float lo, float hi) {
 }
 
 __device__ __forceinline__ void scales_from_amax(float a, float fmax, float& s, float& d) {
+  s = 1.0f;
+  d = 1.0f;
   if (a > 0.0f && a <= 3.402823466e38f) {
-    s = __fdiv_rn(fmax, a);
-    d = __fdiv_rn(a, fmax);
-  } else {
-    s = 1.0f;
-    d = 1.0f;
+    const float si = __fdiv_rn(fmax, a);
+    if (si <= 3.402823466e38f) {  // a subnormal amax can overflow the quotient: keep 1, 1
+      s = si;
+      d = __fdiv_rn(a, fmax);
+    }
   }
 }
 
-// max of the bf16 magnitudes (NaN lanes zeroed) of a 32-bit word holding two bf16.
-__device__ __forceinline__ uint32_t absmax2(uint32_t m, uint32_t w) {
-  const uint32_t a = w & 0x7FFF7FFFu;
-  const uint32_t nan = __vcmpgtu2(a, 0x7F807F80u);
-  return __vmaxu2(m, a & ~nan);
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) {
+  __nv_bfloat162 r;
+  memcpy(&r, &u, sizeof(r));
+  return r;
 }
 
+__device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 b) {
+  uint32_t r;
+  memcpy(&r, &b, sizeof(r));
+  return r;
+}
+
+// Running max of |x| over words of two bf16, one max per half; NaN is ignored (the bf16
+// maximum returns the other operand, and the running value starts at +0 and is never NaN).
+__device__ __forceinline__ uint32_t absmax_h2(uint32_t m, uint32_t w) {
+  return as_u32(__hmax2(as_bf2(m), as_bf2(w & 0x7FFF7FFFu)));
+}
+
+__device__ __forceinline__ uint32_t absmax_v(uint32_t m, const uint4& v) {
+  return absmax_h2(absmax_h2(absmax_h2(absmax_h2(m, v.x), v.y), v.z), v.w);
+}
+
+// The larger half, as bf16 magnitude bits (non-negative bf16 order = integer order).
 __device__ __forceinline__ uint32_t fold2(uint32_t m) { return max(m & 0xFFFFu, m >> 16); }
 
-// Cast one word (two bf16) with counters. Returns the two codes in bits 0..15.
+// ---------------------------------------------------------------------------------------
+// exact per-element path (with counters and the canonical NaN code)
+// ---------------------------------------------------------------------------------------
 template <int FMT>
 __device__ __forceinline__ uint32_t cast_word(uint32_t w, float s, uint32_t& ov, uint32_t& un) {
   const float x0 = __uint_as_float(w << 16);
@@ -75,18 +104,15 @@ __device__ __forceinline__ uint32_t cast_word(uint32_t w, float s, uint32_t& ov,
   const float v0 = __fmul_rn(x0, s);
   const float v1 = __fmul_rn(x1, s);
   uint32_t c = cvt2<FMT>(v0, v1);
-  if (__vcmpgtu2(w & 0x7FFF7FFFu, 0x7F807F80u)) {  // a NaN among the two: canonical code
-    if (x0 != x0) c = (c & 0xFF00u) | 0x7Fu;
-    if (x1 != x1) c = (c & 0x00FFu) | 0x7F00u;
-  }
+  if (x0 != x0) c = (c & 0xFF00u) | 0x7Fu;
+  if (x1 != x1) c = (c & 0x00FFu) | 0x7F00u;
   ov += (fabsf(v0) > Fmt<FMT>::kMax) + (fabsf(v1) > Fmt<FMT>::kMax);
   un += ((x0 != 0.0f) & ((c & 0x7Fu) == 0u)) + ((x1 != 0.0f) & ((c & 0x7F00u) == 0u));
   return c;
 }
 
-// 8 bf16 -> 8 codes.
 template <int FMT>
-__device__ __forceinline__ uint2 cast8(uint4 v, float s, uint32_t& ov, uint32_t& un) {
+__device__ __forceinline__ uint2 cast8_exact(uint4 v, float s, uint32_t& ov, uint32_t& un) {
   uint2 o;
   o.x = cast_word<FMT>(v.x, s, ov, un) | (cast_word<FMT>(v.y, s, ov, un) << 16);
   o.y = cast_word<FMT>(v.z, s, ov, un) | (cast_word<FMT>(v.w, s, ov, un) << 16);
@@ -104,7 +130,69 @@ __device__ __forceinline__ uint8_t cast1(uint16_t b, float s, uint32_t& ov, uint
   return static_cast<uint8_t>(c);
 }
 
-// Block-wide reductions (kThreads threads). `red` holds kThreads / 32 words.
+// ---------------------------------------------------------------------------------------
+// fast path
+// ---------------------------------------------------------------------------------------
+// T_ov is the largest bf16 magnitude whose scaled value fl32(|x| s) stays <= FP8_MAX, T_un
+// the largest whose scaled value is <= half the smallest subnormal (code +-0). Both are
+// exact: fl32(|x| s) and the cast are monotone in |x|, so |x| <= T_ov means no saturation
+// and |x| > T_un means no flush to zero. NaN fails both comparisons and zeros fail the
+// second, so such vectors, and any that may saturate or flush, take the exact path.
+struct Scaler {
+  float s;
+  __nv_bfloat162 tov;
+  __nv_bfloat162 tun;
+};
+
+// Largest bf16 magnitude bits b (0 .. 0x7F7F) with fl32(bf16(b) * s) <= target. `d` is the
+// reciprocal scale, so fl32(target * d) lands within a few fp32 ulps of target / s and the
+// two exact adjustment loops move by at most a step or two.
+__device__ __forceinline__ uint32_t bf16_threshold(float s, float d, float target) {
+  const float q = __fmul_rn(target, d);
+  uint32_t b = min(__float_as_uint(q) >> 16, 0x7F7Fu);
+  while (b < 0x7F7Fu && __fmul_rn(__uint_as_float((b + 1u) << 16), s) <= target) ++b;
+  while (b > 0u && __fmul_rn(__uint_as_float(b << 16), s) > target) --b;
+  return b;
+}
+
+template <int FMT>
+__device__ __forceinline__ Scaler make_scaler(float s, float d) {
+  Scaler c;
+  c.s = s;
+  const uint32_t tov = bf16_threshold(s, d, Fmt<FMT>::kMax);
+  const uint32_t tun = bf16_threshold(s, d, Fmt<FMT>::kHalfMinSub);
+  c.tov = as_bf2(tov | (tov << 16));
+  c.tun = as_bf2(tun | (tun << 16));
+  return c;
+}
+
+// 8 bf16 -> 8 codes with exact counters; with AMAX, `am` accumulates max |x| (NaN ignored)
+// as two bf16 magnitudes.
+template <int FMT, bool AMAX>
+__device__ __forceinline__ uint2 cast8(uint4 v, const Scaler& c, uint32_t& ov, uint32_t& un, uint32_t& am) {
+  const __nv_bfloat162 b0 = as_bf2(v.x & 0x7FFF7FFFu), b1 = as_bf2(v.y & 0x7FFF7FFFu);
+  const __nv_bfloat162 b2 = as_bf2(v.z & 0x7FFF7FFFu), b3 = as_bf2(v.w & 0x7FFF7FFFu);
+  const __nv_bfloat162 mx = __hmax2_nan(__hmax2_nan(b0, b1), __hmax2_nan(b2, b3));
+  const __nv_bfloat162 mn = __hmin2_nan(__hmin2_nan(b0, b1), __hmin2_nan(b2, b3));
+  if (__hble2(mx, c.tov) && __hbgt2(mn, c.tun)) {
+    if constexpr (AMAX) am = as_u32(__hmax2(as_bf2(am), mx));
+    const float s = c.s;
+    uint2 o;
+    o.x = cvt2<FMT>(__fmul_rn(__uint_as_float(v.x << 16), s), __fmul_rn(__uint_as_float(v.x & 0xFFFF0000u), s)) |
+          (cvt2<FMT>(__fmul_rn(__uint_as_float(v.y << 16), s), __fmul_rn(__uint_as_float(v.y & 0xFFFF0000u), s))
+           << 16);
+    o.y = cvt2<FMT>(__fmul_rn(__uint_as_float(v.z << 16), s), __fmul_rn(__uint_as_float(v.z & 0xFFFF0000u), s)) |
+          (cvt2<FMT>(__fmul_rn(__uint_as_float(v.w << 16), s), __fmul_rn(__uint_as_float(v.w & 0xFFFF0000u), s))
+           << 16);
+    return o;
+  }
+  if constexpr (AMAX) am = absmax_v(am, v);
+  return cast8_exact<FMT>(v, c.s, ov, un);
+}
+
+// ---------------------------------------------------------------------------------------
+// block-wide reductions (kThreads threads); `red` holds 2 * kThreads / 32 words
+// ---------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
   v = __reduce_max_sync(0xFFFFFFFFu, v);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
@@ -155,12 +243,18 @@ __device__ __forceinline__ float effective_amax(const QuantState& st, bool delay
   return *st.amax_cur;
 }
 
+__device__ __forceinline__ void atomic_max_amax(float* amax, uint32_t bf16_bits) {
+  if (bf16_bits != 0) atomicMax(reinterpret_cast<unsigned int*>(amax), bf16_bits << 16);
+}
+
 // ---------------------------------------------------------------------------------------
 // amax pass (per tensor)
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
                                                         int64_t ld, float* amax_out, const int32_t* gate_count) {
-  __shared__ uint32_t red[kThreads / 32];
+  __shared__ uint32_t red[2 * kThreads / 32];
+  pdl_wait();
+  pdl_trigger();
   if (gate_count != nullptr && *gate_count != 0) return;  // delayed mode past bootstrap
   uint32_t m = 0;
   const int64_t tid = blockIdx.x * (int64_t)kThreads + threadIdx.x;
@@ -175,19 +269,16 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
 #pragma unroll
       for (int u = 0; u < 4; ++u) v[u] = __ldcs(xv + i + u * nth);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) m = absmax2(absmax2(absmax2(absmax2(m, v[u].x), v[u].y), v[u].z), v[u].w);
+      for (int u = 0; u < 4; ++u) m = absmax_v(m, v[u]);
     }
-    for (; i < nv; i += nth) {
-      const uint4 v = __ldcs(xv + i);
-      m = absmax2(absmax2(absmax2(absmax2(m, v.x), v.y), v.z), v.w);
-    }
-    for (int64_t j = nv * 8 + tid; j < n; j += nth) m = absmax2(m, x[j]);
+    for (; i < nv; i += nth) m = absmax_v(m, __ldcs(xv + i));
+    for (int64_t j = nv * 8 + tid; j < n; j += nth) m = absmax_h2(m, x[j]);
   } else {
     const int64_t n = rows * cols;
-    for (int64_t j = tid; j < n; j += nth) m = absmax2(m, x[(j / cols) * ld + (j % cols)]);
+    for (int64_t j = tid; j < n; j += nth) m = absmax_h2(m, x[(j / cols) * ld + (j % cols)]);
   }
   const uint32_t b = block_max_u32(fold2(m), red);
-  if (threadIdx.x == 0 && b != 0) atomicMax(reinterpret_cast<unsigned int*>(amax_out), b << 16);
+  if (threadIdx.x == 0) atomic_max_amax(amax_out, b);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -198,12 +289,15 @@ __global__ void __launch_bounds__(kThreads) cast_flat_kernel(const uint16_t* __r
                                                              int64_t cols, int64_t ld, uint8_t* __restrict__ q,
                                                              QuantState st) {
   __shared__ uint32_t red[2 * kThreads / 32];
+  pdl_wait();
+  pdl_trigger();
   float s, d;
   scales_from_amax(effective_amax(st, DELAYED), Fmt<FMT>::kMax, s, d);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     *st.scale = s;
     *st.scale_inv = d;
   }
+  const Scaler sc = make_scaler<FMT>(s, d);
   uint32_t ov = 0, un = 0, m = 0;
   const int64_t tid = blockIdx.x * (int64_t)kThreads + threadIdx.x;
   const int64_t nth = (int64_t)gridDim.x * kThreads;
@@ -222,27 +316,19 @@ __global__ void __launch_bounds__(kThreads) cast_flat_kernel(const uint16_t* __r
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        if constexpr (DELAYED) {
-          m = absmax2(absmax2(absmax2(absmax2(m, a[u][0].x), a[u][0].y), a[u][0].z), a[u][0].w);
-          m = absmax2(absmax2(absmax2(absmax2(m, a[u][1].x), a[u][1].y), a[u][1].z), a[u][1].w);
-        }
-        const uint2 lo = cast8<FMT>(a[u][0], s, ov, un);
-        const uint2 hi = cast8<FMT>(a[u][1], s, ov, un);
-        __stcs(qv + i + u * nth, make_uint4(lo.x, lo.y, hi.x, hi.y));
+        const uint2 lo = cast8<FMT, DELAYED>(a[u][0], sc, ov, un, m);
+        const uint2 hi = cast8<FMT, DELAYED>(a[u][1], sc, ov, un, m);
+        qv[i + u * nth] = make_uint4(lo.x, lo.y, hi.x, hi.y);
       }
     }
     for (; i < nv; i += nth) {
       const uint4 a0 = __ldcs(xv + 2 * i), a1 = __ldcs(xv + 2 * i + 1);
-      if constexpr (DELAYED) {
-        m = absmax2(absmax2(absmax2(absmax2(m, a0.x), a0.y), a0.z), a0.w);
-        m = absmax2(absmax2(absmax2(absmax2(m, a1.x), a1.y), a1.z), a1.w);
-      }
-      const uint2 lo = cast8<FMT>(a0, s, ov, un);
-      const uint2 hi = cast8<FMT>(a1, s, ov, un);
-      __stcs(qv + i, make_uint4(lo.x, lo.y, hi.x, hi.y));
+      const uint2 lo = cast8<FMT, DELAYED>(a0, sc, ov, un, m);
+      const uint2 hi = cast8<FMT, DELAYED>(a1, sc, ov, un, m);
+      qv[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
     for (int64_t j = nv * 16 + tid; j < n; j += nth) {
-      if constexpr (DELAYED) m = absmax2(m, x[j]);
+      if constexpr (DELAYED) m = absmax_h2(m, x[j]);
       q[j] = cast1<FMT>(x[j], s, ov, un);
     }
   } else {
@@ -250,21 +336,21 @@ __global__ void __launch_bounds__(kThreads) cast_flat_kernel(const uint16_t* __r
     for (int64_t j = tid; j < n; j += nth) {
       const int64_t r = j / cols, c = j % cols;
       const uint16_t b = x[r * ld + c];
-      if constexpr (DELAYED) m = absmax2(m, b);
+      if constexpr (DELAYED) m = absmax_h2(m, b);
       q[r * cols + c] = cast1<FMT>(b, s, ov, un);
     }
   }
   block_add_counters(ov, un, st.counters, red);
   if constexpr (DELAYED) {
     const uint32_t b = block_max_u32(fold2(m), red);
-    if (threadIdx.x == 0 && b != 0) atomicMax(reinterpret_cast<unsigned int*>(st.amax_cur), b << 16);
+    if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
   }
 }
 
 // ---------------------------------------------------------------------------------------
 // 128 x 128 tile cast: row-major and/or transposed codes; per-tensor or per-block scale
 // ---------------------------------------------------------------------------------------
-// 8x8 byte transpose: in[r] = {lo, hi} holds row r (bytes c0..c7); out[c] the column c.
+// 4x4 byte transpose of the words a0..a3 (row r = bytes of a_r) into t0..t3 (columns).
 __device__ __forceinline__ void transpose4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t& t0,
                                            uint32_t& t1, uint32_t& t2, uint32_t& t3) {
   const uint32_t x0 = __byte_perm(a0, a1, 0x5140), x1 = __byte_perm(a0, a1, 0x7362);
@@ -275,6 +361,7 @@ __device__ __forceinline__ void transpose4(uint32_t a0, uint32_t a1, uint32_t a2
   t3 = __byte_perm(x1, y1, 0x7632);
 }
 
+// 8x8 byte transpose: in[r] = {lo, hi} holds row r (bytes c0..c7); out[c] the column c.
 __device__ __forceinline__ void transpose8x8(const uint2 (&in)[8], uint2 (&out)[8]) {
   uint32_t t[4];
   transpose4(in[0].x, in[1].x, in[2].x, in[3].x, t[0], t[1], t[2], t[3]);
@@ -304,25 +391,24 @@ __global__ void __launch_bounds__(kThreads) cast_tile_kernel(const uint16_t* __r
   const int64_t r0 = (int64_t)blockIdx.y * 128 + rg * 8;
   const int64_t c0 = (int64_t)blockIdx.x * 128 + cg * 8;
   const bool in = (r0 < rows) && (c0 < cols);
+  pdl_wait();
+  pdl_trigger();
 
   uint4 v[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     v[i] = in ? __ldcs(reinterpret_cast<const uint4*>(x + (r0 + i) * ld + c0)) : make_uint4(0, 0, 0, 0);
   }
-  uint32_t m = 0;
-  if constexpr (SK != kTensorCurrent) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m = absmax2(absmax2(absmax2(absmax2(m, v[i].x), v[i].y), v[i].z), v[i].w);
-  }
   float s, d;
   if constexpr (SK == kBlock) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = absmax_v(m, v[i]);
     const uint32_t b = block_max_u32(fold2(m), red);
-    const float a = __uint_as_float(b << 16);
-    scales_from_amax(a, Fmt<FMT>::kMax, s, d);
+    scales_from_amax(__uint_as_float(b << 16), Fmt<FMT>::kMax, s, d);
     if (t == 0) {
       unit_scale_inv[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = d;
-      if (st.amax_cur != nullptr && b != 0) atomicMax(reinterpret_cast<unsigned int*>(st.amax_cur), b << 16);
+      if (st.amax_cur != nullptr) atomic_max_amax(st.amax_cur, b);
     }
   } else {
     scales_from_amax(effective_amax(st, SK == kTensorDelayed), Fmt<FMT>::kMax, s, d);
@@ -331,15 +417,16 @@ __global__ void __launch_bounds__(kThreads) cast_tile_kernel(const uint16_t* __r
       *st.scale_inv = d;
     }
   }
+  const Scaler sc = make_scaler<FMT>(s, d);
 
-  uint32_t ov = 0, un = 0;
+  uint32_t ov = 0, un = 0, m = 0;
   uint2 c[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) c[i] = cast8<FMT>(v[i], s, ov, un);
+  for (int i = 0; i < 8; ++i) c[i] = cast8<FMT, SK == kTensorDelayed>(v[i], sc, ov, un, m);
   if (!in) ov = un = 0;
   if (in && q != nullptr) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) __stcs(reinterpret_cast<uint2*>(q + (r0 + i) * cols + c0), c[i]);
+    for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(q + (r0 + i) * cols + c0) = c[i];
   }
   if (qT != nullptr) {
     uint2 ct[8];
@@ -362,73 +449,79 @@ __global__ void __launch_bounds__(kThreads) cast_tile_kernel(const uint16_t* __r
       const int64_t gc = rowbase + j * 16;
       if (gr < cols && gc < rows) {
         const uint4 val = *reinterpret_cast<const uint4*>(tT + R * 128 + ((j ^ ((R >> 3) & 7)) * 16));
-        __stcs(reinterpret_cast<uint4*>(qT + gr * rows + gc), val);
+        *reinterpret_cast<uint4*>(qT + gr * rows + gc) = val;
       }
     }
   }
   if (st.counters != nullptr) block_add_counters(ov, un, st.counters, red);
   if constexpr (SK == kTensorDelayed) {
     const uint32_t b = block_max_u32(fold2(m), red);
-    if (t == 0 && b != 0) atomicMax(reinterpret_cast<unsigned int*>(st.amax_cur), b << 16);
+    if (t == 0) atomic_max_amax(st.amax_cur, b);
   }
 }
 
 // ---------------------------------------------------------------------------------------
-// 1 x 128 tile cast: one half-warp per tile, 8 elements per lane
+// 1 x 128 tile cast: four lanes per tile, 32 elements per lane
 // ---------------------------------------------------------------------------------------
+// Lane l of a tile's group of four loads the 16-byte chunks l, l+4, l+8, l+12 of the tile's
+// 256 bytes, so each load instruction reads 64 contiguous bytes per tile.
 template <int FMT>
 __global__ void __launch_bounds__(kThreads) cast_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                               int64_t cols, int64_t ld, uint8_t* __restrict__ q,
                                                               float* __restrict__ unit_scale_inv, QuantState st) {
   __shared__ uint32_t red[2 * kThreads / 32];
+  pdl_wait();
+  pdl_trigger();
   const int64_t tiles_per_row = cols / 128;
   const int64_t ntiles = rows * tiles_per_row;
-  const int lane = threadIdx.x & 31;
-  const int half = lane >> 4, hl = lane & 15;
-  const int64_t warp = (blockIdx.x * (int64_t)kThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  const int gl = threadIdx.x & 3;  // lane within the tile's group
+  const int64_t group = (blockIdx.x * (int64_t)kThreads + threadIdx.x) >> 2;
+  const int64_t ngroups = ((int64_t)gridDim.x * kThreads) >> 2;
   uint32_t ov = 0, un = 0, mall = 0;
-  constexpr int U = 2;  // tile pairs in flight per warp
-  for (int64_t base = warp * 2 * U; base < ntiles; base += nwarps * 2 * U) {
-    uint4 v[U];
-    int64_t tile[U];
+  // every lane of a warp runs the same number of iterations (the shuffles need it)
+  const int64_t warp_first = (group & ~int64_t(7));
+  for (int64_t base = warp_first; base < ntiles; base += ngroups) {
+    const int64_t tile = base + (group & 7);
+    const bool ok = tile < ntiles;
+    const int64_t r = ok ? tile / tiles_per_row : 0, tc = ok ? tile % tiles_per_row : 0;
+    const uint16_t* src = x + r * ld + tc * 128;
+    uint4 v[4];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      tile[u] = base + 2 * u + half;
-      if (tile[u] < ntiles) {
-        const int64_t r = tile[u] / tiles_per_row, tc = tile[u] % tiles_per_row;
-        v[u] = __ldcs(reinterpret_cast<const uint4*>(x + r * ld + tc * 128 + hl * 8));
-      } else {
-        v[u] = make_uint4(0, 0, 0, 0);
-      }
+    for (int j = 0; j < 4; ++j)
+      v[j] = ok ? __ldcs(reinterpret_cast<const uint4*>(src + (j * 4 + gl) * 8)) : make_uint4(0, 0, 0, 0);
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = absmax_v(m, v[j]);
+    m = fold2(m);
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    mall = max(mall, m);
+    float s, d;
+    scales_from_amax(__uint_as_float(m << 16), Fmt<FMT>::kMax, s, d);
+    const Scaler sc = make_scaler<FMT>(s, d);
+    uint32_t o1 = 0, u1 = 0, dummy = 0;
+    uint8_t* dst = q + r * cols + tc * 128;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint2 cq = cast8<FMT, false>(v[j], sc, o1, u1, dummy);
+      if (ok) *reinterpret_cast<uint2*>(dst + (j * 4 + gl) * 8) = cq;
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      uint32_t m = fold2(absmax2(absmax2(absmax2(absmax2(0u, v[u].x), v[u].y), v[u].z), v[u].w));
-#pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-      mall = max(mall, m);
-      float s, d;
-      scales_from_amax(__uint_as_float(m << 16), Fmt<FMT>::kMax, s, d);
-      uint32_t o1 = 0, u1 = 0;
-      const uint2 cq = cast8<FMT>(v[u], s, o1, u1);
-      if (tile[u] < ntiles) {
-        const int64_t r = tile[u] / tiles_per_row, tc = tile[u] % tiles_per_row;
-        __stcs(reinterpret_cast<uint2*>(q + r * cols + tc * 128 + hl * 8), cq);
-        if (hl == 0) unit_scale_inv[tile[u]] = d;
-        ov += o1;
-        un += u1;
-      }
+    if (ok) {
+      if (gl == 0) unit_scale_inv[tile] = d;
+      ov += o1;
+      un += u1;
     }
   }
   if (st.counters != nullptr) block_add_counters(ov, un, st.counters, red);
   if (st.amax_cur != nullptr) {
     const uint32_t b = block_max_u32(mall, red);
-    if (threadIdx.x == 0 && b != 0) atomicMax(reinterpret_cast<unsigned int*>(st.amax_cur), b << 16);
+    if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
   }
 }
 
 __global__ void history_commit_kernel(QuantState st) {
+  pdl_wait();
+  pdl_trigger();
   const int n = *st.hist_count;
   st.hist[n % st.hist_len] = *st.amax_cur;
   *st.hist_count = n + 1;
@@ -458,8 +551,8 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, f
                         const int32_t* gate_count, cudaStream_t stream) {
   const int sms = num_sms();
   const int g = grid_for(rows * cols, kThreads * 32, sms, 8);
-  amax_kernel<<<g, kThreads, 0, stream>>>(static_cast<const uint16_t*>(x), rows, cols, ld, amax_out, gate_count);
-  return cudaGetLastError();
+  return launch_pdl(amax_kernel, dim3(g), dim3(kThreads), 0, stream, static_cast<const uint16_t*>(x), rows, cols, ld,
+                    amax_out, gate_count);
 }
 
 cudaError_t launch_cast_flat(int fmt, bool delayed, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
@@ -468,14 +561,9 @@ cudaError_t launch_cast_flat(int fmt, bool delayed, const void* x, int64_t rows,
   const int g = grid_for(rows * cols, kThreads * 32, sms, 8);
   auto* xp = static_cast<const uint16_t*>(x);
   auto* qp = static_cast<uint8_t*>(q);
-  if (fmt == 0) {
-    if (delayed) cast_flat_kernel<0, true><<<g, kThreads, 0, stream>>>(xp, rows, cols, ld, qp, st);
-    else cast_flat_kernel<0, false><<<g, kThreads, 0, stream>>>(xp, rows, cols, ld, qp, st);
-  } else {
-    if (delayed) cast_flat_kernel<1, true><<<g, kThreads, 0, stream>>>(xp, rows, cols, ld, qp, st);
-    else cast_flat_kernel<1, false><<<g, kThreads, 0, stream>>>(xp, rows, cols, ld, qp, st);
-  }
-  return cudaGetLastError();
+  auto k = fmt == 0 ? (delayed ? cast_flat_kernel<0, true> : cast_flat_kernel<0, false>)
+                    : (delayed ? cast_flat_kernel<1, true> : cast_flat_kernel<1, false>);
+  return launch_pdl(k, dim3(g), dim3(kThreads), 0, stream, xp, rows, cols, ld, qp, st);
 }
 
 cudaError_t launch_cast_tiles(int fmt, int scale_kind, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
@@ -484,35 +572,26 @@ cudaError_t launch_cast_tiles(int fmt, int scale_kind, const void* x, int64_t ro
   auto* xp = static_cast<const uint16_t*>(x);
   auto* qp = static_cast<uint8_t*>(q);
   auto* tp = static_cast<uint8_t*>(qT);
-#define FP8GB_TILE_LAUNCH(F, S) cast_tile_kernel<F, S><<<grid, kThreads, 0, stream>>>(xp, rows, cols, ld, qp, tp, unit_scale_inv, st)
-  if (fmt == 0) {
-    if (scale_kind == kTensorCurrent) FP8GB_TILE_LAUNCH(0, kTensorCurrent);
-    else if (scale_kind == kTensorDelayed) FP8GB_TILE_LAUNCH(0, kTensorDelayed);
-    else FP8GB_TILE_LAUNCH(0, kBlock);
-  } else {
-    if (scale_kind == kTensorCurrent) FP8GB_TILE_LAUNCH(1, kTensorCurrent);
-    else if (scale_kind == kTensorDelayed) FP8GB_TILE_LAUNCH(1, kTensorDelayed);
-    else FP8GB_TILE_LAUNCH(1, kBlock);
-  }
-#undef FP8GB_TILE_LAUNCH
-  return cudaGetLastError();
+  using K = void (*)(const uint16_t*, int64_t, int64_t, int64_t, uint8_t*, uint8_t*, float*, QuantState);
+  const K table[2][3] = {{cast_tile_kernel<0, kTensorCurrent>, cast_tile_kernel<0, kTensorDelayed>, cast_tile_kernel<0, kBlock>},
+                         {cast_tile_kernel<1, kTensorCurrent>, cast_tile_kernel<1, kTensorDelayed>, cast_tile_kernel<1, kBlock>}};
+  return launch_pdl(table[fmt][scale_kind], grid, dim3(kThreads), 0, stream, xp, rows, cols, ld, qp, tp, unit_scale_inv,
+                    st);
 }
 
 cudaError_t launch_cast_1x128(int fmt, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
                               float* unit_scale_inv, const QuantState& st, cudaStream_t stream) {
   const int sms = num_sms();
   const int64_t ntiles = rows * (cols / 128);
-  const int g = grid_for(ntiles, 2 * (kThreads / 32) * 2, sms, 8);
+  const int g = grid_for(ntiles, kThreads / 4, sms, 8);
   auto* xp = static_cast<const uint16_t*>(x);
   auto* qp = static_cast<uint8_t*>(q);
-  if (fmt == 0) cast_1x128_kernel<0><<<g, kThreads, 0, stream>>>(xp, rows, cols, ld, qp, unit_scale_inv, st);
-  else cast_1x128_kernel<1><<<g, kThreads, 0, stream>>>(xp, rows, cols, ld, qp, unit_scale_inv, st);
-  return cudaGetLastError();
+  return launch_pdl(fmt == 0 ? cast_1x128_kernel<0> : cast_1x128_kernel<1>, dim3(g), dim3(kThreads), 0, stream, xp,
+                    rows, cols, ld, qp, unit_scale_inv, st);
 }
 
 cudaError_t launch_history_commit(const QuantState& st, cudaStream_t stream) {
-  history_commit_kernel<<<1, 1, 0, stream>>>(st);
-  return cudaGetLastError();
+  return launch_pdl(history_commit_kernel, dim3(1), dim3(1), 0, stream, st);
 }
 
 cudaError_t launch_selftest_wait(const WaitCtl& w, cudaStream_t stream) {

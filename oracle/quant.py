@@ -14,7 +14,7 @@ Sources:
 Definitions (readings where the pages leave a step open):
 * amax = max |x| over the scaling unit, NaN ignored, -0 counts as 0; 0 when empty.
 * current scaling: s = fl32(FP8_MAX / amax), d = fl32(amax / FP8_MAX) if amax is
-  finite and > 0, else s = d = 1.  Dividing by the scale d is taken as multiplying by
+  finite and > 0 and the quotient is finite, else s = d = 1.  Dividing by the scale d is taken as multiplying by
   s, so the cast is q = cast(fl32(float(x) * s)).
 * units: the whole tensor; a 1x128 row tile along the contraction dimension; a
   128x128 block.  Dimensions that are not multiples of 128 are not tiled.
@@ -51,11 +51,16 @@ def amax(x_bits: np.ndarray) -> np.float32:
 
 
 def scales_from_amax(a, fmt: str):
-    """(s, d) as float32 from an amax, per the current-scaling rule."""
+    """(s, d) as float32 from an amax, per the current-scaling rule. When FP8_MAX / amax
+    overflows float32 (a subnormal amax), the pair falls back to 1, 1 like a zero amax, so
+    that s * d stays 1 and zeros do not become NaN (0 * inf)."""
     a = np.float32(a)
     mx = np.float32(fp8.fp8_max(fmt))
     if np.isfinite(a) and a > 0:
-        return np.float32(mx / a), np.float32(a / mx)
+        with np.errstate(over="ignore"):
+            s = np.float32(mx / a)
+        if np.isfinite(s):
+            return s, np.float32(a / mx)
     return np.float32(1.0), np.float32(1.0)
 
 

@@ -273,3 +273,19 @@ def test_bounded_wait_reports_timeout(g):
     q = empty_u8(8, 8)
     g.fp8_quantize(x, 8, 8, 8, 0, g.FP8_GRAN_TENSOR, 0, st, q)
     torch.cuda.synchronize()
+
+
+def test_subnormal_amax_keeps_unit_scales(g):
+    """amax = the smallest bf16 subnormal: FP8_MAX / amax overflows float32, so the pair is
+    1, 1 (zeros stay zero codes instead of 0 * inf = NaN); codes and counters as the oracle."""
+    x = np.array([[0x0001, 0x0000, 0x8001, 0x8000] * 4] * 16, dtype=np.uint16)
+    for fi, fmt in FMTS:
+        for qT in (False, True):
+            st = g.TensorState()
+            q = empty_u8(16, 16)
+            t = empty_u8(16, 16) if qT else None
+            g.fp8_quantize(dev_bf16(x), 16, 16, 16, fi, g.FP8_GRAN_TENSOR, 0, st, q, t)
+            ref = quant.quantize_tensor(x, fmt)
+            assert ref["s"] == 1.0 and ref["d"] == 1.0
+            assert np.array_equal(host_u8(q), ref["q"])
+            check_state_tensor(st, ref, fmt, ref["overflow"], ref["underflow"])

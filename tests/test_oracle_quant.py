@@ -31,6 +31,14 @@ def test_scale_closed_forms():
     assert s == 896.0 and d == np.float32(0.5 / 448.0)
     for bad in (0.0, np.inf, np.nan):
         assert quant.scales_from_amax(np.float32(bad), fp8.E4M3) == (1.0, 1.0)
+    # a subnormal amax whose quotient overflows float32 behaves like a zero amax
+    tiny = np.float32(2.0 ** -133)  # the smallest bf16 subnormal
+    assert quant.scales_from_amax(tiny, fp8.E4M3) == (1.0, 1.0)
+    assert quant.scales_from_amax(tiny, fp8.E5M2) == (1.0, 1.0)
+    # the largest amax with a finite quotient keeps the rule
+    a = np.float32(2.0 ** -119)
+    s, d = quant.scales_from_amax(a, fp8.E4M3)
+    assert np.isfinite(s) and s == np.float32(np.float32(448.0) / a)
 
 
 @pytest.mark.parametrize("fmt,maxcode", [(fp8.E4M3, 0x7E), (fp8.E5M2, 0x7B)])
