@@ -54,6 +54,7 @@ _SIGS = {
     "fp8_linear_bwd": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _SP, _I, _P, _P, _P, _P, _P],
     "fp8_linear_bwd_noalloc": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _SP, _I, _P, _P, _P],
     "fp8_history_commit": [_SP, _P],
+    "fp8_history_commit_many": [_SP, ctypes.c_int32, _P],
     "fp8_poll_device_error": [],
     "fp8_set_wait_limit_ns": [ctypes.c_ulonglong],
     "fp8_selftest_wait_timeout": [ctypes.c_ulonglong, _P],
@@ -195,6 +196,12 @@ def fp8_linear_bwd_noalloc(dy, M, K, N, xqT_save, x_st, wq_kn, w_st, dy_st, mode
 
 def fp8_history_commit(st, stream=None):
     return _check(lib.fp8_history_commit(_state(st), _stream(stream)))
+
+
+def fp8_history_commit_many(states, stream=None):
+    """Push the amaxes of several distinct states in one launch (at most 32)."""
+    arr = (fp8_tensor_state_t * len(states))(*[st if isinstance(st, fp8_tensor_state_t) else st.c for st in states])
+    return _check(lib.fp8_history_commit_many(arr, len(states), _stream(stream)))
 
 
 def fp8_poll_device_error():

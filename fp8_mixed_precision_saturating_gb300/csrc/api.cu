@@ -140,18 +140,9 @@ fp8_status_t quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld
 
   if (gran == FP8_GRAN_TENSOR) {
     if ((s = check_state(st, mode, who)) != FP8_OK) return s;
-    if ((e = cudaMemsetAsync(st->amax_cur, 0, sizeof(float), stream)) != cudaSuccess) return cuda_fail(e, who);
-    if (n > 0) {
-      e = launch_amax(x, rows, cols, ld, st->amax_cur, mode == FP8_SCALE_DELAYED ? st->hist_count : nullptr, stream);
-      if (e != cudaSuccess) return cuda_fail(e, "amax kernel");
-    }
-    if (!tiled || n == 0) {
-      if (!contiguous && n > 0 && q == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: no output", who);
-      e = launch_cast_flat(fmt, mode == FP8_SCALE_DELAYED, x, rows, cols, ld, q, qs, stream);
-    } else {
-      e = launch_cast_tiles(fmt, mode == FP8_SCALE_DELAYED ? 1 : 0, x, rows, cols, ld, q, qT, nullptr, qs, stream);
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "cast kernel");
+    if (!tiled && !contiguous && n > 0 && q == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: no output", who);
+    e = launch_quant_tensor(fmt, mode == FP8_SCALE_DELAYED, tiled && n > 0, x, rows, cols, ld, q, qT, qs, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "quantise kernel");
     return FP8_OK;
   }
 
@@ -171,7 +162,7 @@ fp8_status_t quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld
     if (rows % 128 != 0 || cols % 128 != 0)
       return fail(FP8_ERR_UNSUPPORTED, "%s: 128x128 blocks need rows and cols multiples of 128", who);
     if (n == 0) return FP8_OK;
-    e = launch_cast_tiles(fmt, 2, x, rows, cols, ld, q, qT, unit_si, qs, stream);
+    e = launch_cast_blocks(fmt, x, rows, cols, ld, q, qT, unit_si, qs, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "cast kernel");
   return FP8_OK;
@@ -369,10 +360,27 @@ fp8_status_t fp8_linear_bwd_noalloc(const void* dy_bf16, int64_t M, int64_t K, i
 }
 
 fp8_status_t fp8_history_commit(const fp8_tensor_state_t* st, void* stream) {
-  if (st == nullptr || !st->amax_history || !st->hist_count || !st->amax_cur || st->hist_len <= 0)
-    return fail(FP8_ERR_INVALID_ARG, "fp8_history_commit: needs amax_history, hist_count, amax_cur, hist_len > 0");
-  cudaError_t e = launch_history_commit(to_qs(st), static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FP8_OK : cuda_fail(e, "fp8_history_commit");
+  return fp8_history_commit_many(st, 1, stream);
+}
+
+fp8_status_t fp8_history_commit_many(const fp8_tensor_state_t* states, int32_t n, void* stream) {
+  const char* who = "fp8_history_commit";
+  if (n < 0 || n > kMaxCommit) return fail(FP8_ERR_INVALID_ARG, "%s: 0 <= n <= %d states per call", who, kMaxCommit);
+  if (n > 0 && states == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: null states", who);
+  QuantStates sts{};
+  sts.n = n;
+  for (int i = 0; i < n; ++i) {
+    const fp8_tensor_state_t* st = states + i;
+    if (!st->amax_history || !st->hist_count || !st->amax_cur || st->hist_len <= 0)
+      return fail(FP8_ERR_INVALID_ARG, "%s: state %d needs amax_history, hist_count, amax_cur, hist_len > 0", who, i);
+    for (int j = 0; j < i; ++j)
+      if (states[j].hist_count == st->hist_count)
+        return fail(FP8_ERR_INVALID_ARG, "%s: state %d appears twice in one call", who, i);
+    sts.s[i] = to_qs(st);
+  }
+  if (n == 0) return FP8_OK;
+  cudaError_t e = launch_history_commit(sts, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FP8_OK : cuda_fail(e, who);
 }
 
 fp8_status_t fp8_poll_device_error(void) {

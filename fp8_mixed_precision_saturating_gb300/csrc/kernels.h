@@ -38,22 +38,30 @@ struct QuantState {
   int32_t hist_len;
 };
 
+// Up to 32 states pushed by one history-commit launch (distinct states, one thread each).
+constexpr int kMaxCommit = 32;
+struct QuantStates {
+  QuantState s[kMaxCommit];
+  int n;
+};
+
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
 
 // Device error word and wait limit for launches on the current device.
 WaitCtl wait_ctl();
 
-cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* amax_out,
-                        const int32_t* gate_count, cudaStream_t stream);
-cudaError_t launch_cast_flat(int fmt, bool delayed, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
-                             const QuantState& st, cudaStream_t stream);
-// scale_kind: 0 per-tensor current, 1 per-tensor delayed, 2 per 128x128 block.
-cudaError_t launch_cast_tiles(int fmt, int scale_kind, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
-                              void* qT, float* unit_scale_inv, const QuantState& st, cudaStream_t stream);
+// Per-tensor quantise in one cooperative launch: amax (when the call needs it), scale, cast
+// with counters. tiled: 128x128 tiles with q and/or the transposed copy qT (rows, cols, ld
+// multiples of 8); otherwise row-major q of any shape.
+cudaError_t launch_quant_tensor(int fmt, bool delayed, bool tiled, const void* x, int64_t rows, int64_t cols,
+                                int64_t ld, void* q, void* qT, const QuantState& st, cudaStream_t stream);
+// One scale per 128x128 block (full blocks), q and/or qT, inverse scales [rows/128, cols/128].
+cudaError_t launch_cast_blocks(int fmt, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q, void* qT,
+                               float* unit_scale_inv, const QuantState& st, cudaStream_t stream);
 cudaError_t launch_cast_1x128(int fmt, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
                               float* unit_scale_inv, const QuantState& st, cudaStream_t stream);
-cudaError_t launch_history_commit(const QuantState& st, cudaStream_t stream);
+cudaError_t launch_history_commit(const QuantStates& sts, cudaStream_t stream);
 cudaError_t launch_selftest_wait(const WaitCtl& w, cudaStream_t stream);
 
 // GEMM: C [M,N] bf16 = A [M,K] * B [N,K]^T with per-tensor (block_scaled = false: sa, sb

@@ -17,11 +17,15 @@
 // vector of 8 first compares its largest and smallest magnitude with two exact thresholds
 // (see make_scaler) and takes a check-free path when nothing in it can saturate, flush to
 // zero or be NaN.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -30,6 +34,7 @@ namespace fp8gb {
 
 namespace {
 
+namespace cg = cooperative_groups;
 constexpr int kThreads = 256;
 
 template <int FMT>
@@ -248,107 +253,7 @@ __device__ __forceinline__ void atomic_max_amax(float* amax, uint32_t bf16_bits)
 }
 
 // ---------------------------------------------------------------------------------------
-// amax pass (per tensor)
-// ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
-                                                        int64_t ld, float* amax_out, const int32_t* gate_count) {
-  __shared__ uint32_t red[2 * kThreads / 32];
-  pdl_wait();
-  pdl_trigger();
-  if (gate_count != nullptr && *gate_count != 0) return;  // delayed mode past bootstrap
-  uint32_t m = 0;
-  const int64_t tid = blockIdx.x * (int64_t)kThreads + threadIdx.x;
-  const int64_t nth = (int64_t)gridDim.x * kThreads;
-  if (ld == cols) {
-    const int64_t n = rows * cols;
-    const int64_t nv = n / 8;
-    const uint4* xv = reinterpret_cast<const uint4*>(x);
-    int64_t i = tid;
-    for (; i + 3 * nth < nv; i += 4 * nth) {
-      uint4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __ldcs(xv + i + u * nth);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) m = absmax_v(m, v[u]);
-    }
-    for (; i < nv; i += nth) m = absmax_v(m, __ldcs(xv + i));
-    for (int64_t j = nv * 8 + tid; j < n; j += nth) m = absmax_h2(m, x[j]);
-  } else {
-    const int64_t n = rows * cols;
-    for (int64_t j = tid; j < n; j += nth) m = absmax_h2(m, x[(j / cols) * ld + (j % cols)]);
-  }
-  const uint32_t b = block_max_u32(fold2(m), red);
-  if (threadIdx.x == 0) atomic_max_amax(amax_out, b);
-}
-
-// ---------------------------------------------------------------------------------------
-// per-tensor cast, row-major output (flat when contiguous)
-// ---------------------------------------------------------------------------------------
-template <int FMT, bool DELAYED>
-__global__ void __launch_bounds__(kThreads) cast_flat_kernel(const uint16_t* __restrict__ x, int64_t rows,
-                                                             int64_t cols, int64_t ld, uint8_t* __restrict__ q,
-                                                             QuantState st) {
-  __shared__ uint32_t red[2 * kThreads / 32];
-  pdl_wait();
-  pdl_trigger();
-  float s, d;
-  scales_from_amax(effective_amax(st, DELAYED), Fmt<FMT>::kMax, s, d);
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    *st.scale = s;
-    *st.scale_inv = d;
-  }
-  const Scaler sc = make_scaler<FMT>(s, d);
-  uint32_t ov = 0, un = 0, m = 0;
-  const int64_t tid = blockIdx.x * (int64_t)kThreads + threadIdx.x;
-  const int64_t nth = (int64_t)gridDim.x * kThreads;
-  if (ld == cols) {
-    const int64_t n = rows * cols;
-    const int64_t nv = n / 16;  // 16 elements per step: 2 x 16 B in, 16 B out
-    const uint4* xv = reinterpret_cast<const uint4*>(x);
-    uint4* qv = reinterpret_cast<uint4*>(q);
-    int64_t i = tid;
-    for (; i + nth < nv; i += 2 * nth) {
-      uint4 a[2][2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        a[u][0] = __ldcs(xv + 2 * (i + u * nth));
-        a[u][1] = __ldcs(xv + 2 * (i + u * nth) + 1);
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint2 lo = cast8<FMT, DELAYED>(a[u][0], sc, ov, un, m);
-        const uint2 hi = cast8<FMT, DELAYED>(a[u][1], sc, ov, un, m);
-        qv[i + u * nth] = make_uint4(lo.x, lo.y, hi.x, hi.y);
-      }
-    }
-    for (; i < nv; i += nth) {
-      const uint4 a0 = __ldcs(xv + 2 * i), a1 = __ldcs(xv + 2 * i + 1);
-      const uint2 lo = cast8<FMT, DELAYED>(a0, sc, ov, un, m);
-      const uint2 hi = cast8<FMT, DELAYED>(a1, sc, ov, un, m);
-      qv[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
-    }
-    for (int64_t j = nv * 16 + tid; j < n; j += nth) {
-      if constexpr (DELAYED) m = absmax_h2(m, x[j]);
-      q[j] = cast1<FMT>(x[j], s, ov, un);
-    }
-  } else {
-    const int64_t n = rows * cols;
-    for (int64_t j = tid; j < n; j += nth) {
-      const int64_t r = j / cols, c = j % cols;
-      const uint16_t b = x[r * ld + c];
-      if constexpr (DELAYED) m = absmax_h2(m, b);
-      q[r * cols + c] = cast1<FMT>(b, s, ov, un);
-    }
-  }
-  block_add_counters(ov, un, st.counters, red);
-  if constexpr (DELAYED) {
-    const uint32_t b = block_max_u32(fold2(m), red);
-    if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
-  }
-}
-
-// ---------------------------------------------------------------------------------------
-// 128 x 128 tile cast: row-major and/or transposed codes; per-tensor or per-block scale
+// 128 x 128 tiles: thread t handles rows 8*(t/16) .. +8 and columns 8*(t%16) .. +8
 // ---------------------------------------------------------------------------------------
 // 4x4 byte transpose of the words a0..a3 (row r = bytes of a_r) into t0..t3 (columns).
 __device__ __forceinline__ void transpose4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t& t0,
@@ -374,56 +279,29 @@ __device__ __forceinline__ void transpose8x8(const uint2 (&in)[8], uint2 (&out)[
   for (int c = 0; c < 4; ++c) out[4 + c].y = t[c];
 }
 
-enum ScaleKind { kTensorCurrent = 0, kTensorDelayed = 1, kBlock = 2 };
+// This thread's 8x8 patch of tile (ty, tx); zeros outside the tensor (rows, cols % 8 == 0,
+// so a patch is either wholly inside or wholly outside).
+__device__ __forceinline__ bool load_patch(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
+                                           int64_t ty, int64_t tx, uint4 (&v)[8]) {
+  const int t = threadIdx.x;
+  const int64_t r0 = ty * 128 + (t >> 4) * 8;
+  const int64_t c0 = tx * 128 + (t & 15) * 8;
+  const bool in = (r0 < rows) && (c0 < cols);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    v[i] = in ? __ldcs(reinterpret_cast<const uint4*>(x + (r0 + i) * ld + c0)) : make_uint4(0, 0, 0, 0);
+  return in;
+}
 
-// Each CTA covers one 128x128 tile; thread t handles rows 8*(t/16) .. +8 and columns
-// 8*(t%16) .. +8 of it. Requires rows % 8 == 0 and cols % 8 == 0 (and, for the block
-// scale, full tiles; for the transposed output, rows % 16 == 0).
-template <int FMT, int SK>
-__global__ void __launch_bounds__(kThreads) cast_tile_kernel(const uint16_t* __restrict__ x, int64_t rows,
-                                                             int64_t cols, int64_t ld, uint8_t* __restrict__ q,
-                                                             uint8_t* __restrict__ qT, float* unit_scale_inv,
-                                                             QuantState st) {
-  __shared__ __align__(128) uint8_t tT[128 * 128];
-  __shared__ uint32_t red[2 * kThreads / 32];
+// Write the patch's codes row-major into q [rows, cols] and transposed into qT [cols, rows]
+// (through the CTA's shared buffer tT; every thread of the CTA must call this).
+__device__ __forceinline__ void store_patch(const uint2 (&c)[8], bool in, int64_t rows, int64_t cols, int64_t ty,
+                                            int64_t tx, uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
+                                            uint8_t* tT) {
   const int t = threadIdx.x;
   const int cg = t & 15, rg = t >> 4;
-  const int64_t r0 = (int64_t)blockIdx.y * 128 + rg * 8;
-  const int64_t c0 = (int64_t)blockIdx.x * 128 + cg * 8;
-  const bool in = (r0 < rows) && (c0 < cols);
-  pdl_wait();
-  pdl_trigger();
-
-  uint4 v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[i] = in ? __ldcs(reinterpret_cast<const uint4*>(x + (r0 + i) * ld + c0)) : make_uint4(0, 0, 0, 0);
-  }
-  float s, d;
-  if constexpr (SK == kBlock) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m = absmax_v(m, v[i]);
-    const uint32_t b = block_max_u32(fold2(m), red);
-    scales_from_amax(__uint_as_float(b << 16), Fmt<FMT>::kMax, s, d);
-    if (t == 0) {
-      unit_scale_inv[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = d;
-      if (st.amax_cur != nullptr) atomic_max_amax(st.amax_cur, b);
-    }
-  } else {
-    scales_from_amax(effective_amax(st, SK == kTensorDelayed), Fmt<FMT>::kMax, s, d);
-    if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
-      *st.scale = s;
-      *st.scale_inv = d;
-    }
-  }
-  const Scaler sc = make_scaler<FMT>(s, d);
-
-  uint32_t ov = 0, un = 0, m = 0;
-  uint2 c[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) c[i] = cast8<FMT, SK == kTensorDelayed>(v[i], sc, ov, un, m);
-  if (!in) ov = un = 0;
+  const int64_t r0 = ty * 128 + rg * 8;
+  const int64_t c0 = tx * 128 + cg * 8;
   if (in && q != nullptr) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(q + (r0 + i) * cols + c0) = c[i];
@@ -439,25 +317,193 @@ __global__ void __launch_bounds__(kThreads) cast_tile_kernel(const uint16_t* __r
       *reinterpret_cast<uint2*>(tT + R * 128 + chunk * 16 + (rg & 1) * 8) = ct[cc];
     }
     __syncthreads();
-    const int64_t colbase = (int64_t)blockIdx.x * 128;  // rows of qT
-    const int64_t rowbase = (int64_t)blockIdx.y * 128;  // columns of qT
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
       const int R = p * 32 + (t >> 3);
       const int j = t & 7;
-      const int64_t gr = colbase + R;
-      const int64_t gc = rowbase + j * 16;
+      const int64_t gr = tx * 128 + R;      // row of qT
+      const int64_t gc = ty * 128 + j * 16; // column of qT
       if (gr < cols && gc < rows) {
         const uint4 val = *reinterpret_cast<const uint4*>(tT + R * 128 + ((j ^ ((R >> 3) & 7)) * 16));
         *reinterpret_cast<uint4*>(qT + gr * rows + gc) = val;
       }
     }
+    __syncthreads();  // tT is reused by the next tile
   }
-  if (st.counters != nullptr) block_add_counters(ov, un, st.counters, red);
-  if constexpr (SK == kTensorDelayed) {
+}
+
+// ---------------------------------------------------------------------------------------
+// per-tensor quantise: one cooperative launch (every CTA resident, grid-wide syncs)
+// ---------------------------------------------------------------------------------------
+//   1. CTA 0 zeroes amax_cur. If the call needs the tensor's own amax (current scaling, or
+//      delayed scaling before the history holds an entry) every CTA reduces max |x| over its
+//      share; sync; the CTA maxima go into amax_cur with atomicMax; sync. Otherwise one sync
+//      orders the zeroing before the cast's own atomicMax.
+//   2. s and d from amax_cur or from the history; CTA 0 stores them.
+//   3. every CTA casts its share (the second read of x comes from L2 when x fits in it),
+//      counts, and in delayed scaling past bootstrap accumulates the current amax.
+__device__ __forceinline__ bool needs_amax_pass(const QuantState& st, int delayed) {
+  return !delayed || *st.hist_count == 0;
+}
+
+__device__ __forceinline__ float call_amax(const QuantState& st, int delayed) {
+  return effective_amax(st, delayed != 0);
+}
+
+// Tiled layout: rows, cols and ld multiples of 8 (rows of 16 with qT); q and/or qT.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                      int64_t cols, int64_t ld, uint8_t* __restrict__ q,
+                                                                      uint8_t* __restrict__ qT, QuantState st,
+                                                                      int delayed) {
+  __shared__ __align__(128) uint8_t tT[128 * 128];
+  __shared__ uint32_t red[2 * kThreads / 32];
+  cg::grid_group grid = cg::this_grid();
+  const int64_t tiles_x = (cols + 127) / 128;
+  const int64_t ntiles = tiles_x * ((rows + 127) / 128);
+  const bool pass = needs_amax_pass(st, delayed);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *st.amax_cur = 0.0f;
+  if (pass) {
+    uint32_t m = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      uint4 v[8];
+      load_patch(x, rows, cols, ld, t / tiles_x, t % tiles_x, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = absmax_v(m, v[i]);
+    }
     const uint32_t b = block_max_u32(fold2(m), red);
-    if (t == 0) atomic_max_amax(st.amax_cur, b);
+    grid.sync();
+    if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
   }
+  grid.sync();
+  float s, d;
+  scales_from_amax(call_amax(st, delayed), Fmt<FMT>::kMax, s, d);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *st.scale = s;
+    *st.scale_inv = d;
+  }
+  const Scaler sc = make_scaler<FMT>(s, d);
+  uint32_t ov = 0, un = 0, m = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t ty = t / tiles_x, tx = t % tiles_x;
+    uint4 v[8];
+    const bool in = load_patch(x, rows, cols, ld, ty, tx, v);
+    uint2 c[8];
+    uint32_t o1 = 0, u1 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = cast8<FMT, true>(v[i], sc, o1, u1, m);
+    if (in) {
+      ov += o1;
+      un += u1;
+    }
+    store_patch(c, in, rows, cols, ty, tx, q, qT, tT);
+  }
+  block_add_counters(ov, un, st.counters, red);
+  if (!pass) {  // delayed scaling past bootstrap: this cast measures the current amax
+    const uint32_t b = block_max_u32(fold2(m), red);
+    if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
+  }
+}
+
+// Row-major layout of any shape (vector path when contiguous, element path otherwise).
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) quant_tensor_flat_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                     int64_t cols, int64_t ld,
+                                                                     uint8_t* __restrict__ q, QuantState st,
+                                                                     int delayed) {
+  __shared__ uint32_t red[2 * kThreads / 32];
+  cg::grid_group grid = cg::this_grid();
+  const int64_t tid = blockIdx.x * (int64_t)kThreads + threadIdx.x;
+  const int64_t nth = (int64_t)gridDim.x * kThreads;
+  const int64_t n = rows * cols;
+  const bool flat = (ld == cols);
+  const int64_t nv = flat ? n / 16 : 0;  // 16 elements per step: 2 x 16 B in, 16 B out
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  const bool pass = needs_amax_pass(st, delayed);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *st.amax_cur = 0.0f;
+  if (pass) {
+    uint32_t m = 0;
+    for (int64_t i = tid; i < nv; i += nth) m = absmax_v(absmax_v(m, __ldcs(xv + 2 * i)), __ldcs(xv + 2 * i + 1));
+    for (int64_t j = nv * 16 + tid; j < n; j += nth) m = absmax_h2(m, x[flat ? j : (j / cols) * ld + j % cols]);
+    const uint32_t b = block_max_u32(fold2(m), red);
+    grid.sync();
+    if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
+  }
+  grid.sync();
+  float s, d;
+  scales_from_amax(call_amax(st, delayed), Fmt<FMT>::kMax, s, d);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *st.scale = s;
+    *st.scale_inv = d;
+  }
+  const Scaler sc = make_scaler<FMT>(s, d);
+  uint32_t ov = 0, un = 0, m = 0;
+  uint4* qv = reinterpret_cast<uint4*>(q);
+  int64_t i = tid;
+  for (; i + nth < nv; i += 2 * nth) {
+    uint4 a[2][2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      a[u][0] = __ldcs(xv + 2 * (i + u * nth));
+      a[u][1] = __ldcs(xv + 2 * (i + u * nth) + 1);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint2 lo = cast8<FMT, true>(a[u][0], sc, ov, un, m);
+      const uint2 hi = cast8<FMT, true>(a[u][1], sc, ov, un, m);
+      qv[i + u * nth] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+  }
+  for (; i < nv; i += nth) {
+    const uint2 lo = cast8<FMT, true>(__ldcs(xv + 2 * i), sc, ov, un, m);
+    const uint2 hi = cast8<FMT, true>(__ldcs(xv + 2 * i + 1), sc, ov, un, m);
+    qv[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+  }
+  for (int64_t j = nv * 16 + tid; j < n; j += nth) {
+    const uint16_t b = x[flat ? j : (j / cols) * ld + j % cols];
+    m = absmax_h2(m, b);
+    q[j] = cast1<FMT>(b, s, ov, un);
+  }
+  block_add_counters(ov, un, st.counters, red);
+  if (!pass) {
+    const uint32_t b = block_max_u32(fold2(m), red);
+    if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// 128 x 128 block scales: one CTA per block, amax of the block, then its cast
+// ---------------------------------------------------------------------------------------
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) cast_block_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                              int64_t cols, int64_t ld, uint8_t* __restrict__ q,
+                                                              uint8_t* __restrict__ qT, float* unit_scale_inv,
+                                                              QuantState st) {
+  __shared__ __align__(128) uint8_t tT[128 * 128];
+  __shared__ uint32_t red[2 * kThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  const int64_t ty = blockIdx.y, tx = blockIdx.x;
+  uint4 v[8];
+  const bool in = load_patch(x, rows, cols, ld, ty, tx, v);
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = absmax_v(m, v[i]);
+  const uint32_t b = block_max_u32(fold2(m), red);
+  float s, d;
+  scales_from_amax(__uint_as_float(b << 16), Fmt<FMT>::kMax, s, d);
+  if (threadIdx.x == 0) {
+    unit_scale_inv[ty * gridDim.x + tx] = d;
+    if (st.amax_cur != nullptr) atomic_max_amax(st.amax_cur, b);
+  }
+  const Scaler sc = make_scaler<FMT>(s, d);
+  uint32_t ov = 0, un = 0, dummy = 0;
+  uint2 c[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) c[i] = cast8<FMT, false>(v[i], sc, ov, un, dummy);
+  if (!in) ov = un = 0;
+  store_patch(c, in, rows, cols, ty, tx, q, qT, tT);
+  if (st.counters != nullptr) block_add_counters(ov, un, st.counters, red);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -519,12 +565,15 @@ __global__ void __launch_bounds__(kThreads) cast_1x128_kernel(const uint16_t* __
   }
 }
 
-__global__ void history_commit_kernel(QuantState st) {
+__global__ void history_commit_kernel(QuantStates sts) {
   pdl_wait();
   pdl_trigger();
-  const int n = *st.hist_count;
-  st.hist[n % st.hist_len] = *st.amax_cur;
-  *st.hist_count = n + 1;
+  if (threadIdx.x < sts.n) {
+    const QuantState& st = sts.s[threadIdx.x];
+    const int n = *st.hist_count;
+    st.hist[n % st.hist_len] = *st.amax_cur;
+    *st.hist_count = n + 1;
+  }
 }
 
 __global__ void selftest_wait_kernel(WaitCtl w) {
@@ -545,38 +594,69 @@ int grid_for(int64_t work_items, int per_block, int sms, int waves) {
   return static_cast<int>(g);
 }
 
+// Grid of a cooperative launch: every CTA must be resident at once. The resident count per
+// SM is queried once per kernel and device.
+template <typename K>
+int coop_grid(K kernel, int64_t work_items) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int nb = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      nb = it->second;
+    } else {
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess || nb < 1) nb = 1;
+      cache[key] = nb;
+    }
+  }
+  int64_t g = static_cast<int64_t>(nb) * num_sms();
+  if (work_items < g) g = work_items;
+  if (g < 1) g = 1;
+  return static_cast<int>(g);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_coop(void (*kernel)(KArgs...), int grid, cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace
 
-cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, float* amax_out,
-                        const int32_t* gate_count, cudaStream_t stream) {
-  const int sms = num_sms();
-  const int g = grid_for(rows * cols, kThreads * 32, sms, 8);
-  return launch_pdl(amax_kernel, dim3(g), dim3(kThreads), 0, stream, static_cast<const uint16_t*>(x), rows, cols, ld,
-                    amax_out, gate_count);
-}
-
-cudaError_t launch_cast_flat(int fmt, bool delayed, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
-                             const QuantState& st, cudaStream_t stream) {
-  const int sms = num_sms();
-  const int g = grid_for(rows * cols, kThreads * 32, sms, 8);
-  auto* xp = static_cast<const uint16_t*>(x);
-  auto* qp = static_cast<uint8_t*>(q);
-  auto k = fmt == 0 ? (delayed ? cast_flat_kernel<0, true> : cast_flat_kernel<0, false>)
-                    : (delayed ? cast_flat_kernel<1, true> : cast_flat_kernel<1, false>);
-  return launch_pdl(k, dim3(g), dim3(kThreads), 0, stream, xp, rows, cols, ld, qp, st);
-}
-
-cudaError_t launch_cast_tiles(int fmt, int scale_kind, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
-                              void* qT, float* unit_scale_inv, const QuantState& st, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>((rows + 127) / 128));
+cudaError_t launch_quant_tensor(int fmt, bool delayed, bool tiled, const void* x, int64_t rows, int64_t cols,
+                                int64_t ld, void* q, void* qT, const QuantState& st, cudaStream_t stream) {
   auto* xp = static_cast<const uint16_t*>(x);
   auto* qp = static_cast<uint8_t*>(q);
   auto* tp = static_cast<uint8_t*>(qT);
-  using K = void (*)(const uint16_t*, int64_t, int64_t, int64_t, uint8_t*, uint8_t*, float*, QuantState);
-  const K table[2][3] = {{cast_tile_kernel<0, kTensorCurrent>, cast_tile_kernel<0, kTensorDelayed>, cast_tile_kernel<0, kBlock>},
-                         {cast_tile_kernel<1, kTensorCurrent>, cast_tile_kernel<1, kTensorDelayed>, cast_tile_kernel<1, kBlock>}};
-  return launch_pdl(table[fmt][scale_kind], grid, dim3(kThreads), 0, stream, xp, rows, cols, ld, qp, tp, unit_scale_inv,
-                    st);
+  const int dl = delayed ? 1 : 0;
+  if (tiled) {
+    auto k = fmt == 0 ? quant_tensor_tiles_kernel<0> : quant_tensor_tiles_kernel<1>;
+    const int64_t ntiles = ((cols + 127) / 128) * ((rows + 127) / 128);
+    return launch_coop(k, coop_grid(k, ntiles), stream, xp, rows, cols, ld, qp, tp, st, dl);
+  }
+  auto k = fmt == 0 ? quant_tensor_flat_kernel<0> : quant_tensor_flat_kernel<1>;
+  return launch_coop(k, coop_grid(k, (rows * cols + 4095) / 4096), stream, xp, rows, cols, ld, qp, st, dl);
+}
+
+cudaError_t launch_cast_blocks(int fmt, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q, void* qT,
+                               float* unit_scale_inv, const QuantState& st, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>((rows + 127) / 128));
+  return launch_pdl(fmt == 0 ? cast_block_kernel<0> : cast_block_kernel<1>, grid, dim3(kThreads), 0, stream,
+                    static_cast<const uint16_t*>(x), rows, cols, ld, static_cast<uint8_t*>(q),
+                    static_cast<uint8_t*>(qT), unit_scale_inv, st);
 }
 
 cudaError_t launch_cast_1x128(int fmt, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
@@ -590,8 +670,8 @@ cudaError_t launch_cast_1x128(int fmt, const void* x, int64_t rows, int64_t cols
                     rows, cols, ld, qp, unit_scale_inv, st);
 }
 
-cudaError_t launch_history_commit(const QuantState& st, cudaStream_t stream) {
-  return launch_pdl(history_commit_kernel, dim3(1), dim3(1), 0, stream, st);
+cudaError_t launch_history_commit(const QuantStates& sts, cudaStream_t stream) {
+  return launch_pdl(history_commit_kernel, dim3(1), dim3(32), 0, stream, sts);
 }
 
 cudaError_t launch_selftest_wait(const WaitCtl& w, cudaStream_t stream) {

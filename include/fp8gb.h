@@ -209,6 +209,11 @@ fp8_status_t fp8_linear_bwd_noalloc(const void* dy_bf16, int64_t M, int64_t K, i
  * hist_count += 1. [GUARD] "Real products...": amax history tracking. */
 fp8_status_t fp8_history_commit(const fp8_tensor_state_t* st, void* stream);
 
+/* The same push for n distinct states (0 <= n <= 32) in one launch: states points to a
+ * host array of n structs (copied by the call), e.g. the x, W and dy states of a layer at
+ * the end of a training step. A state listed twice is rejected. */
+fp8_status_t fp8_history_commit_many(const fp8_tensor_state_t* states, int32_t n, void* stream);
+
 /* Device-side error word. Every wait inside a kernel is bounded; a wait that runs out
  * sets a bit in this word and its kernel returns early (its outputs are then undefined).
  * fp8_poll_device_error synchronises the current device, returns FP8_ERR_TIMEOUT if any

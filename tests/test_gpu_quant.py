@@ -289,3 +289,24 @@ def test_subnormal_amax_keeps_unit_scales(g):
             assert ref["s"] == 1.0 and ref["d"] == 1.0
             assert np.array_equal(host_u8(q), ref["q"])
             check_state_tensor(st, ref, fmt, ref["overflow"], ref["underflow"])
+
+
+def test_commit_many_matches_single_commits(g):
+    """One launch pushing three states equals three single pushes; duplicates are refused."""
+    xs = [normal_bf16(60 + i, (32, 64), std=2.0 ** i) for i in range(3)]
+    a = [g.TensorState(hist_len=4) for _ in range(3)]
+    b = [g.TensorState(hist_len=4) for _ in range(3)]
+    for step in range(6):
+        for i in range(3):
+            for st in (a[i], b[i]):
+                q = empty_u8(32, 64)
+                g.fp8_quantize(dev_bf16(xs[i]), 32, 64, 64, 0, g.FP8_GRAN_TENSOR, g.FP8_SCALE_DELAYED, st, q)
+        g.fp8_history_commit_many(a)
+        for st in b:
+            g.fp8_history_commit(st)
+    for sa, sb in zip(a, b):
+        x, y = sa.snapshot(), sb.snapshot()
+        assert x["count"] == y["count"] == 6 and np.array_equal(x["hist"], y["hist"])
+    with pytest.raises(g.Fp8Error) as e:
+        g.fp8_history_commit_many([a[0], a[1], a[0]])
+    assert e.value.status == g.FP8_ERR_INVALID_ARG
