@@ -11,9 +11,8 @@ delayed scaling (amax history of 16):
                                             wgrad GEMM    dW = x^T dy
   push the x, W and dy amaxes into their histories.
 The step is captured into a CUDA graph; each timed step replays it with CUDA events around
-the launch, after writing a 256 MiB buffer to flush the 129 MB L2 (not timed). A second
-capture of the same step with external event nodes between the stages is replayed in the
-same loop (also after a flush) for the per-kernel times. value = the step's GEMM FLOPs (3 x 2MNK) over the
+the launch, after writing a 256 MiB buffer to flush the 129 MB L2 (not timed). Per-kernel
+times come from the same stages launched eagerly in the same loop, each behind a flush. value = the step's GEMM FLOPs (3 x 2MNK) over the
 measured step time, summed over ranks (each rank its own batch: weak scaling).
 
 --impl reference times the CPU oracle (test infrastructure) on a bounded sample of the
@@ -207,16 +206,11 @@ def run_gpu(args):
         for _, fn, *_ in stages:  # eager pass: sets kernel attributes and caches
             fn()
         torch.cuda.synchronize()
-        # the step is captured twice: `plain` (what a training loop replays; timed with events
-        # around the launch, so the graph launch itself counts) and `probe` (the same kernels
-        # with external event nodes between the stages, for per-kernel times)
-        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(stages) + 1)]
-        probe = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(probe, stream=stream):
-            ev[0].record(stream)
-            for i, (_, fn, *_) in enumerate(stages):
-                fn()
-                ev[i + 1].record(stream)
+        # the step is one CUDA graph, replayed once per timed step with CUDA events around the
+        # launch (the graph launch itself counts). Per-kernel times come from the same stages
+        # launched eagerly in the same loop, each behind an L2 flush: the GPU is still busy
+        # with the flush while the host enqueues the stage, so the events bracket only the
+        # kernel (cold L2, no event nodes inside a graph).
         plain = torch.cuda.CUDAGraph()
         with torch.cuda.graph(plain, stream=stream):
             for _, fn, *_ in stages:
@@ -225,16 +219,20 @@ def run_gpu(args):
             st.reset()  # the delayed-scaling state starts empty (bootstrap step first)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in stages]
 
         def step():
             flush.zero_()  # L2 flush, outside the timed events
             e0.record(stream)
             plain.replay()
             e1.record(stream)
-            flush.zero_()
-            probe.replay()
+            for (a, b), (_, fn, *_) in zip(ev, stages):
+                flush.zero_()
+                a.record(stream)
+                fn()
+                b.record(stream)
             torch.cuda.synchronize()
-            return e0.elapsed_time(e1), [ev[i].elapsed_time(ev[i + 1]) for i in range(len(stages))]
+            return e0.elapsed_time(e1), [a.elapsed_time(b) for a, b in ev]
 
         for _ in range(args.warmup):
             step()
@@ -300,8 +298,8 @@ def run_gpu(args):
                    "l2": "256 MiB buffer written between timed steps (flush)", "parallelism": f"dp{world} (independent batches)"},
         "roofline": roof,
         "kernels": kernels,
-        "kernels_note": "per-stage CUDA-event times from an instrumented replay of the same step in the timed "
-                        "loop (event nodes between stages; their sum %.4f ms vs the plain step)" % probe_step_ms,
+        "kernels_note": "per-stage CUDA-event times of the same stages launched eagerly in the timed loop, each "
+                        "behind an L2 flush (cold L2; sum %.4f ms vs the graph step)" % probe_step_ms,
         "block_scaled_fwd": blk,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -414,6 +412,10 @@ SWEEP_GEMMS = [
     ("loop_fwd", 32768, 6144, 1536, 0, 0, False),
     ("loop_dgrad", 32768, 1536, 6144, 1, 0, False),
     ("loop_wgrad", 1536, 6144, 32768, 0, 1, False),
+    # the same kernels on the other projections of a GPT-2-small block (8192 tokens, d 768)
+    ("gpt2s_qkv_fwd", 8192, 2304, 768, 0, 0, False),
+    ("gpt2s_down_fwd", 8192, 768, 3072, 0, 0, False),
+    ("gpt2s_attn_out_fwd", 8192, 768, 768, 0, 0, False),
 ]
 # name, rows, cols, format, granularity (0 tensor, 1 1x128, 2 128x128), transposed copy
 SWEEP_CASTS = [

@@ -50,6 +50,7 @@ _SIGS = {
     "fp8_quantize": [_P, _I64, _I64, _I64, _I, _I, _I, _SP, _P, _P, _P, _P],
     "fp8_scaled_mm": [_P, _I, _P, _I, _I64, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _P],
     "fp8_requantize_weights": [_P, _I64, _I64, _I, _I, _SP, _P, _P, _P, _P],
+    "fp8_update_requantize_weights": [_P, _P, _I64, _I64, _I, _SP, _P, _P, _P],
     "fp8_linear_fwd": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _I, _I, _P, _P, _P, _P, _P],
     "fp8_linear_bwd": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _SP, _I, _P, _P, _P, _P, _P],
     "fp8_linear_bwd_noalloc": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _SP, _I, _P, _P, _P],
@@ -172,6 +173,11 @@ def fp8_scaled_mm(A, fa, B, fb, M, N, K, lda, ldb, gran, scale_inv_a, scale_inv_
 def fp8_requantize_weights(w_master, K, N, gran, mode, st, wq_kn, wqT_nk, block_scale_inv=None, stream=None):
     return _check(lib.fp8_requantize_weights(_ptr(w_master), K, N, gran, mode, _state(st), _ptr(wq_kn), _ptr(wqT_nk),
                                              _ptr(block_scale_inv), _stream(stream)))
+
+
+def fp8_update_requantize_weights(w_master, delta, K, N, mode, st, wq_kn, wqT_nk, stream=None):
+    return _check(lib.fp8_update_requantize_weights(_ptr(w_master), _ptr(delta), K, N, mode, _state(st), _ptr(wq_kn),
+                                                    _ptr(wqT_nk), _stream(stream)))
 
 
 def fp8_linear_fwd(x, M, K, N, wqT_nk, w_st, w_block_scale_inv, x_st, gran, mode, xq_save, xqT_save,

@@ -229,6 +229,29 @@ fp8_status_t fp8_requantize_weights(const void* w_master_bf16, int64_t K, int64_
                        static_cast<cudaStream_t>(stream));
 }
 
+fp8_status_t fp8_update_requantize_weights(void* w_master_bf16, const float* delta, int64_t K, int64_t N,
+                                           fp8_scaling_t mode, const fp8_tensor_state_t* st, void* wq_kn,
+                                           void* wqT_nk, void* stream) {
+  const char* who = "fp8_update_requantize_weights";
+  if (K < 0 || N < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
+  if (mode != FP8_SCALE_CURRENT && mode != FP8_SCALE_DELAYED)
+    return fail(FP8_ERR_INVALID_ARG, "%s: unknown scaling mode %d", who, (int)mode);
+  fp8_status_t s = check_state(st, mode, who);
+  if (s != FP8_OK) return s;
+  if (K * N == 0) return quantize_impl(w_master_bf16, K, N, N, FP8_E4M3, FP8_GRAN_TENSOR, mode, st, wq_kn, wqT_nk,
+                                       nullptr, static_cast<cudaStream_t>(stream));
+  if (w_master_bf16 == nullptr || delta == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: null W or delta", who);
+  if (wq_kn == nullptr && wqT_nk == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: no output", who);
+  if (!aligned16(w_master_bf16) || !aligned16(delta) || !aligned16(wq_kn) || !aligned16(wqT_nk))
+    return fail(FP8_ERR_ALIGNMENT, "%s: W, delta and the caches must be 16-byte aligned", who);
+  if (K % 8 != 0 || N % 8 != 0 || (wqT_nk != nullptr && K % 16 != 0))
+    return fail(FP8_ERR_UNSUPPORTED, "%s: K and N must be multiples of 8 (K of 16 with wqT)", who);
+  if (K > (1ll << 31) || N > (1ll << 31)) return fail(FP8_ERR_UNSUPPORTED, "%s: dimension beyond 2^31", who);
+  cudaError_t e = launch_update_quant_tensor(mode == FP8_SCALE_DELAYED, w_master_bf16, delta, K, N, wq_kn, wqT_nk,
+                                             to_qs(st), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FP8_OK : cuda_fail(e, who);
+}
+
 fp8_status_t fp8_linear_fwd(const void* x_bf16, int64_t M, int64_t K, int64_t N, const void* wqT_nk,
                             const fp8_tensor_state_t* w_st, const float* w_block_scale_inv,
                             const fp8_tensor_state_t* x_st, fp8_gran_t gran, fp8_scaling_t mode, void* xq_save,

@@ -1,5 +1,6 @@
 // kernels.h -- internal interface between the C ABI (api.cu) and the kernel launchers.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -45,6 +46,11 @@ struct QuantStates {
   int n;
 };
 
+// 2-D tensor map (TMA descriptor) of a row-major matrix: inner = contiguous extent, outer =
+// rows, row_bytes = leading dimension in bytes; swizzle 128 = 128-byte swizzle, 0 = none.
+bool encode_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t inner, uint64_t outer,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, int swizzle);
+
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
 
@@ -56,6 +62,10 @@ WaitCtl wait_ctl();
 // multiples of 8); otherwise row-major q of any shape.
 cudaError_t launch_quant_tensor(int fmt, bool delayed, bool tiled, const void* x, int64_t rows, int64_t cols,
                                 int64_t ld, void* q, void* qT, const QuantState& st, cudaStream_t stream);
+// W <- bf16(fl32(W) + delta) in place, then the per-tensor E4M3 quantise of the updated W into
+// q [rows, cols] and/or qT [cols, rows], in one cooperative launch (W contiguous).
+cudaError_t launch_update_quant_tensor(bool delayed, void* w, const float* delta, int64_t rows, int64_t cols,
+                                       void* q, void* qT, const QuantState& st, cudaStream_t stream);
 // One scale per 128x128 block (full blocks), q and/or qT, inverse scales [rows/128, cols/128].
 cudaError_t launch_cast_blocks(int fmt, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q, void* qT,
                                float* unit_scale_inv, const QuantState& st, cudaStream_t stream);

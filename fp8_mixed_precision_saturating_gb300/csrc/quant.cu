@@ -350,15 +350,47 @@ __device__ __forceinline__ float call_amax(const QuantState& st, int delayed) {
   return effective_amax(st, delayed != 0);
 }
 
-// Tiled layout: rows, cols and ld multiples of 8 (rows of 16 with qT); q and/or qT.
-template <int FMT>
-__global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(const uint16_t* __restrict__ x, int64_t rows,
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Optimizer-step update of this thread's patch: W' = bf16_rne(fl32(W) + delta), one fp32 add
+// per element; W' is stored back into x (in place) and returned in v. delta is row-major
+// [rows, cols] fp32.
+__device__ __forceinline__ void update_patch(uint16_t* __restrict__ x, const float* __restrict__ delta, int64_t cols,
+                                             int64_t ld, int64_t ty, int64_t tx, bool in, uint4 (&v)[8]) {
+  if (!in) return;
+  const int t = threadIdx.x;
+  const int64_t r0 = ty * 128 + (t >> 4) * 8;
+  const int64_t c0 = tx * 128 + (t & 15) * 8;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4* dp = reinterpret_cast<const float4*>(delta + (r0 + i) * cols + c0);
+    const float4 d0 = __ldcs(dp), d1 = __ldcs(dp + 1);
+    uint4& w = v[i];
+    w.x = pack_bf16x2(__fadd_rn(__uint_as_float(w.x << 16), d0.x), __fadd_rn(__uint_as_float(w.x & 0xFFFF0000u), d0.y));
+    w.y = pack_bf16x2(__fadd_rn(__uint_as_float(w.y << 16), d0.z), __fadd_rn(__uint_as_float(w.y & 0xFFFF0000u), d0.w));
+    w.z = pack_bf16x2(__fadd_rn(__uint_as_float(w.z << 16), d1.x), __fadd_rn(__uint_as_float(w.z & 0xFFFF0000u), d1.y));
+    w.w = pack_bf16x2(__fadd_rn(__uint_as_float(w.w << 16), d1.z), __fadd_rn(__uint_as_float(w.w & 0xFFFF0000u), d1.w));
+    *reinterpret_cast<uint4*>(x + (r0 + i) * ld + c0) = w;
+  }
+}
+
+// Tiled layout: rows, cols and ld multiples of 8 (rows of 16 with qT); q and/or qT. With
+// UPD the tensor is first updated in place by delta (the weight-cache refresh fused with
+// the optimizer step): in the amax pass when there is one, else in the cast pass, so W and
+// delta are read once.
+template <int FMT, bool UPD>
+__global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(uint16_t* __restrict__ x, int64_t rows,
                                                                       int64_t cols, int64_t ld, uint8_t* __restrict__ q,
                                                                       uint8_t* __restrict__ qT, QuantState st,
-                                                                      int delayed) {
+                                                                      int delayed, const float* __restrict__ delta) {
   __shared__ __align__(128) uint8_t tT[128 * 128];
   __shared__ uint32_t red[2 * kThreads / 32];
   cg::grid_group grid = cg::this_grid();
+  pdl_trigger();  // the next kernel may start its prologue as this one drains
   const int64_t tiles_x = (cols + 127) / 128;
   const int64_t ntiles = tiles_x * ((rows + 127) / 128);
   const bool pass = needs_amax_pass(st, delayed);
@@ -367,7 +399,8 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(const uint
     uint32_t m = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
       uint4 v[8];
-      load_patch(x, rows, cols, ld, t / tiles_x, t % tiles_x, v);
+      const bool in = load_patch(x, rows, cols, ld, t / tiles_x, t % tiles_x, v);
+      if constexpr (UPD) update_patch(x, delta, cols, ld, t / tiles_x, t % tiles_x, in, v);
 #pragma unroll
       for (int i = 0; i < 8; ++i) m = absmax_v(m, v[i]);
     }
@@ -388,6 +421,9 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(const uint
     const int64_t ty = t / tiles_x, tx = t % tiles_x;
     uint4 v[8];
     const bool in = load_patch(x, rows, cols, ld, ty, tx, v);
+    if constexpr (UPD) {
+      if (!pass) update_patch(x, delta, cols, ld, ty, tx, in, v);
+    }
     uint2 c[8];
     uint32_t o1 = 0, u1 = 0;
 #pragma unroll
@@ -413,6 +449,7 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_flat_kernel(const uint1
                                                                      int delayed) {
   __shared__ uint32_t red[2 * kThreads / 32];
   cg::grid_group grid = cg::this_grid();
+  pdl_trigger();  // the next kernel may start its prologue as this one drains
   const int64_t tid = blockIdx.x * (int64_t)kThreads + threadIdx.x;
   const int64_t nth = (int64_t)gridDim.x * kThreads;
   const int64_t n = rows * cols;
@@ -597,7 +634,7 @@ int grid_for(int64_t work_items, int per_block, int sms, int waves) {
 // Grid of a cooperative launch: every CTA must be resident at once. The resident count per
 // SM is queried once per kernel and device.
 template <typename K>
-int coop_grid(K kernel, int64_t work_items) {
+int coop_grid(K kernel, int64_t work_items, int smem = 0) {
   static std::mutex mu;
   static std::map<std::pair<const void*, int>, int> cache;
   int dev = 0;
@@ -610,7 +647,7 @@ int coop_grid(K kernel, int64_t work_items) {
     if (it != cache.end()) {
       nb = it->second;
     } else {
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess || nb < 1) nb = 1;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, smem) != cudaSuccess || nb < 1) nb = 1;
       cache[key] = nb;
     }
   }
@@ -621,10 +658,11 @@ int coop_grid(K kernel, int64_t work_items) {
 }
 
 template <typename... KArgs, typename... Args>
-cudaError_t launch_coop(void (*kernel)(KArgs...), int grid, cudaStream_t stream, Args&&... args) {
+cudaError_t launch_coop_smem(void (*kernel)(KArgs...), int grid, cudaStream_t stream, int smem, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -632,6 +670,11 @@ cudaError_t launch_coop(void (*kernel)(KArgs...), int grid, cudaStream_t stream,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_coop(void (*kernel)(KArgs...), int grid, cudaStream_t stream, Args&&... args) {
+  return launch_coop_smem(kernel, grid, stream, 0, std::forward<Args>(args)...);
 }
 
 }  // namespace
@@ -643,12 +686,21 @@ cudaError_t launch_quant_tensor(int fmt, bool delayed, bool tiled, const void* x
   auto* tp = static_cast<uint8_t*>(qT);
   const int dl = delayed ? 1 : 0;
   if (tiled) {
-    auto k = fmt == 0 ? quant_tensor_tiles_kernel<0> : quant_tensor_tiles_kernel<1>;
+    auto k = fmt == 0 ? quant_tensor_tiles_kernel<0, false> : quant_tensor_tiles_kernel<1, false>;
     const int64_t ntiles = ((cols + 127) / 128) * ((rows + 127) / 128);
-    return launch_coop(k, coop_grid(k, ntiles), stream, xp, rows, cols, ld, qp, tp, st, dl);
+    return launch_coop(k, coop_grid(k, ntiles), stream, const_cast<uint16_t*>(xp), rows, cols, ld, qp, tp, st, dl,
+                       static_cast<const float*>(nullptr));
   }
   auto k = fmt == 0 ? quant_tensor_flat_kernel<0> : quant_tensor_flat_kernel<1>;
   return launch_coop(k, coop_grid(k, (rows * cols + 4095) / 4096), stream, xp, rows, cols, ld, qp, st, dl);
+}
+
+cudaError_t launch_update_quant_tensor(bool delayed, void* w, const float* delta, int64_t rows, int64_t cols,
+                                       void* q, void* qT, const QuantState& st, cudaStream_t stream) {
+  auto k = quant_tensor_tiles_kernel<0, true>;
+  const int64_t ntiles = ((cols + 127) / 128) * ((rows + 127) / 128);
+  return launch_coop(k, coop_grid(k, ntiles), stream, static_cast<uint16_t*>(w), rows, cols, cols,
+                     static_cast<uint8_t*>(q), static_cast<uint8_t*>(qT), st, delayed ? 1 : 0, delta);
 }
 
 cudaError_t launch_cast_blocks(int fmt, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q, void* qT,

@@ -152,6 +152,21 @@ fp8_status_t fp8_requantize_weights(const void* w_master_bf16, int64_t K, int64_
                                     const fp8_tensor_state_t* st, void* wq_kn, void* wqT_nk,
                                     float* block_scale_inv, void* stream);
 
+/* The optimizer step's update fused with the weight cache refresh.
+ *  [SPEED] "Hardware precision": the bf16 master weights are updated by the optimizer and
+ *  re-quantised to E4M3 after every step. In one launch:
+ *    W <- bf16_rne( fl32(W) + delta )       (in place; one fp32 add per element)
+ *  then the per-tensor E4M3 quantise of the updated W exactly as fp8_requantize_weights
+ *  with gran TENSOR (mode CURRENT: the updated tensor's own amax; DELAYED: the history
+ *  before this call's amax is pushed), writing wq_kn [K,N] and/or wqT_nk [N,K].
+ *  w_master_bf16 [K,N] contiguous, read and written; delta [K,N] fp32 contiguous (the
+ *  optimizer's step, e.g. -lr * m / (sqrt(v) + eps)), finite. K, N multiples of 8 (K of
+ *  16 with wqT_nk); 16-byte aligned pointers. W and delta are read once: in the amax pass
+ *  when the scale needs the updated tensor's amax, else in the cast pass. */
+fp8_status_t fp8_update_requantize_weights(void* w_master_bf16, const float* delta, int64_t K, int64_t N,
+                                           fp8_scaling_t mode, const fp8_tensor_state_t* st, void* wq_kn,
+                                           void* wqT_nk, void* stream);
+
 /* Forward of the FP8 up-projection: y [M,N] = x [M,K] W [K,N].
  *  Quantises x to E4M3 (per tensor into xq_save [M,K] with x_st, or per 1x128 tile into
  *  xq_save with x_tile_scale_inv [M, K/128]) and runs the scaled GEMM against the cached
