@@ -31,6 +31,16 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+#ifdef FP8GB_TRACE  // tuning builds only: per-CTA %globaltimer stamps of the GEMM's phases
+__device__ unsigned long long g_gemm_trace[1024 * 8];
+#define FP8GB_STAMP(k) (g_gemm_trace[blockIdx.x * 8 + (k)] = fp8gb::globaltimer_ns())
+extern "C" int fp8_trace_read(void* host, int n) {
+  return cudaMemcpyFromSymbol(host, g_gemm_trace, sizeof(unsigned long long) * n) == cudaSuccess ? 0 : 1;
+}
+#else
+#define FP8GB_STAMP(k) ((void)0)
+#endif
+
 namespace fp8gb {
 namespace {
 
@@ -39,10 +49,10 @@ constexpr int A_BYTES = BM * BK;
 constexpr int STG_BYTES = 32 * 128;  // one staging buffer: 32 rows x 64 bf16
 constexpr int GROUP_M = 16;          // tile raster: 16 M-blocks share each B tile
 
-// Tile 128 x BN (BN = 256 or 128); the ring depth fills ~192 KB of shared memory.
+// Tile 128 x BN (BN = 256, 192 or 128); the ring depth fills ~192 KB of shared memory.
 template <bool BLOCK, int BN>
 struct Cfg {
-  static_assert(BN == 128 || BN == 256, "tile width");
+  static_assert(BN == 128 || BN == 192 || BN == 256, "tile width");
   static constexpr int B_BYTES = BN * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
@@ -133,6 +143,7 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
   const uint32_t bar_tempty = bar_tfull + 8 * ACC;
   const uint32_t bar_final = bar_tempty + 8 * ACC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+  if (threadIdx.x == 0) FP8GB_STAMP(0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -160,6 +171,7 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
   // the prologue above overlaps the previous kernel; operands and scales are read after it
   pdl_wait();
   pdl_trigger();
+  if (threadIdx.x == 0) FP8GB_STAMP(1);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -177,6 +189,9 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
             break;
           }
           const uint32_t fb = bar_full + 8 * stage;
+#ifdef FP8GB_TRACE
+          if (t == (int)blockIdx.x && kb == 0) FP8GB_STAMP(7);
+#endif
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           tma_load_2d(sa, &tmA, fb, kb * BK, mb * BM);
@@ -220,6 +235,9 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
             break;
           }
           tc_fence_after();
+#ifdef FP8GB_TRACE
+          if (t == (int)blockIdx.x && kb == 0) FP8GB_STAMP(2);
+#endif
           const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           const uint64_t adesc = smem_desc_sw128(sa);
@@ -246,9 +264,11 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
           if (acc == 0) acc_phase ^= 1u;
         }
       }
+      FP8GB_STAMP(3);
       // every MMA this thread issued has completed once this barrier flips
       mma_commit(bar_final);
       if (!mbar_wait_drain(bar_final, 0, 1000000000ull)) atomicOr(p.w.err, DEV_ERR_WAIT_TEARDOWN);
+      FP8GB_STAMP(4);
     }
   } else {
     // ---------------- epilogue ----------------
@@ -261,8 +281,9 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
     bool ok = true;
     if constexpr (!BLOCK) {
       const float dd = __fmul_rn(__ldg(p.sa), __ldg(p.sb));
-      const int hc = ew >> 2;  // which half of the tile's columns this warp drains
-      constexpr int CHUNKS = BN / 128;  // 64-column chunks per warp
+      // the tile's 64-column chunks alternate between the two warps of a lane quarter
+      const int hc = ew >> 2;
+      constexpr int NCH = BN / 64;
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
         int mb, nb;
         tile_coords(t, p, mb, nb);
@@ -270,17 +291,17 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
         __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the spin
         tc_fence_after();
 #pragma unroll 1
-        for (int ch = 0; ch < CHUNKS; ++ch) {
+        for (int ch = hc; ch < NCH; ch += 2) {
           __syncwarp();
           uint32_t r0[32], r1[32];
-          const int col = hc * (BN / 2) + ch * 64;
+          const int col = ch * 64;
           const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col);
           tmem_ld32(taddr, r0);
           tmem_ld32(taddr + 32, r1);
           tmem_ld_wait();
           reg_fence(r0);
           reg_fence(r1);
-          if (ch == CHUNKS - 1) {  // this warp's part of the accumulator is read: hand it back
+          if (ch + 2 >= NCH) {  // this warp's part of the accumulator is read: hand it back
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
@@ -355,10 +376,12 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
       }
     }
     if (lane == 0) bulk_wait_group<0>();
+    if (warp == 2 && lane == 0) FP8GB_STAMP(5);
   }
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) FP8GB_STAMP(6);
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -407,15 +430,25 @@ cudaError_t prepare_kernel() {
   return e;
 }
 
-// Tile width: cost = rounds of tiles over the SMs x time of one tile. A 128-wide tile needs
-// 1.33x the operand bytes per FLOP of a 256-wide one and its mainloop runs at ~60 % of the
-// tensor peak against ~94 % (measured on GB300), so its per-round time is ~213/272 of the
-// wide tile's; it wins only when it saves rounds (few, long tiles).
+// Tile width: cost = rounds of tiles over the SMs x time of one tile (width / mainloop
+// efficiency). Narrower tiles move more operand bytes per FLOP: measured on GB300 the
+// mainloop runs at ~94 % of the tensor peak with 256-wide tiles, ~80 % with 192-wide and
+// ~60 % with 128-wide ones. Narrower tiles win only when they save rounds.
 int choose_bn(int64_t M, int64_t N, int sms) {
   const int64_t tm = (M + BM - 1) / BM;
-  const int64_t r256 = (tm * ((N + 255) / 256) + sms - 1) / sms;
-  const int64_t r128 = (tm * ((N + 127) / 128) + sms - 1) / sms;
-  return r128 * 213 < r256 * 272 ? 128 : 256;
+  const int widths[3] = {256, 192, 128};
+  const int per_round[3] = {272, 240, 213};  // width / efficiency
+  int best = 256;
+  int64_t best_cost = -1;
+  for (int i = 0; i < 3; ++i) {
+    const int64_t rounds = (tm * ((N + widths[i] - 1) / widths[i]) + sms - 1) / sms;
+    const int64_t cost = rounds * per_round[i];
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = widths[i];
+    }
+  }
+  return best;
 }
 
 template <bool BLOCK, int BN>
@@ -478,7 +511,9 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why
     return cudaErrorInvalidDevice;
   }
   if (g.block_scaled) return launch_variant<true, 128>(ta, tb, tc, p, stream);
-  return bn == 256 ? launch_variant<false, 256>(ta, tb, tc, p, stream) : launch_variant<false, 128>(ta, tb, tc, p, stream);
+  if (bn == 256) return launch_variant<false, 256>(ta, tb, tc, p, stream);
+  if (bn == 192) return launch_variant<false, 192>(ta, tb, tc, p, stream);
+  return launch_variant<false, 128>(ta, tb, tc, p, stream);
 }
 
 }  // namespace fp8gb

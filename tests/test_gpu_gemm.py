@@ -67,6 +67,7 @@ CASES = [
     (16, 8, 32, 1, 1),
     (640, 768, 384, 1, 0),
     (4096, 4096, 256, 0, 0),   # 512 tiles: several per CTA
+    (8192, 560, 256, 1, 0),    # 192-wide tiles, ragged last tile
 ]
 
 
