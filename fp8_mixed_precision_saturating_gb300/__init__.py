@@ -49,6 +49,7 @@ _SP = ctypes.POINTER(fp8_tensor_state_t)
 _SIGS = {
     "fp8_quantize": [_P, _I64, _I64, _I64, _I, _I, _I, _SP, _P, _P, _P, _P],
     "fp8_scaled_mm": [_P, _I, _P, _I, _I64, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _P],
+    "fp8_scaled_mm_quant": [_P, _I, _P, _I, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _I64, _I, _SP, _P, _P],
     "fp8_requantize_weights": [_P, _I64, _I64, _I, _I, _SP, _P, _P, _P, _P],
     "fp8_update_requantize_weights": [_P, _P, _I64, _I64, _I, _SP, _P, _P, _P],
     "fp8_linear_fwd": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _I, _I, _P, _P, _P, _P, _P],
@@ -168,6 +169,12 @@ def fp8_quantize(x, rows, cols, ld, fmt, gran, mode, st, q_out, qT_out=None, uni
 def fp8_scaled_mm(A, fa, B, fb, M, N, K, lda, ldb, gran, scale_inv_a, scale_inv_b, C, ldc, stream=None):
     return _check(lib.fp8_scaled_mm(_ptr(A), fa, _ptr(B), fb, M, N, K, lda, ldb, gran, _ptr(scale_inv_a),
                                     _ptr(scale_inv_b), _ptr(C), ldc, _stream(stream)))
+
+
+def fp8_scaled_mm_quant(A, fa, B, fb, M, N, K, lda, ldb, scale_inv_a, scale_inv_b, C, ldc, fc, c_st, Cq,
+                        stream=None):
+    return _check(lib.fp8_scaled_mm_quant(_ptr(A), fa, _ptr(B), fb, M, N, K, lda, ldb, _ptr(scale_inv_a),
+                                          _ptr(scale_inv_b), _ptr(C), ldc, fc, _state(c_st), _ptr(Cq), _stream(stream)))
 
 
 def fp8_requantize_weights(w_master, K, N, gran, mode, st, wq_kn, wqT_nk, block_scale_inv=None, stream=None):

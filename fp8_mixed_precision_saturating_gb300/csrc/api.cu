@@ -218,6 +218,46 @@ fp8_status_t fp8_scaled_mm(const void* A, fp8_format_t fa, const void* B, fp8_fo
                         static_cast<cudaStream_t>(stream));
 }
 
+fp8_status_t fp8_scaled_mm_quant(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb, int64_t M,
+                                 int64_t N, int64_t K, int64_t lda, int64_t ldb, const float* scale_inv_a,
+                                 const float* scale_inv_b, void* C_bf16, int64_t ldc, fp8_format_t fc,
+                                 const fp8_tensor_state_t* c_st, void* Cq, void* stream) {
+  const char* who = "fp8_scaled_mm_quant";
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (fc != FP8_E4M3 && fc != FP8_E5M2) return fail(FP8_ERR_INVALID_ARG, "%s: unknown output format", who);
+  fp8_status_t st = check_state(c_st, FP8_SCALE_DELAYED, who);
+  if (st != FP8_OK) return st;
+  if (M < 0 || N < 0 || K < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
+  if (M == 0 || N == 0) return FP8_OK;
+  if (C_bf16 == nullptr || Cq == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: C_bf16 and Cq are required", who);
+  if (!aligned16(Cq) || N % 16 != 0) return fail(FP8_ERR_ALIGNMENT, "%s: Cq 16-byte aligned, N %% 16 == 0", who);
+  if (K == 0) return fail(FP8_ERR_UNSUPPORTED, "%s: K must be positive", who);
+  // the same checks as fp8_scaled_mm (per-tensor scales)
+  if ((fa != FP8_E4M3 && fa != FP8_E5M2) || (fb != FP8_E4M3 && fb != FP8_E5M2))
+    return fail(FP8_ERR_INVALID_ARG, "%s: unknown format", who);
+  if (ldc < N) return fail(FP8_ERR_INVALID_ARG, "%s: ldc < N", who);
+  if (!aligned16(C_bf16) || ldc % 8 != 0) return fail(FP8_ERR_ALIGNMENT, "%s: C 16-byte aligned, ldc %% 8 == 0", who);
+  if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31)) return fail(FP8_ERR_UNSUPPORTED, "%s: size >= 2^31", who);
+  if (A == nullptr || B == nullptr || scale_inv_a == nullptr || scale_inv_b == nullptr)
+    return fail(FP8_ERR_INVALID_ARG, "%s: null A, B or scale", who);
+  if (lda < K || ldb < K) return fail(FP8_ERR_INVALID_ARG, "%s: lda or ldb < K", who);
+  if (!aligned16(A) || !aligned16(B) || lda % 16 != 0 || ldb % 16 != 0)
+    return fail(FP8_ERR_ALIGNMENT, "%s: A and B must be 16-byte aligned with lda, ldb multiples of 16", who);
+  cudaError_t e = cudaMemsetAsync(c_st->amax_cur, 0, sizeof(float), s);
+  if (e != cudaSuccess) return cuda_fail(e, who);
+  GemmArgs g{A, B, C_bf16, M, N, K, lda, ldb, ldc, (int)fa, (int)fb, scale_inv_a, scale_inv_b, false};
+  g.qf = (int)fc;
+  g.Cq = Cq;
+  g.ldcq = N;
+  g.cst = to_qs(c_st);
+  const char* why = "launch";
+  e = launch_gemm(g, s, &why);
+  if (e != cudaSuccess) return cuda_fail(e, why);
+  e = launch_quant_tensor_if_empty_history((int)fc, C_bf16, M, N, ldc, Cq, g.cst, s);
+  if (e != cudaSuccess) return cuda_fail(e, "bootstrap cast of the FP8 output");
+  return FP8_OK;
+}
+
 fp8_status_t fp8_requantize_weights(const void* w_master_bf16, int64_t K, int64_t N, fp8_gran_t gran,
                                     fp8_scaling_t mode, const fp8_tensor_state_t* st, void* wq_kn, void* wqT_nk,
                                     float* block_scale_inv, void* stream) {

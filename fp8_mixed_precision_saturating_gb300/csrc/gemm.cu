@@ -28,6 +28,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "cast.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -47,15 +48,21 @@ namespace {
 constexpr int BM = 128, BK = 128;
 constexpr int A_BYTES = BM * BK;
 constexpr int STG_BYTES = 32 * 128;  // one staging buffer: 32 rows x 64 bf16
+constexpr int QSTG_BYTES = 32 * 64;  // one staging buffer of FP8 output: 32 rows x 64 codes
 constexpr int GROUP_M = 16;          // tile raster: 16 M-blocks share each B tile
 
-// Tile 128 x BN (BN = 256, 192 or 128); the ring depth fills ~192 KB of shared memory.
-template <bool BLOCK, int BN>
+// Tile 128 x BN (BN = 256, 192 or 128); the ring depth fills ~192 KB of shared memory, less
+// when the epilogue also stages FP8 output (QF >= 0: 0 = E4M3, 1 = E5M2).
+template <bool BLOCK, int BN, int QF>
 struct Cfg {
   static_assert(BN == 128 || BN == 192 || BN == 256, "tile width");
+  static_assert(QF < 0 || !BLOCK, "FP8 output with per-tensor scales only");
   static constexpr int B_BYTES = BN * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
+  static constexpr int EPI_WARPS_ = BLOCK ? 4 * (BN / 64) : 8;
+  static constexpr int QSTG_PER_WARP = QF >= 0 ? QSTG_BYTES : 0;
+  static constexpr int STAGES_FIT = (230000 - EPI_WARPS_ * (STG_BYTES + QSTG_PER_WARP)) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT < (192 * 1024) / STAGE_BYTES ? STAGES_FIT : (192 * 1024) / STAGE_BYTES;
   static constexpr int ACC = 512 / BN;                   // accumulator buffers in TMEM
   static constexpr uint32_t TMEM_COLS = 512;
   // per tensor: two warps per TMEM lane quarter, each draining half of the tile's columns;
@@ -64,7 +71,8 @@ struct Cfg {
   static constexpr int STG_PER_WARP = 1;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int OFF_STG = STAGES * STAGE_BYTES;
-  static constexpr int OFF_BAR = OFF_STG + EPI_WARPS * STG_PER_WARP * STG_BYTES;
+  static constexpr int OFF_QSTG = OFF_STG + EPI_WARPS * STG_PER_WARP * STG_BYTES;
+  static constexpr int OFF_BAR = OFF_QSTG + EPI_WARPS * QSTG_PER_WARP;
   // full[S], empty[S], tfull[ACC], tempty[ACC], final
   static constexpr int NBAR = 2 * STAGES + 2 * ACC + 1;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + 8 * NBAR;
@@ -80,6 +88,7 @@ struct KParams {
   const float* sb;
   int sa_ld, sb_ld;
   WaitCtl w;
+  QuantState cst;  // scaling state of the FP8 output (QF >= 0)
 };
 
 __device__ __forceinline__ void tile_coords(int t, const KParams& p, int& mb, int& nb) {
@@ -124,11 +133,12 @@ __device__ __forceinline__ void stage_and_store(uint8_t* stg, const uint32_t (&p
   }
 }
 
-template <bool BLOCK, int BN>
-__global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
+template <bool BLOCK, int BN, int QF>
+__global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
     gemm_f8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const KParams p) {
-  using C = Cfg<BLOCK, BN>;
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmQ,
+                   const KParams p) {
+  using C = Cfg<BLOCK, BN, QF>;
   constexpr int STAGES = C::STAGES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
   constexpr uint32_t TMEM_COLS = C::TMEM_COLS;
@@ -281,6 +291,24 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
     bool ok = true;
     if constexpr (!BLOCK) {
       const float dd = __fmul_rn(__ldg(p.sa), __ldg(p.sb));
+      // FP8 output: with a non-empty history the epilogue casts the bf16 result with the
+      // delayed scale (the empty-history call is cast afterwards from its own amax)
+      bool fused = false;
+      castops::Scaler qsc{};
+      uint32_t qov = 0, qun = 0, qam = 0;
+      uint8_t* qstg = smem + C::OFF_QSTG + ew * C::QSTG_PER_WARP;
+      if constexpr (QF >= 0) {
+        fused = *p.cst.hist_count > 0;
+        if (fused) {
+          float s, d;
+          castops::scales_from_amax(castops::effective_amax(p.cst, true), castops::Fmt<QF>::kMax, s, d);
+          qsc = castops::make_scaler<QF>(s, d);
+          if (blockIdx.x == 0 && ew == 0 && lane == 0) {
+            *p.cst.scale = s;
+            *p.cst.scale_inv = d;
+          }
+        }
+      }
       // the tile's 64-column chunks alternate between the two warps of a lane quarter
       const int hc = ew >> 2;
       constexpr int NCH = BN / 64;
@@ -313,12 +341,48 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN>::THREADS, 1)
             pk[16 + j] =
                 pack_bf16x2(__fmul_rn(__uint_as_float(r1[2 * j]), dd), __fmul_rn(__uint_as_float(r1[2 * j + 1]), dd));
           }
-          if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the staging buffer
+          if (lane == 0) bulk_wait_group_read<0>();  // the previous stores have read the staging buffers
           __syncwarp();
-          stage_and_store(stg, pk, lane, &tmC, nb * BN + col, mb * BM + q * 32);
+          if constexpr (QF >= 0) {
+            if (fused) {
+              // 64 codes of this lane's row, staged with the 64-byte swizzle: 16-byte chunk j
+              // of row r sits at chunk j ^ ((r / 2) % 4)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint2 c0 = castops::cast8<QF, true>(make_uint4(pk[8 * j], pk[8 * j + 1], pk[8 * j + 2], pk[8 * j + 3]),
+                                                          qsc, qov, qun, qam);
+                const uint2 c1 = castops::cast8<QF, true>(
+                    make_uint4(pk[8 * j + 4], pk[8 * j + 5], pk[8 * j + 6], pk[8 * j + 7]), qsc, qov, qun, qam);
+                *reinterpret_cast<uint4*>(qstg + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) =
+                    make_uint4(c0.x, c0.y, c1.x, c1.y);
+              }
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) * 16)) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, smem_u32(stg), nb * BN + col, mb * BM + q * 32);
+            if (fused) tma_store_2d(&tmQ, smem_u32(qstg), nb * BN + col, mb * BM + q * 32);
+            bulk_commit_group();
+          }
         }
         acc = (acc + 1 == ACC) ? 0 : acc + 1;
         if (acc == 0) acc_phase ^= 1u;
+      }
+      if (fused) {  // this warp's share of the output's counters and amax
+        qov = __reduce_add_sync(0xFFFFFFFFu, qov);
+        qun = __reduce_add_sync(0xFFFFFFFFu, qun);
+        qam = __reduce_max_sync(0xFFFFFFFFu, castops::fold2(qam));
+        if (lane == 0) {
+          if (qov) atomicAdd(p.cst.counters + 0, static_cast<unsigned long long>(qov));
+          if (qun) atomicAdd(p.cst.counters + 1, static_cast<unsigned long long>(qun));
+          castops::atomic_max_amax(p.cst.amax_cur, qam);
+        }
       }
     } else {
       // each warp folds 64 columns (one 128-column scale block = BN / 128 ... of them) of its
@@ -414,7 +478,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t
   return encode_tmap_2d(m, base, dt, inner, outer, row_bytes, box_inner, box_outer, 128);
 }
 
-template <bool BLOCK, int BN>
+template <bool BLOCK, int BN, int QF>
 cudaError_t prepare_kernel() {
   // the attribute is per device; remember which devices were configured
   static bool done[64] = {};
@@ -424,8 +488,8 @@ cudaError_t prepare_kernel() {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(mu);
   if (dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(gemm_f8_kernel<BLOCK, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<BLOCK, BN>::SMEM);
+  e = cudaFuncSetAttribute(gemm_f8_kernel<BLOCK, BN, QF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<BLOCK, BN, QF>::SMEM);
   if (e == cudaSuccess && dev < 64) done[dev] = true;
   return e;
 }
@@ -451,17 +515,25 @@ int choose_bn(int64_t M, int64_t N, int sms) {
   return best;
 }
 
-template <bool BLOCK, int BN>
-cudaError_t launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, KParams p,
-                           cudaStream_t stream) {
-  cudaError_t e = prepare_kernel<BLOCK, BN>();
+template <bool BLOCK, int BN, int QF>
+cudaError_t launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tq,
+                           KParams p, cudaStream_t stream) {
+  cudaError_t e = prepare_kernel<BLOCK, BN, QF>();
   if (e != cudaSuccess) return e;
   p.num_n = (p.N + BN - 1) / BN;
   p.num_tiles = p.num_m * p.num_n;
   p.idesc = idesc_f8(p.idesc & 7u, (p.idesc >> 3) & 7u, BM, BN);
   const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  return launch_pdl(gemm_f8_kernel<BLOCK, BN>, dim3(grid), dim3(Cfg<BLOCK, BN>::THREADS), Cfg<BLOCK, BN>::SMEM, stream,
-                    ta, tb, tc, p);
+  return launch_pdl(gemm_f8_kernel<BLOCK, BN, QF>, dim3(grid), dim3(Cfg<BLOCK, BN, QF>::THREADS),
+                    Cfg<BLOCK, BN, QF>::SMEM, stream, ta, tb, tc, tq, p);
+}
+
+template <int QF>
+cudaError_t launch_width(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                         const CUtensorMap& tq, const KParams& p, cudaStream_t stream) {
+  if (bn == 256) return launch_variant<false, 256, QF>(ta, tb, tc, tq, p, stream);
+  if (bn == 192) return launch_variant<false, 192, QF>(ta, tb, tc, tq, p, stream);
+  return launch_variant<false, 128, QF>(ta, tb, tc, tq, p, stream);
 }
 
 }  // namespace
@@ -474,7 +546,9 @@ bool encode_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, ui
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapSwizzle sw = swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  const CUtensorMapSwizzle sw = swizzle == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                : CU_TENSOR_MAP_SWIZZLE_NONE;
   return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -494,7 +568,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why
     *why = "cuTensorMapEncodeTiled failed (driver entry point missing or tensor map rejected)";
     return cudaErrorInvalidValue;
   }
-  KParams p;
+  KParams p{};
   p.M = static_cast<int>(g.M);
   p.N = static_cast<int>(g.N);
   p.K = static_cast<int>(g.K);
@@ -510,10 +584,18 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why
     *why = "device error word unavailable";
     return cudaErrorInvalidDevice;
   }
-  if (g.block_scaled) return launch_variant<true, 128>(ta, tb, tc, p, stream);
-  if (bn == 256) return launch_variant<false, 256>(ta, tb, tc, p, stream);
-  if (bn == 192) return launch_variant<false, 192>(ta, tb, tc, p, stream);
-  return launch_variant<false, 128>(ta, tb, tc, p, stream);
+  CUtensorMap tq = tc;  // unused unless the epilogue also writes FP8 codes
+  if (g.qf >= 0) {
+    if (!encode_tmap_2d(&tq, g.Cq, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.N, g.M, g.ldcq, 64, 32, 64)) {
+      *why = "cuTensorMapEncodeTiled failed for the FP8 output";
+      return cudaErrorInvalidValue;
+    }
+    p.cst = g.cst;
+  }
+  if (g.block_scaled) return launch_variant<true, 128, -1>(ta, tb, tc, tq, p, stream);
+  if (g.qf == 0) return launch_width<0>(bn, ta, tb, tc, tq, p, stream);
+  if (g.qf == 1) return launch_width<1>(bn, ta, tb, tc, tq, p, stream);
+  return launch_width<-1>(bn, ta, tb, tc, tq, p, stream);
 }
 
 }  // namespace fp8gb

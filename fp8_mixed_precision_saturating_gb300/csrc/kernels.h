@@ -62,6 +62,10 @@ WaitCtl wait_ctl();
 // multiples of 8); otherwise row-major q of any shape.
 cudaError_t launch_quant_tensor(int fmt, bool delayed, bool tiled, const void* x, int64_t rows, int64_t cols,
                                 int64_t ld, void* q, void* qT, const QuantState& st, cudaStream_t stream);
+// Current-scaling quantise of a row-major tensor into contiguous codes, run only while
+// st's history is empty (decided on the device); a no-op launch otherwise.
+cudaError_t launch_quant_tensor_if_empty_history(int fmt, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                                 void* q, const QuantState& st, cudaStream_t stream);
 // W <- bf16(fl32(W) + delta) in place, then the per-tensor E4M3 quantise of the updated W into
 // q [rows, cols] and/or qT [cols, rows], in one cooperative launch (W contiguous).
 cudaError_t launch_update_quant_tensor(bool delayed, void* w, const float* delta, int64_t rows, int64_t cols,
@@ -86,6 +90,11 @@ struct GemmArgs {
   const float* sa;
   const float* sb;
   bool block_scaled;
+  // optional FP8 output of the same epilogue: qf = -1 none, 0 E4M3, 1 E5M2
+  int qf = -1;
+  void* Cq = nullptr;
+  int64_t ldcq = 0;
+  QuantState cst{};
 };
 // Returns cudaSuccess, or an error; `why` receives a static message for host-side failures.
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why);

@@ -140,6 +140,23 @@ fp8_status_t fp8_scaled_mm(const void* A, fp8_format_t fa, const void* B, fp8_fo
                            fp8_gran_t gran, const float* scale_inv_a, const float* scale_inv_b,
                            void* C_bf16, int64_t ldc, void* stream);
 
+/* fp8_scaled_mm (per-tensor scales) whose epilogue also emits the FP8 codes of its output for
+ * a following FP8 consumer (for example dgrad's dx, cast to E5M2 for the previous layer's
+ * backward), so the bf16 result is not read back by a separate cast.
+ *  [GUARD] "Real products...": delayed scaling with amax history. The codes use the output's
+ *  delayed scale: Cq = cast_fc( fl32( bf16(C) * s_c ) ), s_c from c_st's history (required,
+ *  delayed mode); the call records c_st->amax_cur = max |bf16(C)|, scale, scale_inv and adds
+ *  to the counters, exactly as fp8_quantize of the bf16 output with FP8_SCALE_DELAYED would.
+ *  While the history is empty (the bootstrap call) the scale needs the output's own amax, so
+ *  the epilogue writes only C_bf16 and a second kernel, launched every call and returning at
+ *  once when the history is non-empty, casts it from its current amax.
+ *  C_bf16 [M,N] (leading dimension ldc) is required; Cq [M,N] contiguous codes, N % 16 == 0;
+ *  K > 0. Other rules as fp8_scaled_mm. */
+fp8_status_t fp8_scaled_mm_quant(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb, int64_t M,
+                                 int64_t N, int64_t K, int64_t lda, int64_t ldb, const float* scale_inv_a,
+                                 const float* scale_inv_b, void* C_bf16, int64_t ldc, fp8_format_t fc,
+                                 const fp8_tensor_state_t* c_st, void* Cq, void* stream);
+
 /* Refresh the FP8 weight cache from the bf16 master weight W [K,N] (contiguous).
  *  [SPEED] "Hardware precision": after each optimizer step the bf16 master weights are
  *  re-quantised to E4M3 and cached for the next forward. One pass over W writes
