@@ -8,18 +8,23 @@
 //   C[m, n] = bf16( d_a * d_b * sum_k A[m, k] B[n, k] )                    (per tensor)
 //   C[m, n] = bf16( sum_kb d_a[m, kb] d_b[kb, n/128] sum_{k in kb} A B )  (block scaled)
 //
-// Design (one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0      one thread issues TMA loads of A [128 x 128] and B [256 x 128] (K-major,
-//               128-byte swizzle) into a 4-stage shared-memory ring;
-//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma (M=128, N=256,
+// Design (one CTA per SM, persistent over output tiles):
+//   warp 0      one thread issues TMA loads of A [128 x 128] and B [BN x 128] (K-major,
+//               128-byte swizzle) into a shared-memory ring;
+//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma (M=128, N=BN,
 //               K=32) into a TMEM accumulator and frees ring slots with tcgen05.commit;
 //   warps 2..   epilogue: tcgen05.ld of the accumulator (each warp owns the 32 TMEM lanes
 //               its warp index selects), multiply by the scales, convert to bf16, stage
 //               128-byte rows through swizzled shared memory and write them with TMA.
 // Per tensor: two 256-column accumulators, so the epilogue of one tile overlaps the
-// mainloop of the next. Block scaled: every 128-deep K block gets a fresh accumulator
-// buffer (two, alternating), and 8 epilogue warps fold each block into fp32 registers
-// with its scale product before the next block lands.
+// mainloop of the next; each epilogue warp reads all of its columns before handing the
+// accumulator back. A CTA takes in operands at ~140 GB/s on GB300, which caps a
+// 128 x 256 tile at ~80 % of the tensor peak; with more than 128 rows the per-tensor GEMM
+// therefore runs on CTA pairs (clusters of two, tcgen05 cta_group::2): the pair computes a
+// 256 x BN tile, each CTA loads its own 128 rows of A and half of B's BN rows, the even
+// CTA issues the MMAs, and both CTAs drain their half of the accumulator.
+// Block scaled: every 128-deep K block gets a fresh accumulator buffer (four, rotating),
+// and 8 epilogue warps fold each block into fp32 registers with its scale product.
 // Every mbarrier wait is bounded (see ptx.cuh); on a timeout the CTA stops issuing work,
 // drains what it issued and frees its TMEM.
 #include <cuda.h>
@@ -51,23 +56,27 @@ constexpr int STG_BYTES = 32 * 128;  // one staging buffer: 32 rows x 64 bf16
 constexpr int QSTG_BYTES = 32 * 64;  // one staging buffer of FP8 output: 32 rows x 64 codes
 constexpr int GROUP_M = 16;          // tile raster: 16 M-blocks share each B tile
 
-// Tile 128 x BN (BN = 256, 192 or 128); the ring depth fills ~192 KB of shared memory, less
-// when the epilogue also stages FP8 output (QF >= 0: 0 = E4M3, 1 = E5M2).
-template <bool BLOCK, int BN, int QF>
+// Tile 128 x BN per CTA (BN = 256, 192 or 128); the ring depth fills ~192 KB of shared
+// memory, less when the epilogue also stages FP8 output (QF >= 0: 0 = E4M3, 1 = E5M2).
+// PAIR: two CTAs of a cluster share one 256 x BN tile through the CTA-pair MMA; each holds
+// its 128 rows of A and half of B's BN rows, so a CTA loads 16 KB + BN * 64 bytes per
+// 128-deep K block instead of 16 KB + BN * 128 for the same tensor work.
+template <bool BLOCK, int BN, int QF, bool PAIR = false>
 struct Cfg {
   static_assert(BN == 128 || BN == 192 || BN == 256, "tile width");
   static_assert(QF < 0 || !BLOCK, "FP8 output with per-tensor scales only");
-  static constexpr int B_BYTES = BN * BK;
+  static_assert(!(PAIR && BLOCK), "CTA pairs with per-tensor scales only");
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;   // B rows this CTA loads per stage
+  static constexpr int B_BYTES = B_ROWS * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int EPI_WARPS_ = BLOCK ? 4 * (BN / 64) : 8;
-  static constexpr int QSTG_PER_WARP = QF >= 0 ? QSTG_BYTES : 0;
-  static constexpr int STAGES_FIT = (230000 - EPI_WARPS_ * (STG_BYTES + QSTG_PER_WARP)) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT < (192 * 1024) / STAGE_BYTES ? STAGES_FIT : (192 * 1024) / STAGE_BYTES;
-  static constexpr int ACC = 512 / BN;                   // accumulator buffers in TMEM
-  static constexpr uint32_t TMEM_COLS = 512;
   // per tensor: two warps per TMEM lane quarter, each draining half of the tile's columns;
   // block scaled: one warp per lane quarter and 64 columns
   static constexpr int EPI_WARPS = BLOCK ? 4 * (BN / 64) : 8;
+  static constexpr int QSTG_PER_WARP = QF >= 0 ? QSTG_BYTES : 0;
+  static constexpr int STAGES_FIT = (230000 - EPI_WARPS * (STG_BYTES + QSTG_PER_WARP)) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT < (192 * 1024) / STAGE_BYTES ? STAGES_FIT : (192 * 1024) / STAGE_BYTES;
+  static constexpr int ACC = 512 / BN;                   // accumulator buffers in TMEM
+  static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int STG_PER_WARP = 1;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int OFF_STG = STAGES * STAGE_BYTES;
@@ -77,7 +86,10 @@ struct Cfg {
   static constexpr int NBAR = 2 * STAGES + 2 * ACC + 1;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + 8 * NBAR;
   static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;  // + alignment slack
+  // arrivals that free an accumulator: every epilogue warp of the tile's CTAs
+  static constexpr int TEMPTY_COUNT = (PAIR ? 2 : 1) * EPI_WARPS;
   static_assert(SMEM <= 232448, "shared memory");
+  static_assert((A_BYTES % 1024) == 0 && (B_BYTES % 1024) == 0, "stage halves on 1024-byte swizzle atoms");
 };
 
 struct KParams {
@@ -133,12 +145,12 @@ __device__ __forceinline__ void stage_and_store(uint8_t* stg, const uint32_t (&p
   }
 }
 
-template <bool BLOCK, int BN, int QF>
-__global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
+template <bool BLOCK, int BN, int QF, bool PAIR>
+__global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
     gemm_f8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmQ,
                    const KParams p) {
-  using C = Cfg<BLOCK, BN, QF>;
+  using C = Cfg<BLOCK, BN, QF, PAIR>;
   constexpr int STAGES = C::STAGES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
   constexpr uint32_t TMEM_COLS = C::TMEM_COLS;
@@ -154,6 +166,12 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
   const uint32_t bar_final = bar_tempty + 8 * ACC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
   if (threadIdx.x == 0) FP8GB_STAMP(0);
+  // CTA pairs: rank 0 issues the MMAs and owns the stage-full and accumulator-empty
+  // barriers both CTAs signal; tiles are 256 rows (rank r holds rows 128 r .. 128 r + 127)
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int tile0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tile_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  constexpr int TILE_M = PAIR ? 2 * BM : BM;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -162,7 +180,7 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
     }
     for (int a = 0; a < ACC; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
-      mbar_init(bar_tempty + 8 * a, C::EPI_WARPS);
+      mbar_init(bar_tempty + 8 * a, C::TEMPTY_COUNT);
     }
     mbar_init(bar_final, 1);
     fence_mbar_init();
@@ -171,11 +189,17 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
     tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // the peer's barriers are initialised
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // the prologue above overlaps the previous kernel; operands and scales are read after it
@@ -190,9 +214,12 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_phase = 0;  // per stage: issued?, parity of last issue
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      const uint32_t full_lead = PAIR ? mapa_shared(bar_full, 0) : bar_full;
+      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
         int mb, nb;
         tile_coords(t, p, mb, nb);
+        const int arow = mb * TILE_M + static_cast<int>(rank) * BM;
+        const int brow = nb * BN + static_cast<int>(rank) * C::B_ROWS;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.w, DEV_ERR_WAIT_PRODUCER)) {
             ok = false;
@@ -202,10 +229,17 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
 #ifdef FP8GB_TRACE
           if (t == (int)blockIdx.x && kb == 0) FP8GB_STAMP(7);
 #endif
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
           const uint32_t sa = sbase + stage * STAGE_BYTES;
-          tma_load_2d(sa, &tmA, fb, kb * BK, mb * BM);
-          tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, nb * BN);
+          if constexpr (PAIR) {
+            // both CTAs' bytes land on rank 0's barrier, which alone expects them
+            if (rank == 0) mbar_arrive_expect_tx(fb, 2 * STAGE_BYTES);
+            tma_load_2d_pair(sa, &tmA, full_lead + 8 * stage, kb * BK, arow);
+            tma_load_2d_pair(sa + A_BYTES, &tmB, full_lead + 8 * stage, kb * BK, brow);
+          } else {
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            tma_load_2d(sa, &tmA, fb, kb * BK, arow);
+            tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, brow);
+          }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -215,19 +249,27 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
         }
       }
       if (!ok) {  // let every load already issued land before the CTA exits
-        for (int s = 0; s < STAGES; ++s)
-          if (issued_mask & (1u << s)) mbar_wait_drain(bar_full + 8 * s, (issued_phase >> s) & 1u, 1000000000ull);
+        if constexpr (PAIR) {
+          // the loads signal rank 0's barriers, which may also wait for the peer's bytes:
+          // give them a fixed 200 us (a TMA load lands in microseconds)
+          const unsigned long long t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 200000ull) {
+          }
+        } else {
+          for (int s = 0; s < STAGES; ++s)
+            if (issued_mask & (1u << s)) mbar_wait_drain(bar_full + 8 * s, (issued_phase >> s) & 1u, 1000000000ull);
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer ----------------
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
         if (!BLOCK) {
           if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.w, DEV_ERR_WAIT_MMA)) break;
           tc_fence_after();
@@ -255,9 +297,15 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k) {
             const uint32_t accumulate = BLOCK ? (k != 0) : ((kb | k) != 0);
-            mma_f8(d, adesc + 2 * k, bdesc + 2 * k, p.idesc, accumulate);
+            if constexpr (PAIR)
+              mma_f8_pair(d, adesc + 2 * k, bdesc + 2 * k, p.idesc, accumulate);
+            else
+              mma_f8(d, adesc + 2 * k, bdesc + 2 * k, p.idesc, accumulate);
           }
-          mma_commit(bar_empty + 8 * stage);
+          if constexpr (PAIR)
+            mma_commit_pair(bar_empty + 8 * stage, 0x3);  // frees the stage in both CTAs
+          else
+            mma_commit(bar_empty + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -269,14 +317,20 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
           }
         }
         if (!BLOCK && ok) {
-          mma_commit(bar_tfull + 8 * acc);
+          if constexpr (PAIR)
+            mma_commit_pair(bar_tfull + 8 * acc, 0x3);  // both halves of the tile are ready
+          else
+            mma_commit(bar_tfull + 8 * acc);
           acc = (acc + 1 == ACC) ? 0 : acc + 1;
           if (acc == 0) acc_phase ^= 1u;
         }
       }
       FP8GB_STAMP(3);
       // every MMA this thread issued has completed once this barrier flips
-      mma_commit(bar_final);
+      if constexpr (PAIR)
+        mma_commit_pair(bar_final, 0x1);
+      else
+        mma_commit(bar_final);
       if (!mbar_wait_drain(bar_final, 0, 1000000000ull)) atomicOr(p.w.err, DEV_ERR_WAIT_TEARDOWN);
       FP8GB_STAMP(4);
     }
@@ -312,34 +366,47 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
       // the tile's 64-column chunks alternate between the two warps of a lane quarter
       const int hc = ew >> 2;
       constexpr int NCH = BN / 64;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      const uint32_t tempty_lead = PAIR ? mapa_shared(bar_tempty, 0) : bar_tempty;
+      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
         int mb, nb;
         tile_coords(t, p, mb, nb);
+        const int row0 = mb * TILE_M + static_cast<int>(rank) * BM + q * 32;  // this warp's 32 rows
+        const bool rows_live = row0 < p.M;
         if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE)) break;
         __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the spin
         tc_fence_after();
-#pragma unroll 1
-        for (int ch = hc; ch < NCH; ch += 2) {
-          __syncwarp();
-          uint32_t r0[32], r1[32];
-          const int col = ch * 64;
-          const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col);
-          tmem_ld32(taddr, r0);
-          tmem_ld32(taddr + 32, r1);
-          tmem_ld_wait();
-          reg_fence(r0);
-          reg_fence(r1);
-          if (ch + 2 >= NCH) {  // this warp's part of the accumulator is read: hand it back
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
-          }
+        // both of this warp's chunks (64 columns each) are read before the accumulator is
+        // handed back, so the next tile's MMAs do not wait for this tile's stores
+        const bool two = NCH > 2 && hc + 2 < NCH;
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + hc * 64);
+        tmem_ld32(taddr, r0);
+        tmem_ld32(taddr + 32, r1);
+        if (two) {
+          tmem_ld32(taddr + 128, r2);
+          tmem_ld32(taddr + 160, r3);
+        }
+        tmem_ld_wait();
+        reg_fence(r0);
+        reg_fence(r1);
+        reg_fence(r2);
+        reg_fence(r3);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR)
+            mbar_arrive_cluster(tempty_lead + 8 * acc);
+          else
+            mbar_arrive(bar_tempty + 8 * acc);
+        }
+        // scale, convert to bf16 (and FP8 when fused), stage and store one 64-column chunk
+        auto emit = [&](const uint32_t(&ra)[32], const uint32_t(&rb)[32], int col) {
           uint32_t pk[32];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            pk[j] = pack_bf16x2(__fmul_rn(__uint_as_float(r0[2 * j]), dd), __fmul_rn(__uint_as_float(r0[2 * j + 1]), dd));
+            pk[j] = pack_bf16x2(__fmul_rn(__uint_as_float(ra[2 * j]), dd), __fmul_rn(__uint_as_float(ra[2 * j + 1]), dd));
             pk[16 + j] =
-                pack_bf16x2(__fmul_rn(__uint_as_float(r1[2 * j]), dd), __fmul_rn(__uint_as_float(r1[2 * j + 1]), dd));
+                pack_bf16x2(__fmul_rn(__uint_as_float(rb[2 * j]), dd), __fmul_rn(__uint_as_float(rb[2 * j + 1]), dd));
           }
           if (lane == 0) bulk_wait_group_read<0>();  // the previous stores have read the staging buffers
           __syncwarp();
@@ -365,12 +432,14 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmC, smem_u32(stg), nb * BN + col, mb * BM + q * 32);
-            if (fused) tma_store_2d(&tmQ, smem_u32(qstg), nb * BN + col, mb * BM + q * 32);
+          if (lane == 0 && rows_live) {
+            tma_store_2d(&tmC, smem_u32(stg), nb * BN + col, row0);
+            if (fused) tma_store_2d(&tmQ, smem_u32(qstg), nb * BN + col, row0);
             bulk_commit_group();
           }
-        }
+        };
+        emit(r0, r1, hc * 64);
+        if (two) emit(r2, r3, (hc + 2) * 64);
         acc = (acc + 1 == ACC) ? 0 : acc + 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -385,50 +454,60 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
         }
       }
     } else {
-      // each warp folds 64 columns (one 128-column scale block = BN / 128 ... of them) of its
-      // TMEM lane quarter: two x32 loads issued back to back, one wait, 64 FMAs
+      // each warp folds 64 columns (half of the 128-column scale block) of its TMEM lane
+      // quarter, as two 32-column chunks per K block. The load of the next chunk is in flight
+      // while the current one is folded (software pipeline over chunks), so a TMEM round trip
+      // overlaps 32 FMAs instead of stalling the warp.
       const int col0 = (ew >> 2) * 64;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
         int mb, nb;
         tile_coords(t, p, mb, nb);
         const int row = mb * BM + q * 32 + lane;
         const int nblk = (nb * BN + col0) / 128;
         const bool row_ok = row < p.M;
         const bool col_ok = nblk * 128 < p.N;
+        const float* sa_row = p.sa + (int64_t)row * p.sa_ld;
+        const float* sb_col = p.sb + nblk;
         float accum[64];
 #pragma unroll
         for (int j = 0; j < 64; ++j) accum[j] = 0.0f;
-        float sa_next = row_ok ? __ldg(p.sa + (int64_t)row * p.sa_ld) : 0.0f;
-        float sb_next = col_ok ? __ldg(p.sb + nblk) : 0.0f;
+        float sa_n = row_ok ? __ldg(sa_row) : 0.0f;
+        float sb_n = col_ok ? __ldg(sb_col) : 0.0f;
+        uint32_t ra[32], rb[32];
+        if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE)) break;
+        __syncwarp();
+        tc_fence_after();
+        tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), ra);
+        tmem_ld_wait();
+        reg_fence(ra);
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          const float sc = __fmul_rn(sa_next, sb_next);
-          if (kb + 1 < p.num_kb) {
-            sa_next = row_ok ? __ldg(p.sa + (int64_t)row * p.sa_ld + kb + 1) : 0.0f;
-            sb_next = col_ok ? __ldg(p.sb + (int64_t)(kb + 1) * p.sb_ld + nblk) : 0.0f;
-          }
-          if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE)) {
-            ok = false;
-            break;
-          }
-          __syncwarp();
-          tc_fence_after();
-          const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0);
-          uint32_t r0[32], r1[32];
-          tmem_ld32(taddr, r0);
-          tmem_ld32(taddr + 32, r1);
+          const float sc = __fmul_rn(sa_n, sb_n);
+          const bool more = kb + 1 < p.num_kb;
+          sa_n = (row_ok && more) ? __ldg(sa_row + kb + 1) : 0.0f;
+          sb_n = (col_ok && more) ? __ldg(sb_col + (int64_t)(kb + 1) * p.sb_ld) : 0.0f;
+          tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0 + 32), rb);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) accum[j] = fmaf(__uint_as_float(ra[j]), sc, accum[j]);
           tmem_ld_wait();
-          reg_fence(r0);
-          reg_fence(r1);
+          reg_fence(rb);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);  // registers hold the block now
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            accum[j] = fmaf(__uint_as_float(r0[j]), sc, accum[j]);
-            accum[32 + j] = fmaf(__uint_as_float(r1[j]), sc, accum[32 + j]);
-          }
+          if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);  // block kb is in registers
           acc = (acc + 1 == ACC) ? 0 : acc + 1;
           if (acc == 0) acc_phase ^= 1u;
+          if (more) {
+            ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE);
+            __syncwarp();
+            tc_fence_after();
+            if (ok) tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), ra);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) accum[32 + j] = fmaf(__uint_as_float(rb[j]), sc, accum[32 + j]);
+          if (!ok) break;
+          if (more) {
+            tmem_ld_wait();
+            reg_fence(ra);
+          }
         }
         if (!ok) break;
         uint32_t pk[32];
@@ -445,11 +524,16 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // a pair's CTAs leave together: no MMA, commit arrival or TMA write targets an exited CTA
+  if constexpr (PAIR) cluster_sync_all();
   if (threadIdx.x == 0) FP8GB_STAMP(6);
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -478,38 +562,80 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t
   return encode_tmap_2d(m, base, dt, inner, outer, row_bytes, box_inner, box_outer, 128);
 }
 
-template <bool BLOCK, int BN, int QF>
-cudaError_t prepare_kernel() {
-  // the attribute is per device; remember which devices were configured
+template <bool BLOCK, int BN, int QF, bool PAIR>
+cudaError_t prepare_kernel(int* pair_clusters) {
+  // the attribute is per device; remember which devices were configured and, for CTA-pair
+  // kernels, how many pairs the device holds at once
   static bool done[64] = {};
+  static int clusters[64] = {};
   static std::mutex mu;
+  using C = Cfg<BLOCK, BN, QF, PAIR>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(mu);
-  if (dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(gemm_f8_kernel<BLOCK, BN, QF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<BLOCK, BN, QF>::SMEM);
-  if (e == cudaSuccess && dev < 64) done[dev] = true;
-  return e;
+  if (dev < 64 && done[dev]) {
+    *pair_clusters = clusters[dev];
+    return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(gemm_f8_kernel<BLOCK, BN, QF, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  int n = 0;
+  if (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(gemm_f8_kernel<BLOCK, BN, QF, PAIR>), &cfg);
+    if (e != cudaSuccess) return e;
+  }
+  if (dev < 64) {
+    done[dev] = true;
+    clusters[dev] = n;
+  }
+  *pair_clusters = n;
+  return cudaSuccess;
 }
 
-// Tile width: cost = rounds of tiles over the SMs x time of one tile (width / mainloop
-// efficiency). Narrower tiles move more operand bytes per FLOP: measured on GB300 the
-// mainloop runs at ~94 % of the tensor peak with 256-wide tiles, ~80 % with 192-wide and
-// ~60 % with 128-wide ones. Narrower tiles win only when they save rounds.
-int choose_bn(int64_t M, int64_t N, int sms) {
-  const int64_t tm = (M + BM - 1) / BM;
+// Tile shape: cost = rounds of tiles over the SMs (or CTA pairs) x time of one round.
+// Measured on GB300, a CTA takes in ~140 GB/s of operands, so a 128 x BN tile's mainloop
+// runs at ~80 % of the tensor peak with BN = 256 (48 KB per 128-deep K block), less with
+// narrower tiles; a CTA pair moves 16 KB + BN * 64 bytes per CTA and K block for the same
+// work and is bound by the tensor pipe at BN = 256 and 192. Weights are per-SM times of one
+// round in arbitrary units.
+struct TileChoice {
+  int bn;
+  bool pair;
+};
+
+TileChoice choose_tile(int64_t M, int64_t N, int sms, int pair_clusters) {
   const int widths[3] = {256, 192, 128};
-  const int per_round[3] = {272, 240, 213};  // width / efficiency
-  int best = 256;
+  const int w_single[3] = {272, 240, 213};
+  const int w_pair[3] = {236, 184, 150};
+  TileChoice best{256, false};
   int64_t best_cost = -1;
   for (int i = 0; i < 3; ++i) {
-    const int64_t rounds = (tm * ((N + widths[i] - 1) / widths[i]) + sms - 1) / sms;
-    const int64_t cost = rounds * per_round[i];
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = widths[i];
+    const int64_t tn = (N + widths[i] - 1) / widths[i];
+    const int64_t r1 = ((M + BM - 1) / BM * tn + sms - 1) / sms;
+    const int64_t c1 = r1 * w_single[i];
+    if (best_cost < 0 || c1 < best_cost) {
+      best_cost = c1;
+      best = {widths[i], false};
+    }
+    if (M > BM && pair_clusters > 0) {  // a pair computes 256 rows: pointless for M <= 128
+      const int64_t r2 = ((M + 2 * BM - 1) / (2 * BM) * tn + pair_clusters - 1) / pair_clusters;
+      const int64_t c2 = r2 * w_pair[i];
+      if (c2 < best_cost) {
+        best_cost = c2;
+        best = {widths[i], true};
+      }
     }
   }
   return best;
@@ -518,22 +644,69 @@ int choose_bn(int64_t M, int64_t N, int sms) {
 template <bool BLOCK, int BN, int QF>
 cudaError_t launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tq,
                            KParams p, cudaStream_t stream) {
-  cudaError_t e = prepare_kernel<BLOCK, BN, QF>();
+  int unused = 0;
+  cudaError_t e = prepare_kernel<BLOCK, BN, QF, false>(&unused);
   if (e != cudaSuccess) return e;
   p.num_n = (p.N + BN - 1) / BN;
   p.num_tiles = p.num_m * p.num_n;
   p.idesc = idesc_f8(p.idesc & 7u, (p.idesc >> 3) & 7u, BM, BN);
   const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  return launch_pdl(gemm_f8_kernel<BLOCK, BN, QF>, dim3(grid), dim3(Cfg<BLOCK, BN, QF>::THREADS),
-                    Cfg<BLOCK, BN, QF>::SMEM, stream, ta, tb, tc, tq, p);
+  return launch_pdl(gemm_f8_kernel<BLOCK, BN, QF, false>, dim3(grid), dim3(Cfg<BLOCK, BN, QF, false>::THREADS),
+                    Cfg<BLOCK, BN, QF, false>::SMEM, stream, ta, tb, tc, tq, p);
+}
+
+// CTA-pair launch: clusters of two, one pair per 256 x BN tile, persistent over the tiles.
+template <int BN, int QF>
+cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tq,
+                        KParams p, cudaStream_t stream) {
+  using C = Cfg<false, BN, QF, true>;
+  int clusters = 0;
+  cudaError_t e = prepare_kernel<false, BN, QF, true>(&clusters);
+  if (e != cudaSuccess) return e;
+  if (clusters <= 0) return cudaErrorInvalidConfiguration;
+  p.num_m = (p.M + 2 * BM - 1) / (2 * BM);
+  p.num_n = (p.N + BN - 1) / BN;
+  p.num_tiles = p.num_m * p.num_n;
+  p.idesc = idesc_f8(p.idesc & 7u, (p.idesc >> 3) & 7u, 2 * BM, BN);
+  const int ncl = p.num_tiles < clusters ? p.num_tiles : clusters;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * ncl);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_f8_kernel<false, BN, QF, true>, ta, tb, tc, tq, p);
 }
 
 template <int QF>
-cudaError_t launch_width(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+cudaError_t launch_width(TileChoice tc_, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                          const CUtensorMap& tq, const KParams& p, cudaStream_t stream) {
-  if (bn == 256) return launch_variant<false, 256, QF>(ta, tb, tc, tq, p, stream);
-  if (bn == 192) return launch_variant<false, 192, QF>(ta, tb, tc, tq, p, stream);
+  if (tc_.pair) {
+    if (tc_.bn == 256) return launch_pair<256, QF>(ta, tb, tc, tq, p, stream);
+    if (tc_.bn == 192) return launch_pair<192, QF>(ta, tb, tc, tq, p, stream);
+    return launch_pair<128, QF>(ta, tb, tc, tq, p, stream);
+  }
+  if (tc_.bn == 256) return launch_variant<false, 256, QF>(ta, tb, tc, tq, p, stream);
+  if (tc_.bn == 192) return launch_variant<false, 192, QF>(ta, tb, tc, tq, p, stream);
   return launch_variant<false, 128, QF>(ta, tb, tc, tq, p, stream);
+}
+
+// Pairs the device holds at once (0 when it cannot launch clusters of two).
+int pair_capacity() {
+  int n = 0;
+  if (prepare_kernel<false, 256, -1, true>(&n) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 }  // namespace
@@ -554,16 +727,24 @@ bool encode_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, ui
 }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why) {
-  // block scaling folds every 128-deep K block out of TMEM: 128-wide tiles keep the fold's
-  // registers (64 fp32 per thread) and its four accumulator buffers within budget
-#ifdef FP8GB_FORCE_BN  // compile-time override of the tile-width heuristic, for tuning builds
-  const int bn = g.block_scaled ? 128 : FP8GB_FORCE_BN;
-#else
-  const int bn = g.block_scaled ? 128 : choose_bn(g.M, g.N, num_sms());
+  // block scaling folds every 128-deep K block out of TMEM: 128-wide single-CTA tiles keep
+  // the fold's registers (64 fp32 per thread) and its four accumulator buffers within budget
+  TileChoice choice{128, false};
+  if (!g.block_scaled) {
+#ifdef FP8GB_FORCE_BN  // compile-time override of the tile choice, for tuning builds
+#ifndef FP8GB_FORCE_PAIR
+#define FP8GB_FORCE_PAIR 0
 #endif
+    choice = {FP8GB_FORCE_BN, FP8GB_FORCE_PAIR != 0};
+#else
+    choice = choose_tile(g.M, g.N, num_sms(), pair_capacity());
+#endif
+  }
+  const int bn = choice.bn;
+  const uint32_t b_rows = choice.pair ? static_cast<uint32_t>(bn / 2) : static_cast<uint32_t>(bn);
   CUtensorMap ta, tb, tc;
   if (!make_map(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.M, g.lda, BK, BM) ||
-      !make_map(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.N, g.ldb, BK, bn) ||
+      !make_map(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.N, g.ldb, BK, b_rows) ||
       !make_map(&tc, g.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.N, g.M, g.ldc * 2, 64, 32)) {
     *why = "cuTensorMapEncodeTiled failed (driver entry point missing or tensor map rejected)";
     return cudaErrorInvalidValue;
@@ -593,9 +774,9 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why
     p.cst = g.cst;
   }
   if (g.block_scaled) return launch_variant<true, 128, -1>(ta, tb, tc, tq, p, stream);
-  if (g.qf == 0) return launch_width<0>(bn, ta, tb, tc, tq, p, stream);
-  if (g.qf == 1) return launch_width<1>(bn, ta, tb, tc, tq, p, stream);
-  return launch_width<-1>(bn, ta, tb, tc, tq, p, stream);
+  if (g.qf == 0) return launch_width<0>(choice, ta, tb, tc, tq, p, stream);
+  if (g.qf == 1) return launch_width<1>(choice, ta, tb, tc, tq, p, stream);
+  return launch_width<-1>(choice, ta, tb, tc, tq, p, stream);
 }
 
 }  // namespace fp8gb
