@@ -605,11 +605,12 @@ cudaError_t prepare_kernel(int* pair_clusters) {
 }
 
 // Tile shape: cost = rounds of tiles over the SMs (or CTA pairs) x time of one round.
-// Measured on GB300, a CTA takes in ~140 GB/s of operands, so a 128 x BN tile's mainloop
-// runs at ~80 % of the tensor peak with BN = 256 (48 KB per 128-deep K block), less with
-// narrower tiles; a CTA pair moves 16 KB + BN * 64 bytes per CTA and K block for the same
-// work and is bound by the tensor pipe at BN = 256 and 192. Weights are per-SM times of one
-// round in arbitrary units.
+// Measured on GB300 (ns per 128-deep K block of one tile, 16384 x 14336 x 4096): the tensor
+// pipe takes ~280-300 ns for any N <= 256, so narrower tiles save little time per tile; a
+// single CTA with 256-wide tiles is bound by its operand intake (~140 GB/s, 48 KB per K
+// block) at ~360 ns, 192-wide at ~320 ns; a CTA pair loads 16 KB + BN * 64 bytes per CTA
+// and K block and runs at the tensor pipe's rate. Narrower tiles win only when they save
+// rounds.
 struct TileChoice {
   int bn;
   bool pair;
@@ -617,8 +618,8 @@ struct TileChoice {
 
 TileChoice choose_tile(int64_t M, int64_t N, int sms, int pair_clusters) {
   const int widths[3] = {256, 192, 128};
-  const int w_single[3] = {272, 240, 213};
-  const int w_pair[3] = {236, 184, 150};
+  const int w_single[3] = {362, 322, 275};
+  const int w_pair[3] = {300, 285, 278};
   TileChoice best{256, false};
   int64_t best_cost = -1;
   for (int i = 0; i < 3; ++i) {

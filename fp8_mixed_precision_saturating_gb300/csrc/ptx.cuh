@@ -155,8 +155,11 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 // Arrive once on an mbarrier given by its shared::cluster address (this CTA's or a peer's).
+// Release at CTA scope only: callers order their tensor-memory reads before the arrive with
+// tcgen05.fence::before_thread_sync and hand over no generic-memory data, so the
+// cluster-scope release (a full memory barrier) is not needed.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 // 2-D tiled load into this CTA's shared memory whose transaction bytes are signalled on an
