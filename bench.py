@@ -187,17 +187,21 @@ def run_gpu(args):
     T = g.FP8_GRAN_TENSOR
     gemm_flops = 2.0 * M * N * K
 
+    # one split-K workspace for the three GEMMs (they run in order on one stream); the
+    # library splits only shapes with too few output tiles (here the weight gradient)
+    ws_bytes = max(g.fp8_scaled_mm_workspace_bytes(*s) for s in ((M, N, K), (M, K, N), (K, N, M)))
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
     # (name, call, kernels launched, algorithmic flops, algorithmic bytes)
     stages = [
         ("requant_w", lambda: g.fp8_requantize_weights(wm, K, N, T, D, wst, wq, wqT), 1, 0.0, K * N * 4.0),
         ("quant_x", lambda: g.fp8_quantize(x, M, K, K, g.FP8_E4M3, T, D, xst, xq, xqT), 1, 0.0, M * K * 4.0),
-        ("gemm_fwd", lambda: g.fp8_scaled_mm(xq, 0, wqT, 0, M, N, K, K, K, T, xst.scale_inv, wst.scale_inv, y, N),
-         1, gemm_flops, 0.0),
+        ("gemm_fwd", lambda: g.fp8_scaled_mm_ws(xq, 0, wqT, 0, M, N, K, K, K, T, xst.scale_inv, wst.scale_inv, y, N,
+                                                ws, ws_bytes), 1, gemm_flops, 0.0),
         ("quant_dy", lambda: g.fp8_quantize(dy, M, N, N, g.FP8_E5M2, T, D, gst, dyq, dyqT), 1, 0.0, M * N * 4.0),
-        ("gemm_dgrad", lambda: g.fp8_scaled_mm(dyq, 1, wq, 0, M, K, N, N, N, T, gst.scale_inv, wst.scale_inv, dx, K),
-         1, gemm_flops, 0.0),
-        ("gemm_wgrad", lambda: g.fp8_scaled_mm(xqT, 0, dyqT, 1, K, N, M, M, M, T, xst.scale_inv, gst.scale_inv, dw, N),
-         1, gemm_flops, 0.0),
+        ("gemm_dgrad", lambda: g.fp8_scaled_mm_ws(dyq, 1, wq, 0, M, K, N, N, N, T, gst.scale_inv, wst.scale_inv, dx, K,
+                                                  ws, ws_bytes), 1, gemm_flops, 0.0),
+        ("gemm_wgrad", lambda: g.fp8_scaled_mm_ws(xqT, 0, dyqT, 1, K, N, M, M, M, T, xst.scale_inv, gst.scale_inv, dw,
+                                                  N, ws, ws_bytes), 1, gemm_flops, 0.0),
         ("commit", lambda: g.fp8_history_commit_many([wst, xst, gst]), 1, 0.0, 0.0),
     ]
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -474,10 +478,18 @@ def run_sweep(args):
             sa = torch.full((1,), 1e-2, device="cuda")
             sb = torch.full((1,), 1e-2, device="cuda")
             gran = g.FP8_GRAN_TENSOR
-        ms = timed(lambda: g.fp8_scaled_mm(A, fa, B, fb, m, n, k, k, k, gran, sa, sb, C, n), args.steps)
+        # per-tensor GEMMs through the workspace entry point (split K where the shape asks)
+        wsb = 0 if blk else g.fp8_scaled_mm_workspace_bytes(m, n, k)
+        ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
+        if blk:
+            fn = lambda: g.fp8_scaled_mm(A, fa, B, fb, m, n, k, k, k, gran, sa, sb, C, n)
+        else:
+            fn = lambda: g.fp8_scaled_mm_ws(A, fa, B, fb, m, n, k, k, k, gran, sa, sb, C, n, ws, wsb)
+        ms = timed(fn, args.steps)
         tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
         print(json.dumps({"sweep": "gemm", "name": name, "M": m, "N": n, "K": k, "block_scaled": blk,
-                          "ms": round(ms, 5), "TFLOP/s": round(tf, 1), "frac_fp8_peak": round(tf / fp8_peak, 4)}))
+                          "split_k_workspace": wsb, "ms": round(ms, 5), "TFLOP/s": round(tf, 1),
+                          "frac_fp8_peak": round(tf / fp8_peak, 4)}))
         del A, B, C
     for name, r, c, fmt, gran, tr in SWEEP_CASTS:
         if only and name not in only:

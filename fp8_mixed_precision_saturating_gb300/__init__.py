@@ -49,6 +49,7 @@ _SP = ctypes.POINTER(fp8_tensor_state_t)
 _SIGS = {
     "fp8_quantize": [_P, _I64, _I64, _I64, _I, _I, _I, _SP, _P, _P, _P, _P],
     "fp8_scaled_mm": [_P, _I, _P, _I, _I64, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _P],
+    "fp8_scaled_mm_ws": [_P, _I, _P, _I, _I64, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _P, _I64, _P],
     "fp8_scaled_mm_quant": [_P, _I, _P, _I, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _I64, _I, _SP, _P, _P],
     "fp8_requantize_weights": [_P, _I64, _I64, _I, _I, _SP, _P, _P, _P, _P],
     "fp8_update_requantize_weights": [_P, _P, _I64, _I64, _I, _SP, _P, _P, _P],
@@ -66,6 +67,8 @@ for _name, _args in _SIGS.items():
     _f = getattr(lib, _name)
     _f.argtypes = _args
     _f.restype = ctypes.c_int
+lib.fp8_scaled_mm_workspace_bytes.argtypes = [_I64, _I64, _I64]
+lib.fp8_scaled_mm_workspace_bytes.restype = ctypes.c_int64
 lib.fp8_status_string.argtypes = [ctypes.c_int]
 lib.fp8_status_string.restype = ctypes.c_char_p
 
@@ -169,6 +172,20 @@ def fp8_quantize(x, rows, cols, ld, fmt, gran, mode, st, q_out, qT_out=None, uni
 def fp8_scaled_mm(A, fa, B, fb, M, N, K, lda, ldb, gran, scale_inv_a, scale_inv_b, C, ldc, stream=None):
     return _check(lib.fp8_scaled_mm(_ptr(A), fa, _ptr(B), fb, M, N, K, lda, ldb, gran, _ptr(scale_inv_a),
                                     _ptr(scale_inv_b), _ptr(C), ldc, _stream(stream)))
+
+
+def fp8_scaled_mm_ws(A, fa, B, fb, M, N, K, lda, ldb, gran, scale_inv_a, scale_inv_b, C, ldc, workspace,
+                     workspace_bytes, stream=None):
+    return _check(lib.fp8_scaled_mm_ws(_ptr(A), fa, _ptr(B), fb, M, N, K, lda, ldb, gran, _ptr(scale_inv_a),
+                                       _ptr(scale_inv_b), _ptr(C), ldc, _ptr(workspace), workspace_bytes,
+                                       _stream(stream)))
+
+
+def fp8_scaled_mm_workspace_bytes(M, N, K) -> int:
+    n = lib.fp8_scaled_mm_workspace_bytes(M, N, K)
+    if n < 0:
+        raise Fp8Error(FP8_ERR_CUDA, "fp8_scaled_mm_workspace_bytes")
+    return n
 
 
 def fp8_scaled_mm_quant(A, fa, B, fb, M, N, K, lda, ldb, scale_inv_a, scale_inv_b, C, ldc, fc, c_st, Cq,

@@ -170,8 +170,8 @@ fp8_status_t quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld
 
 fp8_status_t scaled_mm_impl(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb, int64_t M, int64_t N,
                             int64_t K, int64_t lda, int64_t ldb, fp8_gran_t gran, const float* sa, const float* sb,
-                            void* C, int64_t ldc, cudaStream_t stream) {
-  const char* who = "fp8_scaled_mm";
+                            void* C, int64_t ldc, cudaStream_t stream, void* ws = nullptr, int64_t ws_bytes = 0,
+                            const char* who = "fp8_scaled_mm") {
   if (M < 0 || N < 0 || K < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
   if ((fa != FP8_E4M3 && fa != FP8_E5M2) || (fb != FP8_E4M3 && fb != FP8_E5M2))
     return fail(FP8_ERR_INVALID_ARG, "%s: unknown format", who);
@@ -194,6 +194,10 @@ fp8_status_t scaled_mm_impl(const void* A, fp8_format_t fa, const void* B, fp8_f
   if (gran == FP8_GRAN_BLOCK_128x128 && (K % 128 != 0 || N % 128 != 0))
     return fail(FP8_ERR_UNSUPPORTED, "%s: block scaling needs K and N multiples of 128", who);
   GemmArgs g{A, B, C, M, N, K, lda, ldb, ldc, (int)fa, (int)fb, sa, sb, gran == FP8_GRAN_BLOCK_128x128};
+  if (ws != nullptr && gran == FP8_GRAN_TENSOR) {
+    g.ws = ws;
+    g.ws_bytes = ws_bytes;
+  }
   const char* why = "launch";
   cudaError_t e = launch_gemm(g, stream, &why);
   if (e != cudaSuccess) return cuda_fail(e, why);
@@ -216,6 +220,27 @@ fp8_status_t fp8_scaled_mm(const void* A, fp8_format_t fa, const void* B, fp8_fo
                            const float* scale_inv_b, void* C_bf16, int64_t ldc, void* stream) {
   return scaled_mm_impl(A, fa, B, fb, M, N, K, lda, ldb, gran, scale_inv_a, scale_inv_b, C_bf16, ldc,
                         static_cast<cudaStream_t>(stream));
+}
+
+fp8_status_t fp8_scaled_mm_ws(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb, int64_t M, int64_t N,
+                              int64_t K, int64_t lda, int64_t ldb, fp8_gran_t gran, const float* scale_inv_a,
+                              const float* scale_inv_b, void* C_bf16, int64_t ldc, void* workspace,
+                              int64_t workspace_bytes, void* stream) {
+  const char* who = "fp8_scaled_mm_ws";
+  if (gran != FP8_GRAN_TENSOR) return fail(FP8_ERR_UNSUPPORTED, "%s: per-tensor scales only", who);
+  if (workspace_bytes < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative workspace size", who);
+  if (workspace != nullptr && !aligned16(workspace))
+    return fail(FP8_ERR_ALIGNMENT, "%s: workspace must be 16-byte aligned", who);
+  return scaled_mm_impl(A, fa, B, fb, M, N, K, lda, ldb, gran, scale_inv_a, scale_inv_b, C_bf16, ldc,
+                        static_cast<cudaStream_t>(stream), workspace, workspace_bytes, who);
+}
+
+int64_t fp8_scaled_mm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (current_device() < 0) {
+    fail(FP8_ERR_CUDA, "fp8_scaled_mm_workspace_bytes: no CUDA device");
+    return -1;
+  }
+  return gemm_workspace_bytes(M, N, K);
 }
 
 fp8_status_t fp8_scaled_mm_quant(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb, int64_t M,

@@ -101,7 +101,21 @@ struct KParams {
   int sa_ld, sb_ld;
   WaitCtl w;
   QuantState cst;  // scaling state of the FP8 output (QF >= 0)
+  // split K: each output tile is `splits` (1 or 2) work units over the two halves of its
+  // K blocks; the last unit of a tile to finish adds the other's fp32 partial (ws) to its own.
+  // ws_cnt holds one arrival counter per (tile, CTA rank, epilogue warp), zero between calls.
+  int splits;
+  float4* ws;
+  int* ws_cnt;
 };
+
+// Work unit u -> output tile and its K-block range [kb0, kb1).
+__device__ __forceinline__ void unit_range(int u, const KParams& p, int& tile, int& split, int& kb0, int& kb1) {
+  tile = u / p.splits;
+  split = u - tile * p.splits;
+  kb0 = split * p.num_kb / p.splits;
+  kb1 = (split + 1) * p.num_kb / p.splits;
+}
 
 __device__ __forceinline__ void tile_coords(int t, const KParams& p, int& mb, int& nb) {
   const int per_group = GROUP_M * p.num_n;
@@ -215,12 +229,13 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
       uint32_t issued_mask = 0, issued_phase = 0;  // per stage: issued?, parity of last issue
       bool ok = true;
       const uint32_t full_lead = PAIR ? mapa_shared(bar_full, 0) : bar_full;
-      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
-        int mb, nb;
+      for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step) {
+        int t, split, kb0, kb1, mb, nb;
+        unit_range(u, p, t, split, kb0, kb1);
         tile_coords(t, p, mb, nb);
         const int arow = mb * TILE_M + static_cast<int>(rank) * BM;
         const int brow = nb * BN + static_cast<int>(rank) * C::B_ROWS;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.w, DEV_ERR_WAIT_PRODUCER)) {
             ok = false;
             break;
@@ -269,12 +284,14 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
+      for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step) {
+        int t, split, kb0, kb1;
+        unit_range(u, p, t, split, kb0, kb1);
         if (!BLOCK) {
           if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.w, DEV_ERR_WAIT_MMA)) break;
           tc_fence_after();
         }
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (BLOCK) {
             if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.w, DEV_ERR_WAIT_MMA)) {
               ok = false;
@@ -296,7 +313,7 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
           const uint64_t bdesc = smem_desc_sw128(sa + A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k) {
-            const uint32_t accumulate = BLOCK ? (k != 0) : ((kb | k) != 0);
+            const uint32_t accumulate = BLOCK ? (k != 0) : (kb != kb0 || k != 0);
             if constexpr (PAIR)
               mma_f8_pair(d, adesc + 2 * k, bdesc + 2 * k, p.idesc, accumulate);
             else
@@ -367,8 +384,9 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
       const int hc = ew >> 2;
       constexpr int NCH = BN / 64;
       const uint32_t tempty_lead = PAIR ? mapa_shared(bar_tempty, 0) : bar_tempty;
-      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
-        int mb, nb;
+      for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step) {
+        int t, split, kb0, kb1, mb, nb;
+        unit_range(u, p, t, split, kb0, kb1);
         tile_coords(t, p, mb, nb);
         const int row0 = mb * TILE_M + static_cast<int>(rank) * BM + q * 32;  // this warp's 32 rows
         const bool rows_live = row0 < p.M;
@@ -438,8 +456,65 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
             bulk_commit_group();
           }
         };
-        emit(r0, r1, hc * 64);
-        if (two) emit(r2, r3, (hc + 2) * 64);
+        bool last = true;  // this unit stores the tile
+        if constexpr (QF < 0 && BN != 192) {  // split K: 256- and 128-wide bf16-output tiles
+          if (p.splits > 1) {
+            // this warp's slice of the partial tile: 32 lanes x (64 or 128) fp32, stored so that
+            // each float4 index is 512 contiguous bytes across the warp
+            constexpr int SLOT_V = ((NCH + 1) / 2) * 16;  // float4 per lane
+            const int slice = (t * (PAIR ? 2 : 1) + static_cast<int>(rank)) * C::EPI_WARPS + ew;
+            float4* slot0 = p.ws + static_cast<size_t>(slice) * p.splits * SLOT_V * 32;
+            float4* mine = slot0 + static_cast<size_t>(split) * SLOT_V * 32 + lane;
+            auto put = [&](const uint32_t(&r)[32], int v0) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                __stcg(mine + (v0 + i) * 32, make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                         __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+            };
+            put(r0, 0);
+            put(r1, 8);
+            if (two) {
+              put(r2, 16);
+              put(r3, 24);
+            }
+            __threadfence();
+            __syncwarp();
+            int ticket = 0;
+            if (lane == 0) ticket = atomicAdd(p.ws_cnt + slice, 1);
+            ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
+            last = ticket == p.splits - 1;
+            if (last) {
+              __threadfence();
+              // two splits: add the other unit's partial to this one's in place; fp32 addition
+              // is commutative, so the sum does not depend on which unit finished last. Eight
+              // loads in flight per lane, then eight adds.
+              const float4* other = slot0 + static_cast<size_t>(1 - split) * SLOT_V * 32 + lane;
+              auto add = [&](uint32_t(&r)[32], int v0) {
+                float4 b[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) b[i] = __ldcg(other + (v0 + i) * 32);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  r[4 * i] = __float_as_uint(__fadd_rn(__uint_as_float(r[4 * i]), b[i].x));
+                  r[4 * i + 1] = __float_as_uint(__fadd_rn(__uint_as_float(r[4 * i + 1]), b[i].y));
+                  r[4 * i + 2] = __float_as_uint(__fadd_rn(__uint_as_float(r[4 * i + 2]), b[i].z));
+                  r[4 * i + 3] = __float_as_uint(__fadd_rn(__uint_as_float(r[4 * i + 3]), b[i].w));
+                }
+              };
+              add(r0, 0);
+              add(r1, 8);
+              if (two) {
+                add(r2, 16);
+                add(r3, 24);
+              }
+              if (lane == 0) p.ws_cnt[slice] = 0;  // zero again for the next call
+            }
+          }
+        }
+        if (last) {
+          emit(r0, r1, hc * 64);
+          if (two) emit(r2, r3, (hc + 2) * 64);
+        }
         acc = (acc + 1 == ACC) ? 0 : acc + 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -459,7 +534,7 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
       // while the current one is folded (software pipeline over chunks), so a TMEM round trip
       // overlaps 32 FMAs instead of stalling the warp.
       const int col0 = (ew >> 2) * 64;
-      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
+      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {  // block scaling never splits K
         int mb, nb;
         tile_coords(t, p, mb, nb);
         const int row = mb * BM + q * 32 + lane;
@@ -614,32 +689,68 @@ cudaError_t prepare_kernel(int* pair_clusters) {
 struct TileChoice {
   int bn;
   bool pair;
+  int splits;
 };
 
-TileChoice choose_tile(int64_t M, int64_t N, int sms, int pair_clusters) {
+// Split K costs each unit a write of its fp32 partial and the tile's last unit a read of all
+// of them (~128 KB per CTA each at ~140 GB/s): about 3 K blocks of time per unit and round,
+// plus ~900 ns per split for the last round's reads. Splits are for tiles too few to fill
+// the GPU, with a workspace that stays in L2.
+constexpr int kSplitCostNs = 900;
+constexpr int kSplitUnitKb = 3;
+constexpr int64_t kSplitMaxBytes = int64_t(64) << 20;
+// The workspace starts with a fixed 16 KB of arrival counters (one per tile, CTA rank and
+// epilogue warp: at most 64 MB / (2 splits x 8 KB) = 4096 of them), so the partials of one
+// shape never overlap the counters of another and a reused workspace needs no clearing.
+constexpr int64_t kSplitCounterBytes = 4096 * 4;
+
+TileChoice choose_tile(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters, int max_splits) {
   const int widths[3] = {256, 192, 128};
   const int w_single[3] = {362, 322, 275};
   const int w_pair[3] = {300, 285, 278};
-  TileChoice best{256, false};
+  const int64_t kb = (K + BK - 1) / BK;
+  TileChoice best{256, false, 1};
   int64_t best_cost = -1;
   for (int i = 0; i < 3; ++i) {
     const int64_t tn = (N + widths[i] - 1) / widths[i];
-    const int64_t r1 = ((M + BM - 1) / BM * tn + sms - 1) / sms;
-    const int64_t c1 = r1 * w_single[i];
-    if (best_cost < 0 || c1 < best_cost) {
-      best_cost = c1;
-      best = {widths[i], false};
-    }
-    if (M > BM && pair_clusters > 0) {  // a pair computes 256 rows: pointless for M <= 128
-      const int64_t r2 = ((M + 2 * BM - 1) / (2 * BM) * tn + pair_clusters - 1) / pair_clusters;
-      const int64_t c2 = r2 * w_pair[i];
-      if (c2 < best_cost) {
-        best_cost = c2;
-        best = {widths[i], true};
+    for (int pair = 0; pair < 2; ++pair) {
+      if (pair && (M <= BM || pair_clusters <= 0)) continue;  // a pair computes 256 rows
+      const int64_t tiles = pair ? (M + 2 * BM - 1) / (2 * BM) * tn : (M + BM - 1) / BM * tn;
+      const int64_t slots = pair ? pair_clusters : sms;
+      for (int sp = 1; sp <= (widths[i] == 192 ? 1 : max_splits) && sp <= kb; ++sp) {
+        if (sp > 1) {  // workspace: one 16 KB (8 KB at 128 wide) slice per warp, tile and split
+          const int64_t bytes = tiles * (pair ? 2 : 1) * 8 * sp * (widths[i] == 128 ? 8192 : 16384);
+          if (bytes > kSplitMaxBytes) break;
+        }
+        const int64_t rounds = (tiles * sp + slots - 1) / slots;
+        const int64_t cost = rounds * ((kb + sp - 1) / sp + (sp > 1 ? kSplitUnitKb : 0)) *
+                                 (pair ? w_pair[i] : w_single[i]) +
+                             (sp > 1 ? static_cast<int64_t>(sp) * kSplitCostNs : 0);
+        if (best_cost < 0 || cost < best_cost) {
+          best_cost = cost;
+          best = {widths[i], pair != 0, sp};
+        }
       }
     }
   }
   return best;
+}
+
+// Workspace of a split-K launch: arrival counters, then the fp32 partials.
+struct SplitLayout {
+  int64_t slices, counter_bytes, total_bytes;
+};
+
+SplitLayout split_layout(int64_t M, int64_t N, const TileChoice& c) {
+  SplitLayout l{0, 0, 0};
+  if (c.splits <= 1) return l;
+  const int64_t tn = (N + c.bn - 1) / c.bn;
+  const int64_t tiles = c.pair ? (M + 2 * BM - 1) / (2 * BM) * tn : (M + BM - 1) / BM * tn;
+  const int64_t slot_v = ((c.bn / 64 + 1) / 2) * 16;  // float4 per lane of one warp's slice
+  l.slices = tiles * (c.pair ? 2 : 1) * 8;
+  l.counter_bytes = kSplitCounterBytes;
+  l.total_bytes = l.counter_bytes + l.slices * c.splits * slot_v * 32 * 16;
+  return l;
 }
 
 template <bool BLOCK, int BN, int QF>
@@ -651,7 +762,8 @@ cudaError_t launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const C
   p.num_n = (p.N + BN - 1) / BN;
   p.num_tiles = p.num_m * p.num_n;
   p.idesc = idesc_f8(p.idesc & 7u, (p.idesc >> 3) & 7u, BM, BN);
-  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  const int units = p.num_tiles * p.splits;
+  const int grid = units < num_sms() ? units : num_sms();
   return launch_pdl(gemm_f8_kernel<BLOCK, BN, QF, false>, dim3(grid), dim3(Cfg<BLOCK, BN, QF, false>::THREADS),
                     Cfg<BLOCK, BN, QF, false>::SMEM, stream, ta, tb, tc, tq, p);
 }
@@ -669,7 +781,8 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   p.num_n = (p.N + BN - 1) / BN;
   p.num_tiles = p.num_m * p.num_n;
   p.idesc = idesc_f8(p.idesc & 7u, (p.idesc >> 3) & 7u, 2 * BM, BN);
-  const int ncl = p.num_tiles < clusters ? p.num_tiles : clusters;
+  const int units = p.num_tiles * p.splits;
+  const int ncl = units < clusters ? units : clusters;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * ncl);
   cfg.blockDim = dim3(C::THREADS);
@@ -727,18 +840,30 @@ bool encode_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  const TileChoice c = choose_tile(M, N, K, num_sms(), pair_capacity(), 2);
+  return split_layout(M, N, c).total_bytes;
+}
+
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why) {
   // block scaling folds every 128-deep K block out of TMEM: 128-wide single-CTA tiles keep
   // the fold's registers (64 fp32 per thread) and its four accumulator buffers within budget
-  TileChoice choice{128, false};
+  TileChoice choice{128, false, 1};
   if (!g.block_scaled) {
 #ifdef FP8GB_FORCE_BN  // compile-time override of the tile choice, for tuning builds
 #ifndef FP8GB_FORCE_PAIR
 #define FP8GB_FORCE_PAIR 0
 #endif
-    choice = {FP8GB_FORCE_BN, FP8GB_FORCE_PAIR != 0};
+    choice = {FP8GB_FORCE_BN, FP8GB_FORCE_PAIR != 0, 1};
 #else
-    choice = choose_tile(g.M, g.N, num_sms(), pair_capacity());
+    choice = choose_tile(g.M, g.N, g.K, num_sms(), pair_capacity(), g.qf < 0 && g.ws != nullptr ? 2 : 1);
+    // a workspace too small for the best split falls back to the best unsplit shape
+    if (choice.splits > 1) {
+      const SplitLayout l = split_layout(g.M, g.N, choice);
+      if (l.total_bytes > g.ws_bytes || l.slices * 4 > kSplitCounterBytes)
+        choice = choose_tile(g.M, g.N, g.K, num_sms(), pair_capacity(), 1);
+    }
 #endif
   }
   const int bn = choice.bn;
@@ -761,6 +886,15 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why
   p.sb = g.sb;
   p.sa_ld = static_cast<int>(g.K / 128);
   p.sb_ld = static_cast<int>(g.N / 128);
+  p.splits = 1;
+  p.ws = nullptr;
+  p.ws_cnt = nullptr;
+  if (choice.splits > 1) {
+    const SplitLayout l = split_layout(g.M, g.N, choice);
+    p.splits = choice.splits;
+    p.ws_cnt = static_cast<int*>(g.ws);
+    p.ws = reinterpret_cast<float4*>(static_cast<uint8_t*>(g.ws) + l.counter_bytes);
+  }
   p.w = wait_ctl();
   if (p.w.err == nullptr) {
     *why = "device error word unavailable";

@@ -95,8 +95,13 @@ struct GemmArgs {
   void* Cq = nullptr;
   int64_t ldcq = 0;
   QuantState cst{};
+  // optional workspace for split K (per-tensor scales, bf16 output only)
+  void* ws = nullptr;
+  int64_t ws_bytes = 0;
 };
 // Returns cudaSuccess, or an error; `why` receives a static message for host-side failures.
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why);
+// Workspace bytes a split-K launch of this per-tensor problem uses (0: it would not split).
+int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 }  // namespace fp8gb

@@ -140,6 +140,34 @@ fp8_status_t fp8_scaled_mm(const void* A, fp8_format_t fa, const void* B, fp8_fo
                            fp8_gran_t gran, const float* scale_inv_a, const float* scale_inv_b,
                            void* C_bf16, int64_t ldc, void* stream);
 
+/* fp8_scaled_mm with a caller-owned workspace that lets the library split the contraction:
+ * when the output has too few 256 x 256 tiles to occupy every SM (for example a weight
+ * gradient, [K_model, N] with a long token contraction), each tile is computed as two units
+ * over the two halves of its K range; each unit writes its fp32 partial product to the
+ * workspace and the tile's second unit to finish adds the other's to its own, scales and
+ * stores.
+ *  The pages have no such entry point: it restates "Explanation"'s scaled FP8 matmul
+ *  ([SPEED]) with the same result definition as fp8_scaled_mm. The two partial sums change
+ *  the fp32 summation order, so C can differ from fp8_scaled_mm's by fp32 rounding (always
+ *  within the same error bound); fp32 addition being commutative, it is the same for every
+ *  call with the same inputs.
+ *  gran must be FP8_GRAN_TENSOR (block scaling never splits). workspace: device, 16-byte
+ *  aligned, workspace_bytes long, owned by the caller and zero-filled before its first use;
+ *  its head holds arrival counters that every successful call leaves at zero, so later
+ *  calls of any shape need no clearing (after an error, zero-fill it again). A workspace
+ *  smaller than fp8_scaled_mm_workspace_bytes(M, N, K), or null, runs the unsplit GEMM.
+ *  Two calls must not use one workspace concurrently (different streams without ordering).
+ *  Other rules as fp8_scaled_mm. */
+fp8_status_t fp8_scaled_mm_ws(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb,
+                              int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                              fp8_gran_t gran, const float* scale_inv_a, const float* scale_inv_b,
+                              void* C_bf16, int64_t ldc, void* workspace, int64_t workspace_bytes,
+                              void* stream);
+
+/* Workspace bytes fp8_scaled_mm_ws uses for this per-tensor problem on the current device:
+ * 0 when it would not split (a null workspace then costs nothing). Negative on a CUDA error. */
+int64_t fp8_scaled_mm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
 /* fp8_scaled_mm (per-tensor scales) whose epilogue also emits the FP8 codes of its output for
  * a following FP8 consumer (for example dgrad's dx, cast to E5M2 for the previous layer's
  * backward), so the bf16 result is not read back by a separate cast.

@@ -1,0 +1,103 @@
+"""GPU parity of the split-K GEMM (fp8_scaled_mm_ws) against the oracle's exact products,
+with the same bound as fp8_scaled_mm: |C - C_ref| <= 1e-3 * sum_k |a b| d_a d_b + 1 bf16 ulp.
+Shapes are ones the library splits (few output tiles, long K): single-CTA and CTA-pair tiles,
+ragged M, N and K."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import fp8, gemm
+
+from gpu_util import dev_u8, f32_scalar, host_bf16_f64
+from test_gpu_gemm import FMT, assert_close, rand_codes
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g():
+    import fp8_mixed_precision_saturating_gb300 as m
+    return m
+
+
+def run_ws(g, A, fa, B, fb, da, db, ws, nbytes):
+    M, K = A.shape
+    N = B.shape[0]
+    lda = ldb = -(-K // 16) * 16
+    ldc = -(-N // 8) * 8
+    Ad = torch.zeros(M, lda, dtype=torch.uint8, device="cuda")
+    Ad[:, :K] = dev_u8(A)
+    Bd = torch.zeros(N, ldb, dtype=torch.uint8, device="cuda")
+    Bd[:, :K] = dev_u8(B)
+    C = torch.full((M, ldc), float("nan"), dtype=torch.bfloat16, device="cuda")
+    g.fp8_scaled_mm_ws(Ad, fa, Bd, fb, M, N, K, lda, ldb, g.FP8_GRAN_TENSOR, f32_scalar(da), f32_scalar(db), C, ldc,
+                       ws, nbytes)
+    torch.cuda.synchronize()
+    return host_bf16_f64(C)[:, :N]
+
+
+SPLIT_CASES = [
+    # M, N, K, fa, fb
+    (256, 512, 4096, 0, 0),    # single-CTA 128-wide tiles, 32 K blocks in two halves
+    (300, 520, 4000, 1, 0),    # ragged M, N and last K block
+    (1024, 768, 8192, 0, 1),   # CTA-pair 256-wide tiles
+    (768, 3072, 8192, 0, 1),   # the GPT-2-small weight gradient: pairs
+]
+
+
+@pytest.mark.parametrize("M,N,K,fa,fb", SPLIT_CASES)
+def test_split_k_against_exact(g, M, N, K, fa, fb):
+    nbytes = g.fp8_scaled_mm_workspace_bytes(M, N, K)
+    assert nbytes > 0, "the library should split this shape"
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    rng = np.random.default_rng(M + 3 * N + K)
+    A = rand_codes(rng, (M, K), FMT[fa], 30.0)
+    B = rand_codes(rng, (N, K), FMT[fb], 30.0)
+    da, db = np.float32(rng.uniform(0.001, 0.1)), np.float32(rng.uniform(0.001, 0.1))
+    got = run_ws(g, A, fa, B, fb, da, db, ws, nbytes)
+    ref, mag, _ = gemm.scaled_mm(A, FMT[fa], B, FMT[fb], da, db)
+    assert_close(got, ref, mag)
+    # the same inputs give the same bits, whichever of a tile's two units finishes last; the
+    # workspace is reusable without clearing
+    again = run_ws(g, A, fa, B, fb, da, db, ws, nbytes)
+    assert np.array_equal(got.view(np.uint64), again.view(np.uint64))
+    g.fp8_poll_device_error()
+
+
+def test_workspace_reused_across_shapes_and_small_workspace_falls_back(g):
+    rng = np.random.default_rng(11)
+    shapes = [(256, 512, 4096), (1024, 768, 8192), (256, 512, 4096)]
+    big = max(g.fp8_scaled_mm_workspace_bytes(*s) for s in shapes)
+    ws = torch.zeros(big, dtype=torch.uint8, device="cuda")
+    for M, N, K in shapes:
+        A = rand_codes(rng, (M, K), fp8.E4M3, 20.0)
+        B = rand_codes(rng, (N, K), fp8.E4M3, 20.0)
+        ref, mag, _ = gemm.scaled_mm(A, fp8.E4M3, B, fp8.E4M3, 0.01, 0.02)
+        assert_close(run_ws(g, A, 0, B, 0, 0.01, 0.02, ws, big), ref, mag)
+        # too small (and null) workspaces run the unsplit GEMM: still within the bound
+        assert_close(run_ws(g, A, 0, B, 0, 0.01, 0.02, ws, 256), ref, mag)
+        assert_close(run_ws(g, A, 0, B, 0, 0.01, 0.02, None, 0), ref, mag)
+
+
+def test_unsplit_shapes_need_no_workspace(g):
+    assert g.fp8_scaled_mm_workspace_bytes(8192, 3072, 768) == 0    # fills the GPU as it is
+    assert g.fp8_scaled_mm_workspace_bytes(16384, 14336, 4096) == 0
+    assert g.fp8_scaled_mm_workspace_bytes(0, 16, 16) == 0
+
+
+def test_ws_rejections(g):
+    one = f32_scalar(1.0)
+    A = torch.zeros(128, 256, dtype=torch.uint8, device="cuda")
+    C = torch.zeros(128, 128, dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(g.Fp8Error) as e:
+        g.fp8_scaled_mm_ws(A, 0, A, 0, 128, 128, 256, 256, 256, g.FP8_GRAN_BLOCK_128x128, one, one, C, 128, ws, 1024)
+    assert e.value.status == g.FP8_ERR_UNSUPPORTED
+    with pytest.raises(g.Fp8Error) as e:
+        g.fp8_scaled_mm_ws(A, 0, A, 0, 128, 128, 256, 256, 256, g.FP8_GRAN_TENSOR, one, one, C, 128,
+                           ws[8:].data_ptr(), 1000)
+    assert e.value.status == g.FP8_ERR_ALIGNMENT
+    with pytest.raises(g.Fp8Error) as e:
+        g.fp8_scaled_mm_ws(A, 0, A, 0, 128, 128, 256, 256, 256, g.FP8_GRAN_TENSOR, one, one, C, 128, ws, -1)
+    assert e.value.status == g.FP8_ERR_INVALID_ARG
+    g.fp8_poll_device_error()
