@@ -537,7 +537,62 @@ def run_sweep(args):
             out.update(ms_cast_only=round(ms_c, 5), cast_only_GB_s=round(by / (ms_c * 1e-3) / 1e9, 1))
         print(json.dumps(out))
         del x, q, qT
+    if only is None or "delayed_loop" in only:
+        run_delayed_loop(g, torch, fp8_peak)
     g.fp8_poll_device_error()
+
+
+def run_delayed_loop(g, torch, fp8_peak, layers=12, steps=50, tokens=32768, d=1536, hist=16):
+    """The delayed-scaling training loop at full size through the public API: every step and
+    layer refreshes W with its optimizer step and re-quantises it (one fused pass), casts x
+    and dy with the delayed scales, runs the forward, dgrad and wgrad GEMMs and commits the
+    three amaxes. x, dy and the per-layer steps are drawn once (synthetic, seeded); the timed
+    region is the whole trajectory after one untimed step."""
+    n = 4 * d
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    x = (torch.randn(tokens, d, generator=gen, device="cuda")).to(torch.bfloat16)
+    dy = (torch.randn(tokens, n, generator=gen, device="cuda") * 1e-3).to(torch.bfloat16)
+    u8 = lambda *sh: torch.empty(*sh, dtype=torch.uint8, device="cuda")
+    bf = lambda *sh: torch.empty(*sh, dtype=torch.bfloat16, device="cuda")
+    W = [(torch.randn(d, n, generator=gen, device="cuda") * 0.02).to(torch.bfloat16) for _ in range(layers)]
+    delta = [torch.randn(d, n, generator=gen, device="cuda") * 1e-3 for _ in range(layers)]
+    st = [[g.TensorState(hist) for _ in range(3)] for _ in range(layers)]
+    wq, wqT = [u8(d, n) for _ in range(layers)], [u8(n, d) for _ in range(layers)]
+    xq, xqT, dyq, dyqT = u8(tokens, d), u8(d, tokens), u8(tokens, n), u8(n, tokens)
+    y, dx, dw = bf(tokens, n), bf(tokens, d), bf(d, n)
+    wsb = max(g.fp8_scaled_mm_workspace_bytes(*sh) for sh in ((tokens, n, d), (tokens, d, n), (d, n, tokens)))
+    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    D, T = g.FP8_SCALE_DELAYED, g.FP8_GRAN_TENSOR
+
+    def layer_step(l):
+        ws_, xs, gs = st[l]
+        g.fp8_update_requantize_weights(W[l], delta[l], d, n, D, ws_, wq[l], wqT[l])
+        g.fp8_quantize(x, tokens, d, d, g.FP8_E4M3, T, D, xs, xq, xqT)
+        g.fp8_scaled_mm_ws(xq, 0, wqT[l], 0, tokens, n, d, d, d, T, xs.scale_inv, ws_.scale_inv, y, n, ws, wsb)
+        g.fp8_quantize(dy, tokens, n, n, g.FP8_E5M2, T, D, gs, dyq, dyqT)
+        g.fp8_scaled_mm_ws(dyq, 1, wq[l], 0, tokens, d, n, n, n, T, gs.scale_inv, ws_.scale_inv, dx, d, ws, wsb)
+        g.fp8_scaled_mm_ws(xqT, 0, dyqT, 1, d, n, tokens, tokens, tokens, T, xs.scale_inv, gs.scale_inv, dw, n,
+                           ws, wsb)
+        g.fp8_history_commit_many([ws_, xs, gs])
+
+    for l in range(layers):  # untimed first step (bootstrap casts)
+        layer_step(l)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps - 1):
+        for l in range(layers):
+            layer_step(l)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    flops = 3 * 2.0 * tokens * d * n * layers * (steps - 1)
+    tf = flops / (ms * 1e-3) / 1e12
+    ov = sum(int(s.counters[0]) for lay in st for s in lay)
+    print(json.dumps({"sweep": "delayed_loop", "layers": layers, "steps_timed": steps - 1, "tokens": tokens, "d": d,
+                      "ms_total": round(ms, 3), "ms_per_layer_step": round(ms / (layers * (steps - 1)), 4),
+                      "TFLOP/s": round(tf, 1), "frac_fp8_peak": round(tf / fp8_peak, 4),
+                      "launches_per_layer_step": 7, "overflow_counts_total": ov}))
 
 
 # --------------------------------------------------------------------------------------
