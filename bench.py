@@ -375,7 +375,7 @@ def run_block_scaled(g, torch, x, wm, stream, flush, steps):
 def run_e2e(g, torch, x_h, w_h, dy_h, stream, steps, step_flops):
     """The same step through the public API (requantise + linear forward + linear backward
     + commits) with host inputs: pinned host -> device copies of x, W and dy and device ->
-    host copies of y, dx and dW inside the timed region."""
+    host copies of y, dx and dW inside the timed region, overlapped with the compute."""
     import numpy as np
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
     xh, wh, dyh = pin(x_h), pin(w_h), pin(dy_h)
@@ -388,17 +388,36 @@ def run_e2e(g, torch, x_h, w_h, dy_h, stream, steps, step_flops):
     wst, xst, gst = g.TensorState(HIST), g.TensorState(HIST), g.TensorState(HIST)
     D, T = g.FP8_SCALE_DELAYED, g.FP8_GRAN_TENSOR
 
+    # copies overlap the compute on two copy streams: x and W go up first, dy goes up while
+    # the forward runs, y comes down while the backward runs, dx and dW after it; a step's
+    # uploads may overlap the previous step's downloads (different buffers)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_xw, ev_dy, ev_fwd, ev_bwd = (torch.cuda.Event() for _ in range(4))
+
     def one():
-        x.copy_(xh, non_blocking=True)
-        wm.copy_(wh, non_blocking=True)
-        dy.copy_(dyh, non_blocking=True)
+        s_in.wait_stream(stream)  # the previous step's kernels have read x, W and dy
+        with torch.cuda.stream(s_in):
+            x.copy_(xh, non_blocking=True)
+            wm.copy_(wh, non_blocking=True)
+            ev_xw.record(s_in)
+            dy.copy_(dyh, non_blocking=True)
+            ev_dy.record(s_in)
+        stream.wait_stream(s_out)  # the previous step's outputs are on the host
+        stream.wait_event(ev_xw)
         g.fp8_requantize_weights(wm, K, N, T, D, wst, wq, wqT)
         g.fp8_linear_fwd(x, M, K, N, wqT, wst, None, xst, T, D, xq, xqT, None, y)
+        ev_fwd.record(stream)
+        s_out.wait_event(ev_fwd)
+        with torch.cuda.stream(s_out):
+            yh.copy_(y, non_blocking=True)
+        stream.wait_event(ev_dy)
         g.fp8_linear_bwd(dy, M, K, N, xqT, xst, wq, wst, gst, D, dyq, dyqT, dx, dw)
         g.fp8_history_commit_many([wst, xst, gst])
-        yh.copy_(y, non_blocking=True)
-        dxh.copy_(dx, non_blocking=True)
-        dwh.copy_(dw, non_blocking=True)
+        ev_bwd.record(stream)
+        s_out.wait_event(ev_bwd)
+        with torch.cuda.stream(s_out):
+            dxh.copy_(dx, non_blocking=True)
+            dwh.copy_(dw, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -408,6 +427,7 @@ def run_e2e(g, torch, x_h, w_h, dy_h, stream, steps, step_flops):
         e0.record(stream)
         for _ in range(steps):
             one()
+        stream.wait_stream(s_out)  # the last step's results are on the host
         e1.record(stream)
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
