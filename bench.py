@@ -187,11 +187,13 @@ def run_gpu(args):
     T = g.FP8_GRAN_TENSOR
     gemm_flops = 2.0 * M * N * K
 
-    # one split-K workspace for the three GEMMs (they run in order on one stream); the
-    # library splits only shapes with too few output tiles (here the weight gradient)
-    ws_bytes = max(g.fp8_scaled_mm_workspace_bytes(*s) for s in ((M, N, K), (M, K, N), (K, N, M)))
+    # the backward's two GEMMs run as one grouped launch (wgrad split over its tokens through
+    # the workspace, dgrad beside it); the forward GEMM gets the same workspace (unused: its
+    # 384 tiles fill the GPU)
+    bwd = [g.mm_problem(xqT, 0, dyqT, 1, K, N, M, M, M, xst.scale_inv, gst.scale_inv, dw, N),
+           g.mm_problem(dyq, 1, wq, 0, M, K, N, N, N, gst.scale_inv, wst.scale_inv, dx, K)]
+    ws_bytes = max(g.fp8_scaled_mm_grouped_workspace_bytes(bwd), g.fp8_scaled_mm_workspace_bytes(M, N, K))
     ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
-    ws2 = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")  # wgrad runs beside dgrad
     # (name, call, kernels launched, algorithmic flops, algorithmic bytes)
     stages = [
         ("requant_w", lambda: g.fp8_requantize_weights(wm, K, N, T, D, wst, wq, wqT), 1, 0.0, K * N * 4.0),
@@ -199,10 +201,7 @@ def run_gpu(args):
         ("gemm_fwd", lambda: g.fp8_scaled_mm_ws(xq, 0, wqT, 0, M, N, K, K, K, T, xst.scale_inv, wst.scale_inv, y, N,
                                                 ws, ws_bytes), 1, gemm_flops, 0.0),
         ("quant_dy", lambda: g.fp8_quantize(dy, M, N, N, g.FP8_E5M2, T, D, gst, dyq, dyqT), 1, 0.0, M * N * 4.0),
-        ("gemm_dgrad", lambda: g.fp8_scaled_mm_ws(dyq, 1, wq, 0, M, K, N, N, N, T, gst.scale_inv, wst.scale_inv, dx, K,
-                                                  ws, ws_bytes), 1, gemm_flops, 0.0),
-        ("gemm_wgrad", lambda: g.fp8_scaled_mm_ws(xqT, 0, dyqT, 1, K, N, M, M, M, T, xst.scale_inv, gst.scale_inv, dw,
-                                                  N, ws2, ws_bytes), 1, gemm_flops, 0.0),
+        ("gemm_bwd", lambda: g.fp8_scaled_mm_grouped(bwd, ws, ws_bytes), 1, 2 * gemm_flops, 0.0),
         ("commit", lambda: g.fp8_history_commit_many([wst, xst, gst]), 1, 0.0, 0.0),
     ]
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -216,8 +215,8 @@ def run_gpu(args):
         # launched eagerly in the same loop, each behind an L2 flush: the GPU is still busy
         # with the flush while the host enqueues the stage, so the events bracket only the
         # kernel (cold L2, no event nodes inside a graph).
-        # the step's dependency graph on two streams: W's refresh beside x's cast, then the
-        # forward GEMM; dy's cast; dgrad beside wgrad; the history commit after both
+        # the step's dependency graph: W's refresh beside x's cast (two streams), then the
+        # forward GEMM, dy's cast, the grouped backward GEMMs and the history commit
         side = torch.cuda.Stream()
         fn = {name: f for name, f, *_ in stages}
         plain = torch.cuda.CUDAGraph()
@@ -229,11 +228,7 @@ def run_gpu(args):
             stream.wait_stream(side)
             fn["gemm_fwd"]()
             fn["quant_dy"]()
-            side.wait_stream(stream)
-            with torch.cuda.stream(side):
-                fn["gemm_wgrad"]()
-            fn["gemm_dgrad"]()
-            stream.wait_stream(side)
+            fn["gemm_bwd"]()
             fn["commit"]()
         for st in (wst, xst, gst):
             st.reset()  # the delayed-scaling state starts empty (bootstrap step first)
@@ -313,7 +308,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/e5m2 x fp32-accumulate -> bf16", "data": "synthetic",
         "config": {"workload": "gpt2s_upproj_train_step", "M_tokens": M, "d_model": K, "d_ff": N,
-                   "step": "(requantise W || quantise x), fwd GEMM, quantise dy, (dgrad || wgrad), 3 history commits; one CUDA graph on two streams",
+                   "step": "(requantise W || quantise x), fwd GEMM, quantise dy, dgrad + wgrad in one grouped launch, 3 history commits; one CUDA graph",
                    "scaling": "per-tensor delayed, amax history 16", "global_batch_tokens": M * world,
                    "l2": "256 MiB buffer written between timed steps (flush)", "parallelism": f"dp{world} (independent batches)"},
         "roofline": roof,
@@ -387,6 +382,8 @@ def run_e2e(g, torch, x_h, w_h, dy_h, stream, steps, step_flops):
     wq, wqT, xq, xqT, dyq, dyqT = u8(K, N), u8(N, K), u8(M, K), u8(K, M), u8(M, N), u8(N, M)
     wst, xst, gst = g.TensorState(HIST), g.TensorState(HIST), g.TensorState(HIST)
     D, T = g.FP8_SCALE_DELAYED, g.FP8_GRAN_TENSOR
+    wsb = g.fp8_linear_bwd_workspace_bytes(M, K, N)
+    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
 
     # copies overlap the compute on two copy streams: x and W go up first, dy goes up while
     # the forward runs, y comes down while the backward runs, dx and dW after it; a step's
@@ -411,7 +408,7 @@ def run_e2e(g, torch, x_h, w_h, dy_h, stream, steps, step_flops):
         with torch.cuda.stream(s_out):
             yh.copy_(y, non_blocking=True)
         stream.wait_event(ev_dy)
-        g.fp8_linear_bwd(dy, M, K, N, xqT, xst, wq, wst, gst, D, dyq, dyqT, dx, dw)
+        g.fp8_linear_bwd_ws(dy, M, K, N, xqT, xst, wq, wst, gst, D, dyq, dyqT, dx, dw, ws, wsb)
         g.fp8_history_commit_many([wst, xst, gst])
         ev_bwd.record(stream)
         s_out.wait_event(ev_bwd)

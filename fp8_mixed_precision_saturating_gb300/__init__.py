@@ -41,21 +41,42 @@ class fp8_tensor_state_t(ctypes.Structure):
     ]
 
 
+class fp8_mm_problem_t(ctypes.Structure):
+    _fields_ = [
+        ("A", ctypes.c_void_p),
+        ("fa", ctypes.c_int),
+        ("B", ctypes.c_void_p),
+        ("fb", ctypes.c_int),
+        ("M", ctypes.c_int64),
+        ("N", ctypes.c_int64),
+        ("K", ctypes.c_int64),
+        ("lda", ctypes.c_int64),
+        ("ldb", ctypes.c_int64),
+        ("scale_inv_a", ctypes.c_void_p),
+        ("scale_inv_b", ctypes.c_void_p),
+        ("C_bf16", ctypes.c_void_p),
+        ("ldc", ctypes.c_int64),
+    ]
+
+
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _I = ctypes.c_int
 _SP = ctypes.POINTER(fp8_tensor_state_t)
+_MP = ctypes.POINTER(fp8_mm_problem_t)
 
 _SIGS = {
     "fp8_quantize": [_P, _I64, _I64, _I64, _I, _I, _I, _SP, _P, _P, _P, _P],
     "fp8_scaled_mm": [_P, _I, _P, _I, _I64, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _P],
     "fp8_scaled_mm_ws": [_P, _I, _P, _I, _I64, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _P, _I64, _P],
+    "fp8_scaled_mm_grouped": [_MP, ctypes.c_int32, _P, _I64, _P],
     "fp8_scaled_mm_quant": [_P, _I, _P, _I, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _I64, _I, _SP, _P, _P],
     "fp8_requantize_weights": [_P, _I64, _I64, _I, _I, _SP, _P, _P, _P, _P],
     "fp8_update_requantize_weights": [_P, _P, _I64, _I64, _I, _SP, _P, _P, _P],
     "fp8_linear_fwd": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _I, _I, _P, _P, _P, _P, _P],
     "fp8_linear_bwd": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _SP, _I, _P, _P, _P, _P, _P],
     "fp8_linear_bwd_noalloc": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _SP, _I, _P, _P, _P],
+    "fp8_linear_bwd_ws": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _SP, _I, _P, _P, _P, _P, _P, _I64, _P],
     "fp8_history_commit": [_SP, _P],
     "fp8_history_commit_many": [_SP, ctypes.c_int32, _P],
     "fp8_poll_device_error": [],
@@ -67,6 +88,10 @@ for _name, _args in _SIGS.items():
     _f = getattr(lib, _name)
     _f.argtypes = _args
     _f.restype = ctypes.c_int
+lib.fp8_scaled_mm_grouped_workspace_bytes.argtypes = [_MP, ctypes.c_int32]
+lib.fp8_scaled_mm_grouped_workspace_bytes.restype = ctypes.c_int64
+lib.fp8_linear_bwd_workspace_bytes.argtypes = [_I64, _I64, _I64]
+lib.fp8_linear_bwd_workspace_bytes.restype = ctypes.c_int64
 lib.fp8_scaled_mm_workspace_bytes.argtypes = [_I64, _I64, _I64]
 lib.fp8_scaled_mm_workspace_bytes.restype = ctypes.c_int64
 lib.fp8_status_string.argtypes = [ctypes.c_int]
@@ -181,6 +206,25 @@ def fp8_scaled_mm_ws(A, fa, B, fb, M, N, K, lda, ldb, gran, scale_inv_a, scale_i
                                        _stream(stream)))
 
 
+def mm_problem(A, fa, B, fb, M, N, K, lda, ldb, scale_inv_a, scale_inv_b, C, ldc):
+    """One fp8_mm_problem_t (per-tensor scales) for fp8_scaled_mm_grouped."""
+    return fp8_mm_problem_t(_ptr(A), fa, _ptr(B), fb, M, N, K, lda, ldb, _ptr(scale_inv_a), _ptr(scale_inv_b),
+                            _ptr(C), ldc)
+
+
+def fp8_scaled_mm_grouped(problems, workspace=None, workspace_bytes=0, stream=None):
+    arr = (fp8_mm_problem_t * len(problems))(*problems)
+    return _check(lib.fp8_scaled_mm_grouped(arr, len(problems), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def fp8_scaled_mm_grouped_workspace_bytes(problems) -> int:
+    arr = (fp8_mm_problem_t * len(problems))(*problems)
+    n = lib.fp8_scaled_mm_grouped_workspace_bytes(arr, len(problems))
+    if n < 0:
+        raise Fp8Error(FP8_ERR_INVALID_ARG, fp8_get_last_error_detail())
+    return n
+
+
 def fp8_scaled_mm_workspace_bytes(M, N, K) -> int:
     n = lib.fp8_scaled_mm_workspace_bytes(M, N, K)
     if n < 0:
@@ -215,6 +259,20 @@ def fp8_linear_bwd(dy, M, K, N, xqT_save, x_st, wq_kn, w_st, dy_st, mode, dyq_ws
     return _check(lib.fp8_linear_bwd(_ptr(dy), M, K, N, _ptr(xqT_save), _state(x_st), _ptr(wq_kn), _state(w_st),
                                      _state(dy_st), mode, _ptr(dyq_ws), _ptr(dyqT_ws), _ptr(dx), _ptr(dw),
                                      _stream(stream)))
+
+
+def fp8_linear_bwd_ws(dy, M, K, N, xqT_save, x_st, wq_kn, w_st, dy_st, mode, dyq_ws, dyqT_ws, dx, dw, workspace,
+                      workspace_bytes, stream=None):
+    return _check(lib.fp8_linear_bwd_ws(_ptr(dy), M, K, N, _ptr(xqT_save), _state(x_st), _ptr(wq_kn), _state(w_st),
+                                        _state(dy_st), mode, _ptr(dyq_ws), _ptr(dyqT_ws), _ptr(dx), _ptr(dw),
+                                        _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def fp8_linear_bwd_workspace_bytes(M, K, N) -> int:
+    n = lib.fp8_linear_bwd_workspace_bytes(M, K, N)
+    if n < 0:
+        raise Fp8Error(FP8_ERR_CUDA, "fp8_linear_bwd_workspace_bytes")
+    return n
 
 
 def fp8_linear_bwd_noalloc(dy, M, K, N, xqT_save, x_st, wq_kn, w_st, dy_st, mode, dx, dw, stream=None):

@@ -349,12 +349,53 @@ fp8_status_t fp8_linear_fwd(const void* x_bf16, int64_t M, int64_t K, int64_t N,
   return fail(FP8_ERR_INVALID_ARG, "%s: granularity must be TENSOR or BLOCK_128x128", who);
 }
 
-fp8_status_t fp8_linear_bwd(const void* dy_bf16, int64_t M, int64_t K, int64_t N, const void* xqT_save,
-                            const fp8_tensor_state_t* x_st, const void* wq_kn, const fp8_tensor_state_t* w_st,
-                            fp8_tensor_state_t* dy_st, fp8_scaling_t mode, void* dyq_ws, void* dyqT_ws, void* dx_bf16,
-                            void* dw_bf16, void* stream) {
-  const char* who = "fp8_linear_bwd";
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+}  // extern "C"
+
+namespace {
+
+// Checks of fp8_scaled_mm for one problem of a grouped call (per-tensor scales, M, N, K > 0).
+fp8_status_t check_group_problem(const fp8_mm_problem_t& q, int i, const char* who) {
+  if ((q.fa != FP8_E4M3 && q.fa != FP8_E5M2) || (q.fb != FP8_E4M3 && q.fb != FP8_E5M2))
+    return fail(FP8_ERR_INVALID_ARG, "%s: problem %d: unknown format", who, i);
+  if (q.M <= 0 || q.N <= 0 || q.K <= 0) return fail(FP8_ERR_INVALID_ARG, "%s: problem %d: M, N, K must be positive", who, i);
+  if (q.M >= (1ll << 31) || q.N >= (1ll << 31) || q.K >= (1ll << 31))
+    return fail(FP8_ERR_UNSUPPORTED, "%s: problem %d: size >= 2^31", who, i);
+  if (q.A == nullptr || q.B == nullptr || q.C_bf16 == nullptr || q.scale_inv_a == nullptr || q.scale_inv_b == nullptr)
+    return fail(FP8_ERR_INVALID_ARG, "%s: problem %d: null A, B, C or scale", who, i);
+  if (q.lda < q.K || q.ldb < q.K || q.ldc < q.N) return fail(FP8_ERR_INVALID_ARG, "%s: problem %d: lda, ldb < K or ldc < N", who, i);
+  if (!aligned16(q.A) || !aligned16(q.B) || !aligned16(q.C_bf16) || q.lda % 16 || q.ldb % 16 || q.ldc % 8)
+    return fail(FP8_ERR_ALIGNMENT, "%s: problem %d: A, B, C 16-byte aligned, lda and ldb multiples of 16, ldc of 8",
+                who, i);
+  return FP8_OK;
+}
+
+GemmArgs group_args(const fp8_mm_problem_t& q) {
+  return GemmArgs{q.A, q.B, q.C_bf16, q.M, q.N, q.K, q.lda, q.ldb, q.ldc, (int)q.fa, (int)q.fb,
+                  q.scale_inv_a, q.scale_inv_b, false};
+}
+
+fp8_status_t grouped_impl(const fp8_mm_problem_t* pr, int32_t n, void* ws, int64_t ws_bytes, cudaStream_t s,
+                          const char* who) {
+  if (n < 1 || n > 2 || pr == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: 1 or 2 problems", who);
+  if (ws_bytes < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative workspace size", who);
+  if (ws != nullptr && !aligned16(ws)) return fail(FP8_ERR_ALIGNMENT, "%s: workspace must be 16-byte aligned", who);
+  for (int i = 0; i < n; ++i) {
+    const fp8_status_t st = check_group_problem(pr[i], i, who);
+    if (st != FP8_OK) return st;
+  }
+  if (n == 1)
+    return scaled_mm_impl(pr[0].A, pr[0].fa, pr[0].B, pr[0].fb, pr[0].M, pr[0].N, pr[0].K, pr[0].lda, pr[0].ldb,
+                          FP8_GRAN_TENSOR, pr[0].scale_inv_a, pr[0].scale_inv_b, pr[0].C_bf16, pr[0].ldc, s, ws,
+                          ws_bytes, who);
+  const char* why = "launch";
+  const cudaError_t e = launch_gemm_group(group_args(pr[0]), group_args(pr[1]), ws, ws_bytes, s, &why);
+  return e == cudaSuccess ? FP8_OK : cuda_fail(e, why);
+}
+
+fp8_status_t linear_bwd_impl(const void* dy_bf16, int64_t M, int64_t K, int64_t N, const void* xqT_save,
+                             const fp8_tensor_state_t* x_st, const void* wq_kn, const fp8_tensor_state_t* w_st,
+                             fp8_tensor_state_t* dy_st, fp8_scaling_t mode, void* dyq_ws, void* dyqT_ws, void* dx_bf16,
+                             void* dw_bf16, void* ws, int64_t ws_bytes, cudaStream_t s, const char* who) {
   if (M < 0 || K < 0 || N < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
   if (M % 16 || K % 16 || N % 16) return fail(FP8_ERR_UNSUPPORTED, "%s: M, K and N must be multiples of 16", who);
   if (dyq_ws == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: dyq_ws is required", who);
@@ -362,20 +403,92 @@ fp8_status_t fp8_linear_bwd(const void* dy_bf16, int64_t M, int64_t K, int64_t N
     return fail(FP8_ERR_INVALID_ARG, "%s: wgrad needs dyqT_ws, xqT_save and x_st", who);
   if (dx_bf16 != nullptr && (wq_kn == nullptr || w_st == nullptr || !w_st->scale_inv))
     return fail(FP8_ERR_INVALID_ARG, "%s: dgrad needs wq_kn and w_st", who);
+  if (ws_bytes < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative workspace size", who);
+  if (ws != nullptr && !aligned16(ws)) return fail(FP8_ERR_ALIGNMENT, "%s: workspace must be 16-byte aligned", who);
   fp8_status_t st = quantize_impl(dy_bf16, M, N, N, FP8_E5M2, FP8_GRAN_TENSOR, mode, dy_st, dyq_ws,
                                   dw_bf16 != nullptr ? dyqT_ws : nullptr, nullptr, s);
   if (st != FP8_OK) return st;
-  if (dx_bf16 != nullptr) {
-    st = scaled_mm_impl(dyq_ws, FP8_E5M2, wq_kn, FP8_E4M3, M, K, N, N, N, FP8_GRAN_TENSOR, dy_st->scale_inv,
-                        w_st->scale_inv, dx_bf16, K, s);
-    if (st != FP8_OK) return st;
+  if (M == 0 || K == 0 || N == 0) {
+    // an empty contraction writes zeros; empty outputs write nothing
+    if (dx_bf16 != nullptr && (st = scaled_mm_impl(dyq_ws, FP8_E5M2, wq_kn, FP8_E4M3, M, K, N, N, N, FP8_GRAN_TENSOR,
+                                                   dy_st->scale_inv, w_st->scale_inv, dx_bf16, K, s)) != FP8_OK)
+      return st;
+    if (dw_bf16 != nullptr)
+      return scaled_mm_impl(xqT_save, FP8_E4M3, dyqT_ws, FP8_E5M2, K, N, M, M, M, FP8_GRAN_TENSOR, x_st->scale_inv,
+                            dy_st->scale_inv, dw_bf16, N, s);
+    return FP8_OK;
   }
-  if (dw_bf16 != nullptr) {
-    st = scaled_mm_impl(xqT_save, FP8_E4M3, dyqT_ws, FP8_E5M2, K, N, M, M, M, FP8_GRAN_TENSOR, x_st->scale_inv,
-                        dy_st->scale_inv, dw_bf16, N, s);
-    if (st != FP8_OK) return st;
+  if (dx_bf16 != nullptr && dw_bf16 != nullptr) {
+    // dgrad and wgrad in one persistent launch: neither alone fills the GPU at training
+    // shapes, and the pair share the dy codes. The checks fp8_scaled_mm would make:
+    if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31))
+      return fail(FP8_ERR_UNSUPPORTED, "%s: size >= 2^31", who);
+    if (!aligned16(dyq_ws) || !aligned16(dyqT_ws) || !aligned16(xqT_save) || !aligned16(wq_kn) || !aligned16(dx_bf16) ||
+        !aligned16(dw_bf16))
+      return fail(FP8_ERR_ALIGNMENT, "%s: codes and outputs must be 16-byte aligned", who);
+    const fp8_mm_problem_t pr[2] = {
+        {xqT_save, FP8_E4M3, dyqT_ws, FP8_E5M2, K, N, M, M, M, x_st->scale_inv, dy_st->scale_inv, dw_bf16, N},
+        {dyq_ws, FP8_E5M2, wq_kn, FP8_E4M3, M, K, N, N, N, dy_st->scale_inv, w_st->scale_inv, dx_bf16, K}};
+    return grouped_impl(pr, 2, ws, ws_bytes, s, who);
   }
+  if (dx_bf16 != nullptr)
+    return scaled_mm_impl(dyq_ws, FP8_E5M2, wq_kn, FP8_E4M3, M, K, N, N, N, FP8_GRAN_TENSOR, dy_st->scale_inv,
+                          w_st->scale_inv, dx_bf16, K, s, ws, ws_bytes, who);
+  if (dw_bf16 != nullptr)
+    return scaled_mm_impl(xqT_save, FP8_E4M3, dyqT_ws, FP8_E5M2, K, N, M, M, M, FP8_GRAN_TENSOR, x_st->scale_inv,
+                          dy_st->scale_inv, dw_bf16, N, s, ws, ws_bytes, who);
   return FP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8_status_t fp8_linear_bwd(const void* dy_bf16, int64_t M, int64_t K, int64_t N, const void* xqT_save,
+                            const fp8_tensor_state_t* x_st, const void* wq_kn, const fp8_tensor_state_t* w_st,
+                            fp8_tensor_state_t* dy_st, fp8_scaling_t mode, void* dyq_ws, void* dyqT_ws, void* dx_bf16,
+                            void* dw_bf16, void* stream) {
+  return linear_bwd_impl(dy_bf16, M, K, N, xqT_save, x_st, wq_kn, w_st, dy_st, mode, dyq_ws, dyqT_ws, dx_bf16, dw_bf16,
+                         nullptr, 0, static_cast<cudaStream_t>(stream), "fp8_linear_bwd");
+}
+
+fp8_status_t fp8_linear_bwd_ws(const void* dy_bf16, int64_t M, int64_t K, int64_t N, const void* xqT_save,
+                               const fp8_tensor_state_t* x_st, const void* wq_kn, const fp8_tensor_state_t* w_st,
+                               fp8_tensor_state_t* dy_st, fp8_scaling_t mode, void* dyq_ws, void* dyqT_ws,
+                               void* dx_bf16, void* dw_bf16, void* workspace, int64_t workspace_bytes, void* stream) {
+  return linear_bwd_impl(dy_bf16, M, K, N, xqT_save, x_st, wq_kn, w_st, dy_st, mode, dyq_ws, dyqT_ws, dx_bf16, dw_bf16,
+                         workspace, workspace_bytes, static_cast<cudaStream_t>(stream), "fp8_linear_bwd_ws");
+}
+
+int64_t fp8_linear_bwd_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+  if (current_device() < 0) {
+    fail(FP8_ERR_CUDA, "fp8_linear_bwd_workspace_bytes: no CUDA device");
+    return -1;
+  }
+  if (M <= 0 || K <= 0 || N <= 0) return 0;
+  // only the shapes decide the size
+  const GemmArgs gw{nullptr, nullptr, nullptr, K, N, M, M, M, N, (int)FP8_E4M3, (int)FP8_E5M2, nullptr, nullptr, false};
+  const GemmArgs gd{nullptr, nullptr, nullptr, M, K, N, N, N, K, (int)FP8_E5M2, (int)FP8_E4M3, nullptr, nullptr, false};
+  return gemm_group_workspace_bytes(gw, gd);
+}
+
+fp8_status_t fp8_scaled_mm_grouped(const fp8_mm_problem_t* problems, int32_t n, void* workspace,
+                                   int64_t workspace_bytes, void* stream) {
+  return grouped_impl(problems, n, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                      "fp8_scaled_mm_grouped");
+}
+
+int64_t fp8_scaled_mm_grouped_workspace_bytes(const fp8_mm_problem_t* problems, int32_t n) {
+  if (current_device() < 0) {
+    fail(FP8_ERR_CUDA, "fp8_scaled_mm_grouped_workspace_bytes: no CUDA device");
+    return -1;
+  }
+  if (n < 1 || n > 2 || problems == nullptr) {
+    fail(FP8_ERR_INVALID_ARG, "fp8_scaled_mm_grouped_workspace_bytes: 1 or 2 problems");
+    return -1;
+  }
+  if (n == 1) return gemm_workspace_bytes(problems[0].M, problems[0].N, problems[0].K);
+  return gemm_group_workspace_bytes(group_args(problems[0]), group_args(problems[1]));
 }
 
 }  // extern "C"

@@ -31,7 +31,11 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <algorithm>
+#include <array>
+#include <map>
 #include <mutex>
+#include <vector>
 
 #include "cast.cuh"
 #include "kernels.h"
@@ -92,39 +96,101 @@ struct Cfg {
   static_assert((A_BYTES % 1024) == 0 && (B_BYTES % 1024) == 0, "stage halves on 1024-byte swizzle atoms");
 };
 
-struct KParams {
+// One GEMM problem of a launch. A launch runs one problem, or two independent ones (the
+// backward pass's dgrad and wgrad) whose work units share the persistent grid.
+struct KProb {
   int M, N, K;
-  int num_m, num_n, num_kb, num_tiles;
+  int num_m, num_n, num_kb, num_tiles;  // num_m counts 256-row tiles on CTA pairs
   uint32_t idesc;
   const float* sa;
   const float* sb;
   int sa_ld, sb_ld;
-  WaitCtl w;
-  QuantState cst;  // scaling state of the FP8 output (QF >= 0)
   // split K: each output tile is `splits` (1 or 2) work units over the two halves of its
   // K blocks; the last unit of a tile to finish adds the other's fp32 partial (ws) to its own.
   // ws_cnt holds one arrival counter per (tile, CTA rank, epilogue warp), zero between calls.
   int splits;
   float4* ws;
   int* ws_cnt;
+  int unit0;  // first work unit of this problem in the launch
 };
 
-// Work unit u -> output tile and its K-block range [kb0, kb1).
-__device__ __forceinline__ void unit_range(int u, const KParams& p, int& tile, int& split, int& kb0, int& kb1) {
-  tile = u / p.splits;
-  split = u - tile * p.splits;
-  kb0 = split * p.num_kb / p.splits;
-  kb1 = (split + 1) * p.num_kb / p.splits;
+constexpr int kMaxSlots = 160;         // CTAs (or CTA pairs) of a persistent grid
+constexpr int kMaxSchedUnits = 1024;   // units of an explicit schedule
+
+struct KParams {
+  KProb pr[2];
+  int nprob;  // 1 or 2
+  int units;  // work units of all problems
+  WaitCtl w;
+  QuantState cst;  // scaling state of the FP8 output (QF >= 0, one problem)
+  // Units of CTA (pair) slot s: sched_unit[sched_off[s] .. sched_off[s + 1]) when sched_len
+  // > 0 (units of unequal length, placed longest first on the least-loaded slot); otherwise
+  // slot s takes units s, s + slots, s + 2 slots, ...
+  int sched_len;
+  uint16_t sched_off[kMaxSlots + 1];
+  uint16_t sched_unit[kMaxSchedUnits];
+};
+
+__device__ __forceinline__ int slot_units(const KParams& p, int slot, int slots) {
+  if (p.sched_len > 0) return p.sched_off[slot + 1] - p.sched_off[slot];
+  return slot < p.units ? (p.units - slot + slots - 1) / slots : 0;
 }
 
-__device__ __forceinline__ void tile_coords(int t, const KParams& p, int& mb, int& nb) {
-  const int per_group = GROUP_M * p.num_n;
+__device__ __forceinline__ int slot_unit(const KParams& p, int slot, int slots, int i) {
+  return p.sched_len > 0 ? p.sched_unit[p.sched_off[slot] + i] : slot + i * slots;
+}
+
+// Problem pi's fields, selected field by field (no dynamic indexing of kernel parameters).
+__device__ __forceinline__ KProb prob_of(const KParams& p, int pi) {
+  const KProb& a = p.pr[0];
+  const KProb& b = p.pr[1];
+  KProb q;
+  q.M = pi ? b.M : a.M;
+  q.N = pi ? b.N : a.N;
+  q.K = pi ? b.K : a.K;
+  q.num_m = pi ? b.num_m : a.num_m;
+  q.num_n = pi ? b.num_n : a.num_n;
+  q.num_kb = pi ? b.num_kb : a.num_kb;
+  q.num_tiles = pi ? b.num_tiles : a.num_tiles;
+  q.idesc = pi ? b.idesc : a.idesc;
+  q.sa = pi ? b.sa : a.sa;
+  q.sb = pi ? b.sb : a.sb;
+  q.sa_ld = pi ? b.sa_ld : a.sa_ld;
+  q.sb_ld = pi ? b.sb_ld : a.sb_ld;
+  q.splits = pi ? b.splits : a.splits;
+  q.ws = pi ? b.ws : a.ws;
+  q.ws_cnt = pi ? b.ws_cnt : a.ws_cnt;
+  q.unit0 = pi ? b.unit0 : a.unit0;
+  return q;
+}
+
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb, int& nb) {
+  const int per_group = GROUP_M * num_n;
   const int g = t / per_group;
   const int first_m = g * GROUP_M;
-  const int gsize = min(GROUP_M, p.num_m - first_m);
+  const int gsize = min(GROUP_M, num_m - first_m);
   const int local = t - g * per_group;
   mb = first_m + local % gsize;
   nb = local / gsize;
+}
+
+// Work unit u of the launch -> its problem, output tile (row and column block), split and
+// K-block range [kb0, kb1).
+struct Unit {
+  int pi, t, split, kb0, kb1, mb, nb;
+};
+
+__device__ __forceinline__ Unit unit_at(int u, const KParams& p, KProb& q) {
+  Unit r;
+  r.pi = (p.nprob > 1 && u >= p.pr[1].unit0) ? 1 : 0;
+  q = prob_of(p, r.pi);
+  const int v = u - q.unit0;
+  r.t = v / q.splits;
+  r.split = v - r.t * q.splits;
+  r.kb0 = r.split * q.num_kb / q.splits;
+  r.kb1 = (r.split + 1) * q.num_kb / q.splits;
+  tile_coords(r.t, q.num_m, q.num_n, r.mb, r.nb);
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -163,7 +229,8 @@ template <bool BLOCK, int BN, int QF, bool PAIR>
 __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
     gemm_f8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmQ,
-                   const KParams p) {
+                   const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                   const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ KParams p) {
   using C = Cfg<BLOCK, BN, QF, PAIR>;
   constexpr int STAGES = C::STAGES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
@@ -201,6 +268,11 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
+    if (p.nprob > 1) {
+      tma_prefetch_desc(&tmA1);
+      tma_prefetch_desc(&tmB1);
+      tma_prefetch_desc(&tmC1);
+    }
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -229,31 +301,34 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
       uint32_t issued_mask = 0, issued_phase = 0;  // per stage: issued?, parity of last issue
       bool ok = true;
       const uint32_t full_lead = PAIR ? mapa_shared(bar_full, 0) : bar_full;
-      for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step) {
-        int t, split, kb0, kb1, mb, nb;
-        unit_range(u, p, t, split, kb0, kb1);
-        tile_coords(t, p, mb, nb);
-        const int arow = mb * TILE_M + static_cast<int>(rank) * BM;
-        const int brow = nb * BN + static_cast<int>(rank) * C::B_ROWS;
-        for (int kb = kb0; kb < kb1; ++kb) {
+      const int nmine = slot_units(p, tile0, tile_step);
+      for (int i = 0; ok && i < nmine; ++i) {
+        const int u = slot_unit(p, tile0, tile_step, i);
+        KProb q;
+        const Unit un = unit_at(u, p, q);
+        const CUtensorMap* tA = un.pi ? &tmA1 : &tmA;
+        const CUtensorMap* tB = un.pi ? &tmB1 : &tmB;
+        const int arow = un.mb * TILE_M + static_cast<int>(rank) * BM;
+        const int brow = un.nb * BN + static_cast<int>(rank) * C::B_ROWS;
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.w, DEV_ERR_WAIT_PRODUCER)) {
             ok = false;
             break;
           }
           const uint32_t fb = bar_full + 8 * stage;
 #ifdef FP8GB_TRACE
-          if (t == (int)blockIdx.x && kb == 0) FP8GB_STAMP(7);
+          if (i == 0 && kb == un.kb0) FP8GB_STAMP(7);
 #endif
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           if constexpr (PAIR) {
             // both CTAs' bytes land on rank 0's barrier, which alone expects them
             if (rank == 0) mbar_arrive_expect_tx(fb, 2 * STAGE_BYTES);
-            tma_load_2d_pair(sa, &tmA, full_lead + 8 * stage, kb * BK, arow);
-            tma_load_2d_pair(sa + A_BYTES, &tmB, full_lead + 8 * stage, kb * BK, brow);
+            tma_load_2d_pair(sa, tA, full_lead + 8 * stage, kb * BK, arow);
+            tma_load_2d_pair(sa + A_BYTES, tB, full_lead + 8 * stage, kb * BK, brow);
           } else {
             mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            tma_load_2d(sa, &tmA, fb, kb * BK, arow);
-            tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, brow);
+            tma_load_2d(sa, tA, fb, kb * BK, arow);
+            tma_load_2d(sa + A_BYTES, tB, fb, kb * BK, brow);
           }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -284,9 +359,12 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step) {
-        int t, split, kb0, kb1;
-        unit_range(u, p, t, split, kb0, kb1);
+      const int nmine = slot_units(p, tile0, tile_step);
+      for (int i = 0; ok && i < nmine; ++i) {
+        const int u = slot_unit(p, tile0, tile_step, i);
+        KProb q;
+        const Unit un = unit_at(u, p, q);
+        const int kb0 = un.kb0, kb1 = un.kb1;
         if (!BLOCK) {
           if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.w, DEV_ERR_WAIT_MMA)) break;
           tc_fence_after();
@@ -305,7 +383,7 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
           }
           tc_fence_after();
 #ifdef FP8GB_TRACE
-          if (t == (int)blockIdx.x && kb == 0) FP8GB_STAMP(2);
+          if (i == 0 && kb == kb0) FP8GB_STAMP(2);
 #endif
           const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
           const uint32_t sa = sbase + stage * STAGE_BYTES;
@@ -315,9 +393,9 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
           for (int k = 0; k < BK / 32; ++k) {
             const uint32_t accumulate = BLOCK ? (k != 0) : (kb != kb0 || k != 0);
             if constexpr (PAIR)
-              mma_f8_pair(d, adesc + 2 * k, bdesc + 2 * k, p.idesc, accumulate);
+              mma_f8_pair(d, adesc + 2 * k, bdesc + 2 * k, q.idesc, accumulate);
             else
-              mma_f8(d, adesc + 2 * k, bdesc + 2 * k, p.idesc, accumulate);
+              mma_f8(d, adesc + 2 * k, bdesc + 2 * k, q.idesc, accumulate);
           }
           if constexpr (PAIR)
             mma_commit_pair(bar_empty + 8 * stage, 0x3);  // frees the stage in both CTAs
@@ -361,7 +439,8 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     if constexpr (!BLOCK) {
-      const float dd = __fmul_rn(__ldg(p.sa), __ldg(p.sb));
+      const float dd0 = __fmul_rn(__ldg(p.pr[0].sa), __ldg(p.pr[0].sb));
+      const float dd1 = p.nprob > 1 ? __fmul_rn(__ldg(p.pr[1].sa), __ldg(p.pr[1].sb)) : dd0;
       // FP8 output: with a non-empty history the epilogue casts the bf16 result with the
       // delayed scale (the empty-history call is cast afterwards from its own amax)
       bool fused = false;
@@ -384,12 +463,16 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
       const int hc = ew >> 2;
       constexpr int NCH = BN / 64;
       const uint32_t tempty_lead = PAIR ? mapa_shared(bar_tempty, 0) : bar_tempty;
-      for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step) {
-        int t, split, kb0, kb1, mb, nb;
-        unit_range(u, p, t, split, kb0, kb1);
-        tile_coords(t, p, mb, nb);
+      const int nmine = slot_units(p, tile0, tile_step);
+      for (int i = 0; ok && i < nmine; ++i) {
+        const int u = slot_unit(p, tile0, tile_step, i);
+        KProb pq;
+        const Unit un = unit_at(u, p, pq);
+        const int t = un.t, split = un.split, mb = un.mb, nb = un.nb;
+        const float dd = un.pi ? dd1 : dd0;
+        const CUtensorMap* tC = un.pi ? &tmC1 : &tmC;
         const int row0 = mb * TILE_M + static_cast<int>(rank) * BM + q * 32;  // this warp's 32 rows
-        const bool rows_live = row0 < p.M;
+        const bool rows_live = row0 < pq.M;
         if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE)) break;
         __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the spin
         tc_fence_after();
@@ -451,19 +534,19 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && rows_live) {
-            tma_store_2d(&tmC, smem_u32(stg), nb * BN + col, row0);
+            tma_store_2d(tC, smem_u32(stg), nb * BN + col, row0);
             if (fused) tma_store_2d(&tmQ, smem_u32(qstg), nb * BN + col, row0);
             bulk_commit_group();
           }
         };
         bool last = true;  // this unit stores the tile
         if constexpr (QF < 0 && BN != 192) {  // split K: 256- and 128-wide bf16-output tiles
-          if (p.splits > 1) {
+          if (pq.splits > 1) {
             // this warp's slice of the partial tile: 32 lanes x (64 or 128) fp32, stored so that
             // each float4 index is 512 contiguous bytes across the warp
             constexpr int SLOT_V = ((NCH + 1) / 2) * 16;  // float4 per lane
             const int slice = (t * (PAIR ? 2 : 1) + static_cast<int>(rank)) * C::EPI_WARPS + ew;
-            float4* slot0 = p.ws + static_cast<size_t>(slice) * p.splits * SLOT_V * 32;
+            float4* slot0 = pq.ws + static_cast<size_t>(slice) * pq.splits * SLOT_V * 32;
             float4* mine = slot0 + static_cast<size_t>(split) * SLOT_V * 32 + lane;
             auto put = [&](const uint32_t(&r)[32], int v0) {
 #pragma unroll
@@ -480,9 +563,9 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
             __threadfence();
             __syncwarp();
             int ticket = 0;
-            if (lane == 0) ticket = atomicAdd(p.ws_cnt + slice, 1);
+            if (lane == 0) ticket = atomicAdd(pq.ws_cnt + slice, 1);
             ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
-            last = ticket == p.splits - 1;
+            last = ticket == pq.splits - 1;
             if (last) {
               __threadfence();
               // two splits: add the other unit's partial to this one's in place; fp32 addition
@@ -507,7 +590,7 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
                 add(r2, 16);
                 add(r3, 24);
               }
-              if (lane == 0) p.ws_cnt[slice] = 0;  // zero again for the next call
+              if (lane == 0) pq.ws_cnt[slice] = 0;  // zero again for the next call
             }
           }
         }
@@ -534,15 +617,16 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
       // while the current one is folded (software pipeline over chunks), so a TMEM round trip
       // overlaps 32 FMAs instead of stalling the warp.
       const int col0 = (ew >> 2) * 64;
-      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {  // block scaling never splits K
+      const KProb& pb = p.pr[0];  // block scaling: one problem, never split
+      for (int t = tile0; ok && t < pb.num_tiles; t += tile_step) {
         int mb, nb;
-        tile_coords(t, p, mb, nb);
+        tile_coords(t, pb.num_m, pb.num_n, mb, nb);
         const int row = mb * BM + q * 32 + lane;
         const int nblk = (nb * BN + col0) / 128;
-        const bool row_ok = row < p.M;
-        const bool col_ok = nblk * 128 < p.N;
-        const float* sa_row = p.sa + (int64_t)row * p.sa_ld;
-        const float* sb_col = p.sb + nblk;
+        const bool row_ok = row < pb.M;
+        const bool col_ok = nblk * 128 < pb.N;
+        const float* sa_row = pb.sa + (int64_t)row * pb.sa_ld;
+        const float* sb_col = pb.sb + nblk;
         float accum[64];
 #pragma unroll
         for (int j = 0; j < 64; ++j) accum[j] = 0.0f;
@@ -555,11 +639,11 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
         tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), ra);
         tmem_ld_wait();
         reg_fence(ra);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = 0; kb < pb.num_kb; ++kb) {
           const float sc = __fmul_rn(sa_n, sb_n);
-          const bool more = kb + 1 < p.num_kb;
+          const bool more = kb + 1 < pb.num_kb;
           sa_n = (row_ok && more) ? __ldg(sa_row + kb + 1) : 0.0f;
-          sb_n = (col_ok && more) ? __ldg(sb_col + (int64_t)(kb + 1) * p.sb_ld) : 0.0f;
+          sb_n = (col_ok && more) ? __ldg(sb_col + (int64_t)(kb + 1) * pb.sb_ld) : 0.0f;
           tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0 + 32), rb);
 #pragma unroll
           for (int j = 0; j < 32; ++j) accum[j] = fmaf(__uint_as_float(ra[j]), sc, accum[j]);
@@ -753,64 +837,187 @@ SplitLayout split_layout(int64_t M, int64_t N, const TileChoice& c) {
   return l;
 }
 
-template <bool BLOCK, int BN, int QF>
-cudaError_t launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tq,
-                           KParams p, cudaStream_t stream) {
-  int unused = 0;
-  cudaError_t e = prepare_kernel<BLOCK, BN, QF, false>(&unused);
-  if (e != cudaSuccess) return e;
-  p.num_n = (p.N + BN - 1) / BN;
-  p.num_tiles = p.num_m * p.num_n;
-  p.idesc = idesc_f8(p.idesc & 7u, (p.idesc >> 3) & 7u, BM, BN);
-  const int units = p.num_tiles * p.splits;
-  const int grid = units < num_sms() ? units : num_sms();
-  return launch_pdl(gemm_f8_kernel<BLOCK, BN, QF, false>, dim3(grid), dim3(Cfg<BLOCK, BN, QF, false>::THREADS),
-                    Cfg<BLOCK, BN, QF, false>::SMEM, stream, ta, tb, tc, tq, p);
+// Tensor maps of one problem (A and B K-major codes, C bf16).
+struct Maps {
+  CUtensorMap a, b, c;
+};
+
+// The launch's view of one GEMM: tile counts, instruction descriptor, scales and (when the
+// choice splits K) its workspace; the tensor maps with the tile's box sizes.
+bool make_problem(const GemmArgs& g, const TileChoice& c, KProb& q, Maps& m, const char** why) {
+  const int rows = c.pair ? 2 * BM : BM;
+  q.M = static_cast<int>(g.M);
+  q.N = static_cast<int>(g.N);
+  q.K = static_cast<int>(g.K);
+  q.num_m = static_cast<int>((g.M + rows - 1) / rows);
+  q.num_n = static_cast<int>((g.N + c.bn - 1) / c.bn);
+  q.num_kb = static_cast<int>((g.K + BK - 1) / BK);
+  q.num_tiles = q.num_m * q.num_n;
+  q.idesc = idesc_f8(static_cast<uint32_t>(g.fa), static_cast<uint32_t>(g.fb), static_cast<uint32_t>(rows),
+                     static_cast<uint32_t>(c.bn));
+  q.sa = g.sa;
+  q.sb = g.sb;
+  q.sa_ld = static_cast<int>(g.K / 128);
+  q.sb_ld = static_cast<int>(g.N / 128);
+  q.splits = 1;
+  q.ws = nullptr;
+  q.ws_cnt = nullptr;
+  q.unit0 = 0;
+  if (c.splits > 1) {
+    const SplitLayout l = split_layout(g.M, g.N, c);
+    q.splits = c.splits;
+    q.ws_cnt = static_cast<int*>(g.ws);
+    q.ws = reinterpret_cast<float4*>(static_cast<uint8_t*>(g.ws) + l.counter_bytes);
+  }
+  const uint32_t b_rows = c.pair ? static_cast<uint32_t>(c.bn / 2) : static_cast<uint32_t>(c.bn);
+  if (!make_map(&m.a, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.M, g.lda, BK, BM) ||
+      !make_map(&m.b, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.N, g.ldb, BK, b_rows) ||
+      !make_map(&m.c, g.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.N, g.M, g.ldc * 2, 64, 32)) {
+    *why = "cuTensorMapEncodeTiled failed (driver entry point missing or tensor map rejected)";
+    return false;
+  }
+  return true;
 }
 
-// CTA-pair launch: clusters of two, one pair per 256 x BN tile, persistent over the tiles.
-template <int BN, int QF>
-cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tq,
-                        KParams p, cudaStream_t stream) {
-  using C = Cfg<false, BN, QF, true>;
+// Units of unequal length (a grouped launch) are packed onto the slots by first-fit
+// decreasing under a makespan bound found by bisection: the shortest bound under which every
+// unit fits. Returns that makespan (in K blocks) and, when `lists` is given, the packing.
+int64_t pack_units(const std::vector<std::pair<int, int>>& us_sorted, int slots,
+                   std::vector<std::vector<int>>* lists) {
+  int64_t total = 0, longest = 0;
+  for (const auto& x : us_sorted) {
+    total += x.first;
+    longest = std::max<int64_t>(longest, x.first);
+  }
+  auto fits = [&](int64_t bound, std::vector<std::vector<int>>* out) {
+    std::vector<int64_t> load(slots, 0);
+    if (out) out->assign(slots, {});
+    for (const auto& x : us_sorted) {
+      int sl = 0;
+      while (sl < slots && load[sl] + x.first > bound) ++sl;
+      if (sl == slots) return false;
+      load[sl] += x.first;
+      if (out) (*out)[sl].push_back(x.second);
+    }
+    return true;
+  };
+  int64_t lo = std::max<int64_t>(longest, (total + slots - 1) / slots), hi = total;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) / 2;
+    if (fits(mid, nullptr))
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  if (lists) fits(lo, lists);
+  return lo;
+}
+
+// Units of the launch's problems as (K blocks, unit index), longest first.
+std::vector<std::pair<int, int>> launch_units(const KParams& p) {
+  std::vector<std::pair<int, int>> us;
+  for (int pi = 0; pi < p.nprob; ++pi) {
+    const KProb& q = p.pr[pi];
+    for (int v = 0; v < q.num_tiles * q.splits; ++v) {
+      const int sp = v % q.splits;
+      us.push_back({(sp + 1) * q.num_kb / q.splits - sp * q.num_kb / q.splits, q.unit0 + v});
+    }
+  }
+  std::stable_sort(us.begin(), us.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
+  return us;
+}
+
+// Round-robin makespan (slot s takes units s, s + slots, ...), in K blocks.
+int64_t round_robin_makespan(const KParams& p, int slots) {
+  std::vector<int64_t> load(slots, 0);
+  for (const auto& x : launch_units(p)) load[x.second % slots] += x.first;
+  return *std::max_element(load.begin(), load.end());
+}
+
+// Explicit schedule of a grouped launch when it beats round robin; cached per shape (the
+// packing search is host work a repeated call should not pay again).
+void make_schedule(KParams& p, int slots) {
+  p.sched_len = 0;
+  if (p.nprob < 2 || p.units > kMaxSchedUnits || slots > kMaxSlots) return;
+  using Key = std::array<int, 7>;
+  struct Sched {
+    int len;
+    std::vector<uint16_t> off, unit;
+  };
+  static std::mutex mu;
+  static std::map<Key, Sched> cache;
+  const Key key{p.pr[0].num_tiles, p.pr[0].splits, p.pr[0].num_kb, p.pr[1].num_tiles, p.pr[1].splits,
+                p.pr[1].num_kb, slots};
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(key);
+  if (it == cache.end()) {
+    Sched sc{0, {}, {}};
+    std::vector<std::vector<int>> lists;
+    const auto us = launch_units(p);
+    if (pack_units(us, slots, &lists) < round_robin_makespan(p, slots)) {
+      int off = 0;
+      for (int sl = 0; sl < slots; ++sl) {
+        sc.off.push_back(static_cast<uint16_t>(off));
+        for (int u : lists[sl]) {
+          sc.unit.push_back(static_cast<uint16_t>(u));
+          ++off;
+        }
+      }
+      sc.off.push_back(static_cast<uint16_t>(off));
+      sc.len = off;
+    }
+    it = cache.emplace(key, std::move(sc)).first;
+  }
+  const Sched& sc = it->second;
+  p.sched_len = sc.len;
+  for (size_t i = 0; i < sc.off.size(); ++i) p.sched_off[i] = sc.off[i];
+  for (size_t i = 0; i < sc.unit.size(); ++i) p.sched_unit[i] = sc.unit[i];
+}
+
+template <bool BLOCK, int BN, int QF, bool PAIR>
+cudaError_t launch_kernel(const Maps& m0, const Maps& m1, const CUtensorMap& tq, KParams& p, cudaStream_t stream) {
+  using C = Cfg<BLOCK, BN, QF, PAIR>;
   int clusters = 0;
-  cudaError_t e = prepare_kernel<false, BN, QF, true>(&clusters);
+  cudaError_t e = prepare_kernel<BLOCK, BN, QF, PAIR>(&clusters);
   if (e != cudaSuccess) return e;
-  if (clusters <= 0) return cudaErrorInvalidConfiguration;
-  p.num_m = (p.M + 2 * BM - 1) / (2 * BM);
-  p.num_n = (p.N + BN - 1) / BN;
-  p.num_tiles = p.num_m * p.num_n;
-  p.idesc = idesc_f8(p.idesc & 7u, (p.idesc >> 3) & 7u, 2 * BM, BN);
-  const int units = p.num_tiles * p.splits;
-  const int ncl = units < clusters ? units : clusters;
+  int slots = PAIR ? clusters : num_sms();
+  if (slots <= 0) return cudaErrorInvalidConfiguration;
+  if (slots > kMaxSlots) slots = kMaxSlots;
+  if (p.units < slots) slots = p.units;
+  make_schedule(p, slots);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * ncl);
+  cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? 2 * slots : slots));
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  int na = 0;
+  if (PAIR) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_f8_kernel<false, BN, QF, true>, ta, tb, tc, tq, p);
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, gemm_f8_kernel<BLOCK, BN, QF, PAIR>, m0.a, m0.b, m0.c, tq, m1.a, m1.b, m1.c, p);
 }
 
 template <int QF>
-cudaError_t launch_width(TileChoice tc_, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                         const CUtensorMap& tq, const KParams& p, cudaStream_t stream) {
-  if (tc_.pair) {
-    if (tc_.bn == 256) return launch_pair<256, QF>(ta, tb, tc, tq, p, stream);
-    if (tc_.bn == 192) return launch_pair<192, QF>(ta, tb, tc, tq, p, stream);
-    return launch_pair<128, QF>(ta, tb, tc, tq, p, stream);
+cudaError_t launch_choice(const TileChoice& c, const Maps& m0, const Maps& m1, const CUtensorMap& tq, KParams& p,
+                          cudaStream_t stream) {
+  if (c.pair) {
+    if (c.bn == 256) return launch_kernel<false, 256, QF, true>(m0, m1, tq, p, stream);
+    if (c.bn == 192) return launch_kernel<false, 192, QF, true>(m0, m1, tq, p, stream);
+    return launch_kernel<false, 128, QF, true>(m0, m1, tq, p, stream);
   }
-  if (tc_.bn == 256) return launch_variant<false, 256, QF>(ta, tb, tc, tq, p, stream);
-  if (tc_.bn == 192) return launch_variant<false, 192, QF>(ta, tb, tc, tq, p, stream);
-  return launch_variant<false, 128, QF>(ta, tb, tc, tq, p, stream);
+  if (c.bn == 256) return launch_kernel<false, 256, QF, false>(m0, m1, tq, p, stream);
+  if (c.bn == 192) return launch_kernel<false, 192, QF, false>(m0, m1, tq, p, stream);
+  return launch_kernel<false, 128, QF, false>(m0, m1, tq, p, stream);
 }
 
 // Pairs the device holds at once (0 when it cannot launch clusters of two).
@@ -866,41 +1073,18 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why
     }
 #endif
   }
-  const int bn = choice.bn;
-  const uint32_t b_rows = choice.pair ? static_cast<uint32_t>(bn / 2) : static_cast<uint32_t>(bn);
-  CUtensorMap ta, tb, tc;
-  if (!make_map(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.M, g.lda, BK, BM) ||
-      !make_map(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.N, g.ldb, BK, b_rows) ||
-      !make_map(&tc, g.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.N, g.M, g.ldc * 2, 64, 32)) {
-    *why = "cuTensorMapEncodeTiled failed (driver entry point missing or tensor map rejected)";
-    return cudaErrorInvalidValue;
-  }
   KParams p{};
-  p.M = static_cast<int>(g.M);
-  p.N = static_cast<int>(g.N);
-  p.K = static_cast<int>(g.K);
-  p.num_m = static_cast<int>((g.M + BM - 1) / BM);
-  p.num_kb = static_cast<int>((g.K + BK - 1) / BK);
-  p.idesc = static_cast<uint32_t>(g.fa) | (static_cast<uint32_t>(g.fb) << 3);  // formats; finished per variant
-  p.sa = g.sa;
-  p.sb = g.sb;
-  p.sa_ld = static_cast<int>(g.K / 128);
-  p.sb_ld = static_cast<int>(g.N / 128);
-  p.splits = 1;
-  p.ws = nullptr;
-  p.ws_cnt = nullptr;
-  if (choice.splits > 1) {
-    const SplitLayout l = split_layout(g.M, g.N, choice);
-    p.splits = choice.splits;
-    p.ws_cnt = static_cast<int*>(g.ws);
-    p.ws = reinterpret_cast<float4*>(static_cast<uint8_t*>(g.ws) + l.counter_bytes);
-  }
+  Maps m0;
+  if (!make_problem(g, choice, p.pr[0], m0, why)) return cudaErrorInvalidValue;
+  p.pr[1] = p.pr[0];
+  p.nprob = 1;
+  p.units = p.pr[0].num_tiles * p.pr[0].splits;
   p.w = wait_ctl();
   if (p.w.err == nullptr) {
     *why = "device error word unavailable";
     return cudaErrorInvalidDevice;
   }
-  CUtensorMap tq = tc;  // unused unless the epilogue also writes FP8 codes
+  CUtensorMap tq = m0.c;  // unused unless the epilogue also writes FP8 codes
   if (g.qf >= 0) {
     if (!encode_tmap_2d(&tq, g.Cq, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.N, g.M, g.ldcq, 64, 32, 64)) {
       *why = "cuTensorMapEncodeTiled failed for the FP8 output";
@@ -908,10 +1092,103 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why
     }
     p.cst = g.cst;
   }
-  if (g.block_scaled) return launch_variant<true, 128, -1>(ta, tb, tc, tq, p, stream);
-  if (g.qf == 0) return launch_width<0>(choice, ta, tb, tc, tq, p, stream);
-  if (g.qf == 1) return launch_width<1>(choice, ta, tb, tc, tq, p, stream);
-  return launch_width<-1>(choice, ta, tb, tc, tq, p, stream);
+  if (g.block_scaled) return launch_kernel<true, 128, -1, false>(m0, m0, tq, p, stream);
+  if (g.qf == 0) return launch_choice<0>(choice, m0, m0, tq, p, stream);
+  if (g.qf == 1) return launch_choice<1>(choice, m0, m0, tq, p, stream);
+  return launch_choice<-1>(choice, m0, m0, tq, p, stream);
+}
+
+// Split-K workspace bytes of problem g in a grouped launch with tile choice c (0: no split).
+int64_t group_split_bytes(const GemmArgs& g, const TileChoice& c) {
+  if (c.splits <= 1) return 0;
+  return split_layout(g.M, g.N, c).total_bytes;
+}
+
+bool group_pair(const GemmArgs& g0, const GemmArgs& g1) { return g0.M > BM && g1.M > BM && pair_capacity() > 0; }
+
+// Tile choices of a grouped launch: CTA pairs with 256-wide tiles when both problems have
+// more than 128 rows (else single CTAs), and for each problem K whole or in two halves,
+// whichever packs the two problems' units into the shortest makespan (a split unit carries
+// ~3 K blocks of partial-sum traffic) within `ws_limit` bytes of workspace. Cached per shape.
+struct GroupPlan {
+  TileChoice c0, c1;
+  int64_t b0, b1;
+};
+
+GroupPlan plan_group(const GemmArgs& g0, const GemmArgs& g1, int64_t ws_limit) {
+  const bool pair = group_pair(g0, g1);
+  int slots = pair ? pair_capacity() : num_sms();
+  if (slots > kMaxSlots) slots = kMaxSlots;
+  using Key = std::array<int64_t, 9>;
+  static std::mutex mu;
+  static std::map<Key, GroupPlan> cache;
+  const Key key{g0.M, g0.N, g0.K, g1.M, g1.N, g1.K, ws_limit, slots, pair ? 1 : 0};
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  GroupPlan best{{256, pair, 1}, {256, pair, 1}, 0, 0};
+  int64_t best_cost = -1;
+  for (int s0 = 1; s0 <= 2; ++s0) {
+    for (int s1 = 1; s1 <= 2; ++s1) {
+      const TileChoice c0{256, pair, s0}, c1{256, pair, s1};
+      const SplitLayout l0 = split_layout(g0.M, g0.N, c0), l1 = split_layout(g1.M, g1.N, c1);
+      const int64_t b0 = group_split_bytes(g0, c0), b1 = group_split_bytes(g1, c1);
+      if (b0 + b1 > ws_limit || l0.slices * 4 > kSplitCounterBytes || l1.slices * 4 > kSplitCounterBytes) continue;
+      if ((s0 > 1 && b0 - l0.counter_bytes > kSplitMaxBytes) || (s1 > 1 && b1 - l1.counter_bytes > kSplitMaxBytes))
+        continue;
+      std::vector<std::pair<int, int>> us;
+      const GemmArgs* gs[2] = {&g0, &g1};
+      const TileChoice* cs[2] = {&c0, &c1};
+      for (int pi = 0; pi < 2; ++pi) {
+        const int rows = pair ? 2 * BM : BM;
+        const int64_t tiles = (gs[pi]->M + rows - 1) / rows * ((gs[pi]->N + 255) / 256);
+        const int kb = static_cast<int>((gs[pi]->K + BK - 1) / BK), sp = cs[pi]->splits;
+        if (sp > kb) {
+          us.clear();
+          break;
+        }
+        for (int64_t t = 0; t < tiles; ++t)
+          for (int h = 0; h < sp; ++h)
+            us.push_back({(h + 1) * kb / sp - h * kb / sp + (sp > 1 ? kSplitUnitKb : 0), 0});
+      }
+      if (us.empty() || static_cast<int64_t>(us.size()) > kMaxSchedUnits) continue;
+      std::stable_sort(us.begin(), us.end(), [](const auto& x, const auto& y) { return x.first > y.first; });
+      const int64_t cost = pack_units(us, slots, nullptr);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best = {c0, c1, b0, b1};
+      }
+    }
+  }
+  cache.emplace(key, best);
+  return best;
+}
+
+int64_t gemm_group_workspace_bytes(const GemmArgs& g0, const GemmArgs& g1) {
+  const GroupPlan pl = plan_group(g0, g1, INT64_MAX);
+  return pl.b0 + pl.b1;
+}
+
+cudaError_t launch_gemm_group(const GemmArgs& g0in, const GemmArgs& g1in, void* ws, int64_t ws_bytes,
+                              cudaStream_t stream, const char** why) {
+  GemmArgs g0 = g0in, g1 = g1in;
+  const GroupPlan pl = plan_group(g0, g1, ws != nullptr ? ws_bytes : 0);
+  if (pl.b0 > 0) g0.ws = ws;
+  if (pl.b1 > 0) g1.ws = static_cast<uint8_t*>(ws) + pl.b0;
+  KParams p{};
+  Maps m0, m1;
+  if (!make_problem(g0, pl.c0, p.pr[0], m0, why) || !make_problem(g1, pl.c1, p.pr[1], m1, why))
+    return cudaErrorInvalidValue;
+  p.nprob = 2;
+  p.pr[0].unit0 = 0;
+  p.pr[1].unit0 = p.pr[0].num_tiles * p.pr[0].splits;
+  p.units = p.pr[1].unit0 + p.pr[1].num_tiles * p.pr[1].splits;
+  p.w = wait_ctl();
+  if (p.w.err == nullptr) {
+    *why = "device error word unavailable";
+    return cudaErrorInvalidDevice;
+  }
+  return launch_choice<-1>(pl.c0, m0, m1, m0.c, p, stream);
 }
 
 }  // namespace fp8gb

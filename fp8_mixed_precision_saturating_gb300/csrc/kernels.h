@@ -103,5 +103,10 @@ struct GemmArgs {
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why);
 // Workspace bytes a split-K launch of this per-tensor problem uses (0: it would not split).
 int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// Two independent per-tensor GEMMs (bf16 outputs) in one persistent launch; ws (optional,
+// gemm_group_workspace_bytes long, zero-filled once) lets them split K.
+cudaError_t launch_gemm_group(const GemmArgs& g0, const GemmArgs& g1, void* ws, int64_t ws_bytes,
+                              cudaStream_t stream, const char** why);
+int64_t gemm_group_workspace_bytes(const GemmArgs& g0, const GemmArgs& g1);
 
 }  // namespace fp8gb

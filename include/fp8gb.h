@@ -168,6 +168,35 @@ fp8_status_t fp8_scaled_mm_ws(const void* A, fp8_format_t fa, const void* B, fp8
  * 0 when it would not split (a null workspace then costs nothing). Negative on a CUDA error. */
 int64_t fp8_scaled_mm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
+/* One per-tensor-scaled GEMM of a grouped call: the arguments of fp8_scaled_mm with
+ * gran = FP8_GRAN_TENSOR (C_bf16 [M,N] = bf16(d_a d_b sum_k a_ik b_jk)). */
+typedef struct {
+  const void* A;
+  fp8_format_t fa;
+  const void* B;
+  fp8_format_t fb;
+  int64_t M, N, K, lda, ldb;
+  const float* scale_inv_a;
+  const float* scale_inv_b;
+  void* C_bf16;
+  int64_t ldc;
+} fp8_mm_problem_t;
+
+/* n (1 or 2) independent GEMMs in one persistent launch: their tiles share the GPU (longest
+ * work units first, each on the least-loaded SM pair), so two problems that each leave SMs idle
+ * (the backward pass's dgrad and wgrad) finish together instead of one after the other. The
+ * pages have no such entry point: each problem is "Explanation"'s scaled FP8 matmul ([SPEED]),
+ * computed as fp8_scaled_mm computes it. workspace (optional) follows fp8_scaled_mm_ws's rules
+ * and lets a problem split K; size from fp8_scaled_mm_grouped_workspace_bytes. Each problem
+ * obeys fp8_scaled_mm's rules with M, N, K > 0; the outputs must not overlap the inputs or
+ * each other. */
+fp8_status_t fp8_scaled_mm_grouped(const fp8_mm_problem_t* problems, int32_t n, void* workspace,
+                                   int64_t workspace_bytes, void* stream);
+
+/* Workspace bytes fp8_scaled_mm_grouped uses for these problems (0: nothing splits); negative
+ * on a CUDA error or bad arguments. */
+int64_t fp8_scaled_mm_grouped_workspace_bytes(const fp8_mm_problem_t* problems, int32_t n);
+
 /* fp8_scaled_mm (per-tensor scales) whose epilogue also emits the FP8 codes of its output for
  * a following FP8 consumer (for example dgrad's dx, cast to E5M2 for the previous layer's
  * backward), so the bf16 result is not read back by a separate cast.
@@ -240,6 +269,22 @@ fp8_status_t fp8_linear_bwd(const void* dy_bf16, int64_t M, int64_t K, int64_t N
                             fp8_tensor_state_t* dy_st, fp8_scaling_t mode,
                             void* dyq_ws, void* dyqT_ws, void* dx_bf16, void* dw_bf16,
                             void* stream);
+
+/* fp8_linear_bwd with a caller-owned workspace: when both dx and dW are requested, the two
+ * GEMMs run in one persistent launch either way (their tiles share the grid, longest first on
+ * the least-loaded SMs); the workspace also lets the weight gradient split its long token
+ * contraction (see fp8_scaled_mm_ws). The pages have no such entry point: it is
+ * fp8_linear_bwd's computation ("FP8 stability guardrails": E5M2 gradients) with
+ * fp8_scaled_mm_ws's workspace rules (16-byte aligned, zero-filled before first use, left
+ * reusable, one call at a time per workspace; smaller or null runs without split K). */
+fp8_status_t fp8_linear_bwd_ws(const void* dy_bf16, int64_t M, int64_t K, int64_t N, const void* xqT_save,
+                               const fp8_tensor_state_t* x_st, const void* wq_kn, const fp8_tensor_state_t* w_st,
+                               fp8_tensor_state_t* dy_st, fp8_scaling_t mode, void* dyq_ws, void* dyqT_ws,
+                               void* dx_bf16, void* dw_bf16, void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Workspace bytes fp8_linear_bwd_ws uses for these sizes with dx and dW both requested on the
+ * current device (0: it would not split). Negative on a CUDA error. */
+int64_t fp8_linear_bwd_workspace_bytes(int64_t M, int64_t K, int64_t N);
 
 /* fp8_linear_bwd without caller scratch. The pages have no counterpart to this entry point:
  * it exists for callers that cannot allocate device memory at the point of the call -- for

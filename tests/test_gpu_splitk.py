@@ -101,3 +101,53 @@ def test_ws_rejections(g):
         g.fp8_scaled_mm_ws(A, 0, A, 0, 128, 128, 256, 256, 256, g.FP8_GRAN_TENSOR, one, one, C, 128, ws, -1)
     assert e.value.status == g.FP8_ERR_INVALID_ARG
     g.fp8_poll_device_error()
+
+
+def test_grouped_pair_against_exact(g):
+    """Two GEMMs of different shapes and formats in one launch (the backward's dgrad and a
+    split weight gradient), each against its exact product; then each alone."""
+    rng = np.random.default_rng(21)
+    shapes = [(384, 640, 4096, 0, 1), (4096, 384, 640, 1, 0)]  # wgrad-like (splits), dgrad-like
+    probs, refs, outs, ops = [], [], [], []
+    for M, N, K, fa, fb in shapes:
+        A = rand_codes(rng, (M, K), FMT[fa], 20.0)
+        B = rand_codes(rng, (N, K), FMT[fb], 20.0)
+        da, db = np.float32(rng.uniform(0.001, 0.05)), np.float32(rng.uniform(0.001, 0.05))
+        Ad, Bd = dev_u8(A), dev_u8(B)
+        C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        sa, sb = f32_scalar(da), f32_scalar(db)
+        ops.append((Ad, Bd, sa, sb))
+        outs.append(C)
+        probs.append(g.mm_problem(Ad, fa, Bd, fb, M, N, K, K, K, sa, sb, C, N))
+        refs.append(gemm.scaled_mm(A, FMT[fa], B, FMT[fb], da, db)[:2])
+    nbytes = g.fp8_scaled_mm_grouped_workspace_bytes(probs)
+    assert nbytes > 0
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    for _ in range(2):  # the second call reuses the workspace without clearing
+        g.fp8_scaled_mm_grouped(probs, ws, nbytes)
+        torch.cuda.synchronize()
+        for C, (ref, mag) in zip(outs, refs):
+            assert_close(host_bf16_f64(C), ref, mag)
+    g.fp8_scaled_mm_grouped(probs[:1])  # one problem, no workspace
+    torch.cuda.synchronize()
+    assert_close(host_bf16_f64(outs[0]), *refs[0])
+    g.fp8_poll_device_error()
+
+
+def test_grouped_rejections(g):
+    one = f32_scalar(1.0)
+    A = torch.zeros(128, 256, dtype=torch.uint8, device="cuda")
+    C = torch.zeros(128, 128, dtype=torch.bfloat16, device="cuda")
+    ok = g.mm_problem(A, 0, A, 0, 128, 128, 256, 256, 256, one, one, C, 128)
+    bad_k = g.mm_problem(A, 0, A, 0, 128, 128, 0, 256, 256, one, one, C, 128)
+    bad_ld = g.mm_problem(A, 0, A, 0, 128, 128, 256, 264, 256, one, one, C, 128)  # lda % 16 != 0
+    with pytest.raises(g.Fp8Error) as e:
+        g.fp8_scaled_mm_grouped([ok, bad_k])
+    assert e.value.status == g.FP8_ERR_INVALID_ARG
+    with pytest.raises(g.Fp8Error) as e:
+        g.fp8_scaled_mm_grouped([ok, bad_ld])
+    assert e.value.status == g.FP8_ERR_ALIGNMENT
+    with pytest.raises(g.Fp8Error) as e:
+        g.fp8_scaled_mm_grouped([ok, ok, ok])
+    assert e.value.status == g.FP8_ERR_INVALID_ARG
+    g.fp8_poll_device_error()
