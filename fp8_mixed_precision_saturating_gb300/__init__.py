@@ -59,6 +59,20 @@ class fp8_mm_problem_t(ctypes.Structure):
     ]
 
 
+class fp8_quant_job_t(ctypes.Structure):
+    _fields_ = [
+        ("x_bf16", ctypes.c_void_p),
+        ("rows", ctypes.c_int64),
+        ("cols", ctypes.c_int64),
+        ("ld", ctypes.c_int64),
+        ("fmt", ctypes.c_int),
+        ("mode", ctypes.c_int),
+        ("st", ctypes.POINTER(fp8_tensor_state_t)),
+        ("q_out", ctypes.c_void_p),
+        ("qT_out", ctypes.c_void_p),
+    ]
+
+
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _I = ctypes.c_int
@@ -70,6 +84,7 @@ _SIGS = {
     "fp8_scaled_mm": [_P, _I, _P, _I, _I64, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _P],
     "fp8_scaled_mm_ws": [_P, _I, _P, _I, _I64, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _P, _I64, _P],
     "fp8_scaled_mm_grouped": [_MP, ctypes.c_int32, _P, _I64, _P],
+    "fp8_quantize_many": [ctypes.POINTER(fp8_quant_job_t), ctypes.c_int32, _P],
     "fp8_scaled_mm_quant": [_P, _I, _P, _I, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _I64, _I, _SP, _P, _P],
     "fp8_requantize_weights": [_P, _I64, _I64, _I, _I, _SP, _P, _P, _P, _P],
     "fp8_update_requantize_weights": [_P, _P, _I64, _I64, _I, _SP, _P, _P, _P],
@@ -204,6 +219,19 @@ def fp8_scaled_mm_ws(A, fa, B, fb, M, N, K, lda, ldb, gran, scale_inv_a, scale_i
     return _check(lib.fp8_scaled_mm_ws(_ptr(A), fa, _ptr(B), fb, M, N, K, lda, ldb, gran, _ptr(scale_inv_a),
                                        _ptr(scale_inv_b), _ptr(C), ldc, _ptr(workspace), workspace_bytes,
                                        _stream(stream)))
+
+
+def quant_job(x, rows, cols, ld, fmt, mode, st, q, qT):
+    """One fp8_quant_job_t (per-tensor scale) for fp8_quantize_many; keeps st alive."""
+    c = st if isinstance(st, fp8_tensor_state_t) else st.c
+    j = fp8_quant_job_t(_ptr(x), rows, cols, ld, fmt, mode, ctypes.pointer(c), _ptr(q), _ptr(qT))
+    j._keep = st
+    return j
+
+
+def fp8_quantize_many(jobs, stream=None):
+    arr = (fp8_quant_job_t * len(jobs))(*jobs)
+    return _check(lib.fp8_quantize_many(arr, len(jobs), _stream(stream)))
 
 
 def mm_problem(A, fa, B, fb, M, N, K, lda, ldb, scale_inv_a, scale_inv_b, C, ldc):

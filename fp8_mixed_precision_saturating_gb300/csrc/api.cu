@@ -215,6 +215,56 @@ fp8_status_t fp8_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_
                        static_cast<cudaStream_t>(stream));
 }
 
+fp8_status_t fp8_quantize_many(const fp8_quant_job_t* jobs, int32_t n, void* stream) {
+  const char* who = "fp8_quantize_many";
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (n < 1 || n > kMaxJobs || jobs == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: 1 to %d jobs", who, kMaxJobs);
+  bool fused = true;
+  for (int i = 0; i < n; ++i) {
+    const fp8_quant_job_t& jb = jobs[i];
+    if (jb.st == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: job %d: state is required", who, i);
+    for (int k = 0; k < i; ++k)
+      if (jobs[k].st->amax_cur == jb.st->amax_cur) return fail(FP8_ERR_INVALID_ARG, "%s: job %d: state repeated", who, i);
+    fp8_status_t st = validate_common(jb.x_bf16, jb.rows, jb.cols, jb.ld, jb.fmt, who);
+    if (st != FP8_OK) return st;
+    if (jb.mode != FP8_SCALE_CURRENT && jb.mode != FP8_SCALE_DELAYED)
+      return fail(FP8_ERR_INVALID_ARG, "%s: job %d: unknown scaling mode", who, i);
+    if ((st = check_state(jb.st, jb.mode, who)) != FP8_OK) return st;
+    fused = fused && jb.fmt == jobs[0].fmt && jb.qT_out != nullptr && jb.rows > 0 && jb.cols > 0 && jb.rows % 16 == 0 &&
+            jb.cols % 8 == 0 && jb.ld % 8 == 0 && aligned16(jb.x_bf16) && aligned16(jb.q_out) && aligned16(jb.qT_out);
+  }
+  if (!fused || n == 1) {
+    for (int i = 0; i < n; ++i) {
+      const fp8_quant_job_t& jb = jobs[i];
+      const fp8_status_t st = quantize_impl(jb.x_bf16, jb.rows, jb.cols, jb.ld, jb.fmt, FP8_GRAN_TENSOR, jb.mode, jb.st,
+                                            jb.q_out, jb.qT_out, nullptr, s);
+      if (st != FP8_OK) return st;
+    }
+    return FP8_OK;
+  }
+  TileJobs tj{};
+  tj.n = n;
+  int64_t t0 = 0;
+  for (int i = 0; i < n; ++i) {
+    const fp8_quant_job_t& jb = jobs[i];
+    TileJob& t = tj.j[i];
+    t.x = static_cast<const uint16_t*>(jb.x_bf16);
+    t.rows = jb.rows;
+    t.cols = jb.cols;
+    t.ld = jb.ld;
+    t.q = static_cast<uint8_t*>(jb.q_out);
+    t.qT = static_cast<uint8_t*>(jb.qT_out);
+    t.st = to_qs(jb.st);
+    t.delayed = jb.mode == FP8_SCALE_DELAYED ? 1 : 0;
+    t.tiles_x = (jb.cols + 127) / 128;
+    t.ntiles = t.tiles_x * ((jb.rows + 127) / 128);
+    t.tile0 = t0;
+    t0 += t.ntiles;
+  }
+  const cudaError_t e = launch_quant_many((int)jobs[0].fmt, tj, s);
+  return e == cudaSuccess ? FP8_OK : cuda_fail(e, "quantise kernel");
+}
+
 fp8_status_t fp8_scaled_mm(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb, int64_t M, int64_t N,
                            int64_t K, int64_t lda, int64_t ldb, fp8_gran_t gran, const float* scale_inv_a,
                            const float* scale_inv_b, void* C_bf16, int64_t ldc, void* stream) {

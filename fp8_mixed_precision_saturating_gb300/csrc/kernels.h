@@ -57,6 +57,25 @@ int num_sms();
 // Device error word and wait limit for launches on the current device.
 WaitCtl wait_ctl();
 
+// One tensor of a multi-tensor per-tensor quantise (tiled layout: rows, cols, ld multiples of
+// 8, rows of 16 with qT); tile0 is its first tile in the launch's tile space.
+constexpr int kMaxJobs = 4;
+struct TileJob {
+  const uint16_t* x;
+  int64_t rows, cols, ld;
+  uint8_t* q;
+  uint8_t* qT;
+  QuantState st;
+  int delayed;
+  int64_t tiles_x, ntiles, tile0;
+};
+struct TileJobs {
+  TileJob j[kMaxJobs];
+  int n;
+};
+// Up to kMaxJobs tensors of one format (0 E4M3, 1 E5M2) in one cooperative launch.
+cudaError_t launch_quant_many(int fmt, const TileJobs& jobs, cudaStream_t stream);
+
 // Per-tensor quantise in one cooperative launch: amax (when the call needs it), scale, cast
 // with counters. tiled: 128x128 tiles with q and/or the transposed copy qT (rows, cols, ld
 // multiples of 8); otherwise row-major q of any shape.

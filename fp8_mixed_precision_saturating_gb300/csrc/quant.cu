@@ -203,6 +203,13 @@ __device__ __forceinline__ void update_patch(uint16_t* __restrict__ x, const flo
   }
 }
 
+// The first tile index >= t0 that this CTA owns (tiles are dealt out t = blockIdx.x mod grid).
+__device__ __forceinline__ int64_t first_tile(int64_t t0) {
+  const int64_t g = gridDim.x;
+  const int64_t r = (static_cast<int64_t>(blockIdx.x) - t0 % g + g) % g;
+  return t0 + r;
+}
+
 // Tiled layout: rows, cols and ld multiples of 8 (rows of 16 with qT); q and/or qT. With
 // UPD the tensor is first updated in place by delta (the weight-cache refresh fused with
 // the optimizer step): in the amax pass when there is one, else in the cast pass, so W and
@@ -264,6 +271,101 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(uint16_t* 
     const uint32_t b = block_max_u32(fold2(m), red);
     grid.sync();  // block 0 has zeroed amax_cur
     if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
+  }
+}
+
+// Several tensors of one format, tiled layout, in one cooperative launch: the tiles of all
+// jobs share the grid, so tensors too small to fill the GPU alone (a weight and an activation
+// at GPT-2-small sizes) cost one launch's latency. Per job exactly the single-tensor
+// kernel's computation: amax pass when the job needs its own amax, the job's scale, the
+// cast with counters, the delayed cast's amax record. All grid-wide syncs are shared. Four
+// CTAs per SM (64 registers), so GPT-2-small's weight and activation (528 tiles) take one
+// round on 152 SMs.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 4) quant_tiles_many_kernel(const __grid_constant__ TileJobs J) {
+  __shared__ __align__(128) uint8_t tT[128 * 128];
+  __shared__ uint32_t red[2 * kThreads / 32];
+  __shared__ uint32_t s_max[kMaxJobs];
+  cg::grid_group grid = cg::this_grid();
+  pdl_trigger();  // the next kernel may start its prologue as this one drains
+  uint32_t passmask = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxJobs; ++j)
+    if (j < J.n && needs_amax_pass(J.j[j].st, J.j[j].delayed)) passmask |= 1u << j;
+  if (blockIdx.x == 0 && threadIdx.x < J.n) *J.j[threadIdx.x].st.amax_cur = 0.0f;
+  if (passmask) {
+#pragma unroll
+    for (int j = 0; j < kMaxJobs; ++j) {
+      if (threadIdx.x == 0) s_max[j] = 0;
+      if (j >= J.n || !((passmask >> j) & 1u)) continue;
+      const TileJob& jb = J.j[j];
+      if (first_tile(jb.tile0) >= jb.tile0 + jb.ntiles) continue;  // no tile of this job here
+      uint32_t m = 0;
+      for (int64_t t = first_tile(jb.tile0); t < jb.tile0 + jb.ntiles; t += gridDim.x) {
+        const int64_t lt = t - jb.tile0;
+        uint4 v[8];
+        load_patch(jb.x, jb.rows, jb.cols, jb.ld, lt / jb.tiles_x, lt % jb.tiles_x, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = absmax_v(m, v[i]);
+      }
+      const uint32_t b = block_max_u32(fold2(m), red);
+      if (threadIdx.x == 0) s_max[j] = b;
+    }
+    grid.sync();  // every job's amax_cur is zero
+    if (threadIdx.x < J.n && ((passmask >> threadIdx.x) & 1u) && s_max[threadIdx.x] != 0)
+      atomic_max_amax(J.j[threadIdx.x].st.amax_cur, s_max[threadIdx.x]);
+    grid.sync();  // amax_cur holds each such job's tensor amax
+  }
+  __syncthreads();  // s_max is read above before the cast loop reuses it
+  bool any_delayed = false;
+#pragma unroll
+  for (int j = 0; j < kMaxJobs; ++j) {
+    if (j >= J.n) continue;
+    const TileJob& jb = J.j[j];
+    const bool pass = (passmask >> j) & 1u;
+    any_delayed |= !pass;
+    if (threadIdx.x == 0) s_max[j] = 0;
+    if (first_tile(jb.tile0) >= jb.tile0 + jb.ntiles) {  // no tile of this job here
+      if (blockIdx.x == 0 && threadIdx.x == 0) {        // (CTA 0 still publishes the scale)
+        float sj, dj;
+        scales_from_amax(call_amax(jb.st, jb.delayed), Fmt<FMT>::kMax, sj, dj);
+        *jb.st.scale = sj;
+        *jb.st.scale_inv = dj;
+      }
+      continue;
+    }
+    float sj, dj;
+    scales_from_amax(call_amax(jb.st, jb.delayed), Fmt<FMT>::kMax, sj, dj);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      *jb.st.scale = sj;
+      *jb.st.scale_inv = dj;
+    }
+    const Scaler sc = make_scaler<FMT>(sj, dj);
+    uint32_t ov = 0, un = 0, m = 0;
+    for (int64_t t = first_tile(jb.tile0); t < jb.tile0 + jb.ntiles; t += gridDim.x) {
+      const int64_t lt = t - jb.tile0, ty = lt / jb.tiles_x, tx = lt % jb.tiles_x;
+      uint4 v[8];
+      const bool in = load_patch(jb.x, jb.rows, jb.cols, jb.ld, ty, tx, v);
+      uint2 c[8];
+      uint32_t o1 = 0, u1 = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = cast8<FMT, true>(v[i], sc, o1, u1, m);
+      if (in) {
+        ov += o1;
+        un += u1;
+      }
+      store_patch(c, in, jb.rows, jb.cols, ty, tx, jb.q, jb.qT, tT);
+    }
+    block_add_counters(ov, un, jb.st.counters, red);
+    if (!pass) {
+      const uint32_t b = block_max_u32(fold2(m), red);
+      if (threadIdx.x == 0) s_max[j] = b;
+    }
+  }
+  if (any_delayed) {  // delayed casts past bootstrap record their current amax
+    grid.sync();      // block 0 has zeroed every amax_cur
+    if (threadIdx.x < J.n && !((passmask >> threadIdx.x) & 1u) && s_max[threadIdx.x] != 0)
+      atomic_max_amax(J.j[threadIdx.x].st.amax_cur, s_max[threadIdx.x]);
   }
 }
 
@@ -527,6 +629,13 @@ cudaError_t launch_quant_tensor(int fmt, bool delayed, bool tiled, const void* x
   auto k = fmt == 0 ? quant_tensor_flat_kernel<0> : quant_tensor_flat_kernel<1>;
   return launch_coop(k, coop_grid(k, (rows * cols + 4095) / 4096), stream, xp, rows, cols, ld, qp, st, dl,
                      static_cast<const int32_t*>(nullptr));
+}
+
+cudaError_t launch_quant_many(int fmt, const TileJobs& jobs, cudaStream_t stream) {
+  auto k = fmt == 0 ? quant_tiles_many_kernel<0> : quant_tiles_many_kernel<1>;
+  int64_t total = 0;
+  for (int j = 0; j < jobs.n; ++j) total += jobs.j[j].ntiles;
+  return launch_coop(k, coop_grid(k, total), stream, jobs);
 }
 
 cudaError_t launch_quant_tensor_if_empty_history(int fmt, const void* x, int64_t rows, int64_t cols, int64_t ld,

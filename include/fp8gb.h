@@ -122,6 +122,26 @@ fp8_status_t fp8_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_
                           const fp8_tensor_state_t* st, void* q_out, void* qT_out,
                           float* unit_scale_inv, void* stream);
 
+/* One tensor of fp8_quantize_many: the arguments of fp8_quantize with gran = FP8_GRAN_TENSOR. */
+typedef struct {
+  const void* x_bf16;
+  int64_t rows, cols, ld;
+  fp8_format_t fmt;
+  fp8_scaling_t mode;
+  const fp8_tensor_state_t* st;
+  void* q_out;
+  void* qT_out;
+} fp8_quant_job_t;
+
+/* n (1..4) per-tensor quantises, each exactly fp8_quantize(job, FP8_GRAN_TENSOR): when all
+ * share one format, each writes its transposed copy (qT_out non-null) and rows, cols, ld are
+ * multiples of 8 (rows of 16), they run as one cooperative launch whose grid shares their
+ * tiles, so small tensors (a weight cache refresh next to an activation cast) pay one
+ * launch's latency; otherwise one after the other. The pages have no such entry point: it is
+ * [GUARD] "Real products..." per-tensor scaling applied to several tensors at once. Every job
+ * obeys fp8_quantize's rules; the states must be distinct. */
+fp8_status_t fp8_quantize_many(const fp8_quant_job_t* jobs, int32_t n, void* stream);
+
 /* C [M,N] (bf16, leading dimension ldc) = dequantised A [M,K] times B [N,K] transposed:
  *   C_ij = bf16_rne( d_a * d_b * sum_k a_ik b_jk ),  fp32 accumulation.
  *  [SPEED] "Explanation": the scaled FP8 matmul with one scale per operand, both operands
