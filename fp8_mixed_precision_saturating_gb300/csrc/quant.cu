@@ -119,7 +119,9 @@ __device__ __forceinline__ bool load_patch(const uint16_t* __restrict__ x, int64
 }
 
 // Write the patch's codes row-major into q [rows, cols] and transposed into qT [cols, rows]
-// (through the CTA's shared buffer tT; every thread of the CTA must call this).
+// (through the CTA's shared buffer tT; every thread of the CTA must call this). Callers
+// alternate between two buffers from tile to tile: the barrier of the next call orders this
+// call's reads of one buffer before the call after next writes it again.
 __device__ __forceinline__ void store_patch(const uint2 (&c)[8], bool in, int64_t rows, int64_t cols, int64_t ty,
                                             int64_t tx, uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
                                             uint8_t* tT) {
@@ -153,7 +155,6 @@ __device__ __forceinline__ void store_patch(const uint2 (&c)[8], bool in, int64_
         *reinterpret_cast<uint4*>(qT + gr * rows + gc) = val;
       }
     }
-    __syncthreads();  // tT is reused by the next tile
   }
 }
 
@@ -219,10 +220,11 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(uint16_t* 
                                                                       int64_t cols, int64_t ld, uint8_t* __restrict__ q,
                                                                       uint8_t* __restrict__ qT, QuantState st,
                                                                       int delayed, const float* __restrict__ delta) {
-  __shared__ __align__(128) uint8_t tT[128 * 128];
+  __shared__ __align__(128) uint8_t tT[2][128 * 128];  // alternating transpose buffers
   __shared__ uint32_t red[2 * kThreads / 32];
   cg::grid_group grid = cg::this_grid();
   pdl_trigger();  // the next kernel may start its prologue as this one drains
+  int it = 0;     // tiles written by this CTA (picks the transpose buffer)
   const int64_t tiles_x = (cols + 127) / 128;
   const int64_t ntiles = tiles_x * ((rows + 127) / 128);
   const bool pass = needs_amax_pass(st, delayed);
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(uint16_t* 
       ov += o1;
       un += u1;
     }
-    store_patch(c, in, rows, cols, ty, tx, q, qT, tT);
+    store_patch(c, in, rows, cols, ty, tx, q, qT, tT[it++ & 1]);
   }
   block_add_counters(ov, un, st.counters, red);
   if (!pass) {  // delayed scaling past bootstrap: this cast measures the current amax
@@ -283,9 +285,10 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(uint16_t* 
 // round on 152 SMs.
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 4) quant_tiles_many_kernel(const __grid_constant__ TileJobs J) {
-  __shared__ __align__(128) uint8_t tT[128 * 128];
+  __shared__ __align__(128) uint8_t tT[2][128 * 128];  // alternating transpose buffers
   __shared__ uint32_t red[2 * kThreads / 32];
   __shared__ uint32_t s_max[kMaxJobs];
+  int it = 0;  // tiles written by this CTA (picks the transpose buffer)
   cg::grid_group grid = cg::this_grid();
   pdl_trigger();  // the next kernel may start its prologue as this one drains
   uint32_t passmask = 0;
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 4) quant_tiles_many_kernel(const __g
         ov += o1;
         un += u1;
       }
-      store_patch(c, in, jb.rows, jb.cols, ty, tx, jb.q, jb.qT, tT);
+      store_patch(c, in, jb.rows, jb.cols, ty, tx, jb.q, jb.qT, tT[it++ & 1]);
     }
     block_add_counters(ov, un, jb.st.counters, red);
     if (!pass) {
