@@ -636,14 +636,14 @@ def oracle_step(tokens: int):
     return 3 * 2.0 * tokens * N * K
 
 
-def cpu_baseline_full_step():
+def cpu_baseline_full_step(steps: int = 3):
     oracle_step(64)  # load inputs
     t0 = time.perf_counter()
-    fl = oracle_step(M)
+    fl = sum(oracle_step(M) for _ in range(steps))
     dt = time.perf_counter() - t0
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"one full step ({M} tokens): numpy oracle casts (one thread) and fp64 BLAS matmuls "
-                      f"(all cores); {dt:.1f} s"}
+            "sample": f"{steps} full steps ({M} tokens each): numpy oracle casts (one thread) and fp64 BLAS "
+                      f"matmuls (all cores); {dt:.1f} s"}
 
 
 def run_reference(args):
