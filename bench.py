@@ -371,51 +371,59 @@ def run_block_scaled(g, torch, x, wm, stream, flush, steps):
 def run_e2e(g, torch, x_h, w_h, dy_h, stream, steps, step_flops):
     """The same step through the public API (requantise + linear forward + linear backward
     + commits) with host inputs: pinned host -> device copies of x, W and dy and device ->
-    host copies of y, dx and dW inside the timed region, overlapped with the compute."""
+    host copies of y, dx and dW inside the timed region, every step. Steps alternate between
+    two sets of device inputs and outputs (and host result buffers), so one step's uploads
+    and compute overlap the previous step's downloads."""
     import numpy as np
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
     xh, wh, dyh = pin(x_h), pin(w_h), pin(dy_h)
     bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
     u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device="cuda")
-    x, wm, dy = bf(M, K), bf(K, N), bf(M, N)
-    y, dx, dw = bf(M, N), bf(M, K), bf(K, N)
-    yh, dxh, dwh = [torch.empty(*s, dtype=torch.bfloat16).pin_memory() for s in ((M, N), (M, K), (K, N))]
+    sets = []
+    for _ in range(2):
+        sets.append(dict(x=bf(M, K), wm=bf(K, N), dy=bf(M, N), y=bf(M, N), dx=bf(M, K), dw=bf(K, N),
+                         yh=torch.empty(M, N, dtype=torch.bfloat16).pin_memory(),
+                         dxh=torch.empty(M, K, dtype=torch.bfloat16).pin_memory(),
+                         dwh=torch.empty(K, N, dtype=torch.bfloat16).pin_memory(),
+                         ev_xw=torch.cuda.Event(), ev_dy=torch.cuda.Event(), ev_fwd=torch.cuda.Event(),
+                         ev_done=torch.cuda.Event(), ev_out=torch.cuda.Event(), used=False))
     wq, wqT, xq, xqT, dyq, dyqT = u8(K, N), u8(N, K), u8(M, K), u8(K, M), u8(M, N), u8(N, M)
     wst, xst, gst = g.TensorState(HIST), g.TensorState(HIST), g.TensorState(HIST)
     D, T = g.FP8_SCALE_DELAYED, g.FP8_GRAN_TENSOR
     wsb = g.fp8_linear_bwd_workspace_bytes(M, K, N)
     ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
-
-    # copies overlap the compute on two copy streams: x and W go up first, dy goes up while
-    # the forward runs, y comes down while the backward runs, dx and dW after it; a step's
-    # uploads may overlap the previous step's downloads (different buffers)
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_xw, ev_dy, ev_fwd, ev_bwd = (torch.cuda.Event() for _ in range(4))
+    count = [0]
 
     def one():
-        s_in.wait_stream(stream)  # the previous step's kernels have read x, W and dy
+        b = sets[count[0] % 2]
+        count[0] += 1
+        if b["used"]:
+            s_in.wait_event(b["ev_done"])  # this set's previous step has read its inputs
+            stream.wait_event(b["ev_out"])  # ... and its outputs are on the host
+        b["used"] = True
         with torch.cuda.stream(s_in):
-            x.copy_(xh, non_blocking=True)
-            wm.copy_(wh, non_blocking=True)
-            ev_xw.record(s_in)
-            dy.copy_(dyh, non_blocking=True)
-            ev_dy.record(s_in)
-        stream.wait_stream(s_out)  # the previous step's outputs are on the host
-        stream.wait_event(ev_xw)
-        g.fp8_requantize_weights(wm, K, N, T, D, wst, wq, wqT)
-        g.fp8_linear_fwd(x, M, K, N, wqT, wst, None, xst, T, D, xq, xqT, None, y)
-        ev_fwd.record(stream)
-        s_out.wait_event(ev_fwd)
-        with torch.cuda.stream(s_out):
-            yh.copy_(y, non_blocking=True)
-        stream.wait_event(ev_dy)
-        g.fp8_linear_bwd_ws(dy, M, K, N, xqT, xst, wq, wst, gst, D, dyq, dyqT, dx, dw, ws, wsb)
+            b["x"].copy_(xh, non_blocking=True)
+            b["wm"].copy_(wh, non_blocking=True)
+            b["ev_xw"].record(s_in)
+            b["dy"].copy_(dyh, non_blocking=True)
+            b["ev_dy"].record(s_in)
+        stream.wait_event(b["ev_xw"])
+        g.fp8_requantize_weights(b["wm"], K, N, T, D, wst, wq, wqT)
+        g.fp8_linear_fwd(b["x"], M, K, N, wqT, wst, None, xst, T, D, xq, xqT, None, b["y"])
+        b["ev_fwd"].record(stream)
+        stream.wait_event(b["ev_dy"])
+        g.fp8_linear_bwd_ws(b["dy"], M, K, N, xqT, xst, wq, wst, gst, D, dyq, dyqT, b["dx"], b["dw"], ws, wsb)
         g.fp8_history_commit_many([wst, xst, gst])
-        ev_bwd.record(stream)
-        s_out.wait_event(ev_bwd)
+        b["ev_done"].record(stream)
+        s_out.wait_event(b["ev_fwd"])
         with torch.cuda.stream(s_out):
-            dxh.copy_(dx, non_blocking=True)
-            dwh.copy_(dw, non_blocking=True)
+            b["yh"].copy_(b["y"], non_blocking=True)
+        s_out.wait_event(b["ev_done"])
+        with torch.cuda.stream(s_out):
+            b["dxh"].copy_(b["dx"], non_blocking=True)
+            b["dwh"].copy_(b["dw"], non_blocking=True)
+            b["ev_out"].record(s_out)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -423,6 +431,8 @@ def run_e2e(g, torch, x_h, w_h, dy_h, stream, steps, step_flops):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
         for _ in range(steps):
             one()
         stream.wait_stream(s_out)  # the last step's results are on the host
