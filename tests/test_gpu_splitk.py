@@ -151,3 +151,46 @@ def test_grouped_rejections(g):
         g.fp8_scaled_mm_grouped([ok, ok, ok])
     assert e.value.status == g.FP8_ERR_INVALID_ARG
     g.fp8_poll_device_error()
+
+
+GROUP_CASES = [
+    # (M, N, K, fa, fb) x 2: single CTAs (a problem with M <= 128), ragged N and K
+    ((96, 520, 1000, 0, 1), (640, 200, 336, 1, 0)),
+    # CTA pairs, units of very different lengths (explicit schedule)
+    ((512, 512, 8192, 0, 0), (1024, 256, 256, 1, 0)),
+    # CTA pairs, units of one length (round robin)
+    ((512, 768, 1024, 0, 1), (768, 512, 1024, 1, 0)),
+]
+
+
+@pytest.mark.parametrize("pa,pb", GROUP_CASES)
+def test_grouped_shapes_against_exact(g, pa, pb):
+    rng = np.random.default_rng(pa[0] + pb[2])
+    probs, refs, outs, keep = [], [], [], []
+    for M, N, K, fa, fb in (pa, pb):
+        A = rand_codes(rng, (M, K), FMT[fa], 25.0)
+        B = rand_codes(rng, (N, K), FMT[fb], 25.0)
+        da, db = np.float32(rng.uniform(0.001, 0.05)), np.float32(rng.uniform(0.001, 0.05))
+        lda = ldb = -(-K // 16) * 16
+        ldc = -(-N // 8) * 8
+        Ad = torch.zeros(M, lda, dtype=torch.uint8, device="cuda")
+        Ad[:, :K] = dev_u8(A)
+        Bd = torch.zeros(N, ldb, dtype=torch.uint8, device="cuda")
+        Bd[:, :K] = dev_u8(B)
+        C = torch.full((M, ldc), float("nan"), dtype=torch.bfloat16, device="cuda")
+        sa, sb = f32_scalar(da), f32_scalar(db)
+        keep.append((Ad, Bd, sa, sb))
+        outs.append((C, N))
+        probs.append(g.mm_problem(Ad, fa, Bd, fb, M, N, K, lda, ldb, sa, sb, C, ldc))
+        refs.append(gemm.scaled_mm(A, FMT[fa], B, FMT[fb], da, db)[:2])
+    nbytes = g.fp8_scaled_mm_grouped_workspace_bytes(probs)
+    ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    for w, nb in ((ws, nbytes), (None, 0)):
+        for C, _ in outs:
+            C.fill_(float("nan"))
+        g.fp8_scaled_mm_grouped(probs, w, nb)
+        torch.cuda.synchronize()
+        for (C, N), (ref, mag) in zip(outs, refs):
+            assert_close(host_bf16_f64(C)[:, :N], ref, mag)
+            assert np.isnan(host_bf16_f64(C)[:, N:]).all()  # padding columns untouched
+    g.fp8_poll_device_error()
