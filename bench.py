@@ -588,19 +588,15 @@ def run_delayed_loop(g, torch, fp8_peak, layers=12, steps=50, tokens=32768, d=15
     wq, wqT = [u8(d, n) for _ in range(layers)], [u8(n, d) for _ in range(layers)]
     xq, xqT, dyq, dyqT = u8(tokens, d), u8(d, tokens), u8(tokens, n), u8(n, tokens)
     y, dx, dw = bf(tokens, n), bf(tokens, d), bf(d, n)
-    wsb = max(g.fp8_scaled_mm_workspace_bytes(*sh) for sh in ((tokens, n, d), (tokens, d, n), (d, n, tokens)))
+    wsb = g.fp8_linear_bwd_workspace_bytes(tokens, d, n)
     ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
     D, T = g.FP8_SCALE_DELAYED, g.FP8_GRAN_TENSOR
 
-    def layer_step(l):
-        ws_, xs, gs = st[l]
+    def layer_step(l):  # the layer API: 6 launches (update + requantise, x cast, forward GEMM,
+        ws_, xs, gs = st[l]  # dy cast, grouped dgrad + wgrad, history commit)
         g.fp8_update_requantize_weights(W[l], delta[l], d, n, D, ws_, wq[l], wqT[l])
-        g.fp8_quantize(x, tokens, d, d, g.FP8_E4M3, T, D, xs, xq, xqT)
-        g.fp8_scaled_mm_ws(xq, 0, wqT[l], 0, tokens, n, d, d, d, T, xs.scale_inv, ws_.scale_inv, y, n, ws, wsb)
-        g.fp8_quantize(dy, tokens, n, n, g.FP8_E5M2, T, D, gs, dyq, dyqT)
-        g.fp8_scaled_mm_ws(dyq, 1, wq[l], 0, tokens, d, n, n, n, T, gs.scale_inv, ws_.scale_inv, dx, d, ws, wsb)
-        g.fp8_scaled_mm_ws(xqT, 0, dyqT, 1, d, n, tokens, tokens, tokens, T, xs.scale_inv, gs.scale_inv, dw, n,
-                           ws, wsb)
+        g.fp8_linear_fwd(x, tokens, d, n, wqT[l], ws_, None, xs, T, D, xq, xqT, None, y)
+        g.fp8_linear_bwd_ws(dy, tokens, d, n, xqT, xs, wq[l], ws_, gs, D, dyq, dyqT, dx, dw, ws, wsb)
         g.fp8_history_commit_many([ws_, xs, gs])
 
     for l in range(layers):  # untimed first step (bootstrap casts)
@@ -620,7 +616,7 @@ def run_delayed_loop(g, torch, fp8_peak, layers=12, steps=50, tokens=32768, d=15
     print(json.dumps({"sweep": "delayed_loop", "layers": layers, "steps_timed": steps - 1, "tokens": tokens, "d": d,
                       "ms_total": round(ms, 3), "ms_per_layer_step": round(ms / (layers * (steps - 1)), 4),
                       "TFLOP/s": round(tf, 1), "frac_fp8_peak": round(tf / fp8_peak, 4),
-                      "launches_per_layer_step": 7, "overflow_counts_total": ov}))
+                      "launches_per_layer_step": 6, "overflow_counts_total": ov}))
 
 
 # --------------------------------------------------------------------------------------
