@@ -966,6 +966,7 @@ void make_schedule(KParams& p, int slots) {
       sc.off.push_back(static_cast<uint16_t>(off));
       sc.len = off;
     }
+    if (cache.size() >= 256) cache.clear();  // bounded: a workload uses a handful of shapes
     it = cache.emplace(key, std::move(sc)).first;
   }
   const Sched& sc = it->second;
@@ -1160,6 +1161,7 @@ GroupPlan plan_group(const GemmArgs& g0, const GemmArgs& g1, int64_t ws_limit) {
       }
     }
   }
+  if (cache.size() >= 256) cache.clear();  // bounded: a workload uses a handful of shapes
   cache.emplace(key, best);
   return best;
 }
