@@ -110,26 +110,38 @@ class Clocks:
 # --------------------------------------------------------------------------------------
 # GPU arm
 # --------------------------------------------------------------------------------------
+# The sources that decide each stage's kernel and launch (kernel body, its headers, the
+# host code that picks and launches it): a stage's DRAM counters stay valid while these hash
+# the same as when the counters were taken.
+_CAST_SOURCES = ("quant.cu", "cast.cuh", "ptx.cuh", "kernels.h", "api.cu")
+_GEMM_SOURCES = ("gemm.cu", "cast.cuh", "ptx.cuh", "kernels.h", "api.cu")
+STAGE_SOURCES = {"requant_w": _CAST_SOURCES, "quant_x": _CAST_SOURCES, "quant_dy": _CAST_SOURCES,
+                 "gemm_fwd": _GEMM_SOURCES, "gemm_bwd": _GEMM_SOURCES}
+
+
 def traffic_table():
     """Per-launch DRAM bytes from the committed ncu summary, keyed by stage, valid only
-    while the kernel sources hash the same as when the counters were taken."""
+    while the stage's kernel sources hash the same as when the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic_per_launch.txt")
     out = {}
     if not os.path.exists(path):
         return out
-    h = source_hash()
     for line in open(path):
         line = line.split("#")[0].split()
-        if len(line) == 3 and line[2] == h:
+        if len(line) == 3 and line[0] in STAGE_SOURCES and line[2] == source_hash(STAGE_SOURCES[line[0]]):
             out[line[0]] = float(line[1])
     return out
 
 
-def source_hash():
+def source_hash(files, read=None):
+    """First 16 hex digits of the SHA-256 of the named csrc files, in order. `read` maps a
+    file name to its bytes (default: the working tree)."""
     d = os.path.join(ROOT, "fp8_mixed_precision_saturating_gb300", "csrc")
+    read = read or (lambda f: open(os.path.join(d, f), "rb").read())
     hsh = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        hsh.update(open(os.path.join(d, f), "rb").read())
+    for f in files:
+        hsh.update(f.encode() + b"\0")
+        hsh.update(read(f))
     return hsh.hexdigest()[:16]
 
 

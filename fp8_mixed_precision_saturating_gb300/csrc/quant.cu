@@ -211,6 +211,33 @@ __device__ __forceinline__ int64_t first_tile(int64_t t0) {
   return t0 + r;
 }
 
+// The history count and the window maximum of effective_amax, read by a whole warp in one
+// round trip: lane i loads entry i (i + 32, ... for windows longer than 32) together with the
+// count, and entries at or past the count are masked afterwards. Per entry, fmaxf(h, 0) with
+// the sign cleared is what effective_amax folds in (NaN and negative entries count as 0), and
+// the maximum of non-negative floats is the maximum of their bit patterns. Delayed scaling only
+// (the history may be absent otherwise); every lane of the warp calls it.
+struct HistoryView {
+  int n;       // entries pushed so far
+  float amax;  // maximum over the first min(n, hist_len) entries, 0 when n == 0
+};
+
+__device__ __forceinline__ HistoryView read_history_warp(const QuantState& st) {
+  const int lane = threadIdx.x & 31;
+  const int n = *st.hist_count;
+  uint32_t best = 0;
+  for (int base = 0; base < st.hist_len; base += 32) {
+    const int i = base + lane;
+    const float h = i < st.hist_len ? st.hist[i] : 0.0f;
+    const uint32_t b = __float_as_uint(fmaxf(h, 0.0f)) & 0x7FFFFFFFu;
+    if (i < n) best = max(best, b);
+  }
+  HistoryView v;
+  v.n = n;
+  v.amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, best));
+  return v;
+}
+
 // Tiled layout: rows, cols and ld multiples of 8 (rows of 16 with qT); q and/or qT. With
 // UPD the tensor is first updated in place by delta (the weight-cache refresh fused with
 // the optimizer step): in the amax pass when there is one, else in the cast pass, so W and
@@ -288,13 +315,28 @@ __global__ void __launch_bounds__(kThreads, 4) quant_tiles_many_kernel(const __g
   __shared__ __align__(128) uint8_t tT[2][128 * 128];  // alternating transpose buffers
   __shared__ uint32_t red[2 * kThreads / 32];
   __shared__ uint32_t s_max[kMaxJobs];
+  __shared__ int s_hn[kMaxJobs];      // history counts
+  __shared__ float s_ha[kMaxJobs];    // history window maxima
   int it = 0;  // tiles written by this CTA (picks the transpose buffer)
   cg::grid_group grid = cg::this_grid();
   pdl_trigger();  // the next kernel may start its prologue as this one drains
-  uint32_t passmask = 0;
+  {  // every job's scaling state in one round trip: warp j reads job j's history
+    const int w = threadIdx.x >> 5;
+    if (w < J.n) {
+      const TileJob& jb = J.j[w];
+      HistoryView h{0, 0.0f};
+      if (jb.delayed) h = read_history_warp(jb.st);
+      if ((threadIdx.x & 31) == 0) {
+        s_hn[w] = h.n;
+        s_ha[w] = h.amax;
+      }
+    }
+  }
+  __syncthreads();
+  uint32_t passmask = 0;  // jobs that need their own amax first (needs_amax_pass)
 #pragma unroll
   for (int j = 0; j < kMaxJobs; ++j)
-    if (j < J.n && needs_amax_pass(J.j[j].st, J.j[j].delayed)) passmask |= 1u << j;
+    if (j < J.n && (!J.j[j].delayed || s_hn[j] == 0)) passmask |= 1u << j;
   if (blockIdx.x == 0 && threadIdx.x < J.n) *J.j[threadIdx.x].st.amax_cur = 0.0f;
   if (passmask) {
 #pragma unroll
@@ -331,14 +373,14 @@ __global__ void __launch_bounds__(kThreads, 4) quant_tiles_many_kernel(const __g
     if (first_tile(jb.tile0) >= jb.tile0 + jb.ntiles) {  // no tile of this job here
       if (blockIdx.x == 0 && threadIdx.x == 0) {        // (CTA 0 still publishes the scale)
         float sj, dj;
-        scales_from_amax(call_amax(jb.st, jb.delayed), Fmt<FMT>::kMax, sj, dj);
+        scales_from_amax(pass ? *jb.st.amax_cur : s_ha[j], Fmt<FMT>::kMax, sj, dj);
         *jb.st.scale = sj;
         *jb.st.scale_inv = dj;
       }
       continue;
     }
-    float sj, dj;
-    scales_from_amax(call_amax(jb.st, jb.delayed), Fmt<FMT>::kMax, sj, dj);
+    float sj, dj;  // call_amax: the amax pass's result, else the history maximum
+    scales_from_amax(pass ? *jb.st.amax_cur : s_ha[j], Fmt<FMT>::kMax, sj, dj);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
       *jb.st.scale = sj;
       *jb.st.scale_inv = dj;
