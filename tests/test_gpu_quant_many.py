@@ -79,6 +79,30 @@ def test_many_delayed_steps_with_commits(g):
     g.fp8_poll_device_error()
 
 
+def test_many_history_window_longer_than_a_warp(g):
+    """A 40-entry window (the history is read one entry per lane, 32 lanes): before the ring
+    wraps only the first `count` entries count; after it wraps all 40 do, and the largest
+    entry (step 3's) leaves the window when step 43's amax overwrites it."""
+    hist = 40
+    sts = [g.TensorState(hist), g.TensorState(hist)]
+    osts = [quant.DelayedState(hist), quant.DelayedState(hist)]
+    for t in range(46):
+        scale = 32.0 if t == 3 else 2.0 ** ((t % 5) - 2)
+        xs = [bf16_bits_from_f32(quant.widen_bf16(normal_bf16(200 + t, (64, 256))) * np.float32(scale)),
+              bf16_bits_from_f32(quant.widen_bf16(normal_bf16(300 + t, (128, 128), 0.02)) * np.float32(scale))]
+        jobs, keep = zip(*[make_job(g, x, 0, g.FP8_SCALE_DELAYED, st) for x, st in zip(xs, sts)])
+        g.fp8_quantize_many(list(jobs))
+        refs = [o.quantize(x, fp8.E4M3, delayed=True) for x, o in zip(xs, osts)]
+        if t in (0, 1, 2, 4, 31, 32, 33, 39, 40, 41, 43, 44, 45):
+            torch.cuda.synchronize()
+            for st, ref, o, (_, q, qT) in zip(sts, refs, osts, keep):
+                check(st, ref, q, qT, o.snapshot())
+        g.fp8_history_commit_many(sts)
+        for o in osts:
+            o.commit()
+    g.fp8_poll_device_error()
+
+
 def test_many_mixed_formats_run_one_by_one(g):
     xs = [normal_bf16(4, (256, 256)), normal_bf16(5, (128, 64))]
     sts = [g.TensorState(), g.TensorState()]
