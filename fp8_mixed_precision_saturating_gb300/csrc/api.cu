@@ -102,6 +102,9 @@ using namespace fp8gb;
 
 namespace {
 
+// 128 x 128 tiles of a [rows, cols] tensor (the tiled kernels index them in 32 bits).
+int64_t tile_count(int64_t rows, int64_t cols) { return ((rows + 127) / 128) * ((cols + 127) / 128); }
+
 fp8_status_t validate_common(const void* x, int64_t rows, int64_t cols, int64_t ld, int fmt, const char* who) {
   if (rows < 0 || cols < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
   if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_INVALID_ARG, "%s: unknown format %d", who, fmt);
@@ -134,6 +137,7 @@ fp8_status_t quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld
       return fail(FP8_ERR_UNSUPPORTED, "%s: this layout needs rows, cols and ld multiples of 8", who);
     if (qT != nullptr && rows % 16 != 0)
       return fail(FP8_ERR_UNSUPPORTED, "%s: the transposed output needs rows %% 16 == 0", who);
+    if (tile_count(rows, cols) > INT32_MAX) return fail(FP8_ERR_UNSUPPORTED, "%s: more than 2^31 tiles", who);
   }
   const QuantState qs = to_qs(st);
   cudaError_t e = cudaSuccess;
@@ -220,6 +224,7 @@ fp8_status_t fp8_quantize_many(const fp8_quant_job_t* jobs, int32_t n, void* str
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (n < 1 || n > kMaxJobs || jobs == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: 1 to %d jobs", who, kMaxJobs);
   bool fused = true;
+  int64_t total_tiles = 0;
   for (int i = 0; i < n; ++i) {
     const fp8_quant_job_t& jb = jobs[i];
     if (jb.st == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: job %d: state is required", who, i);
@@ -232,8 +237,9 @@ fp8_status_t fp8_quantize_many(const fp8_quant_job_t* jobs, int32_t n, void* str
     if ((st = check_state(jb.st, jb.mode, who)) != FP8_OK) return st;
     fused = fused && jb.fmt == jobs[0].fmt && jb.qT_out != nullptr && jb.rows > 0 && jb.cols > 0 && jb.rows % 16 == 0 &&
             jb.cols % 8 == 0 && jb.ld % 8 == 0 && aligned16(jb.x_bf16) && aligned16(jb.q_out) && aligned16(jb.qT_out);
+    total_tiles += tile_count(jb.rows, jb.cols);
   }
-  if (!fused || n == 1) {
+  if (!fused || n == 1 || total_tiles > INT32_MAX) {  // one launch per job (each checked alone)
     for (int i = 0; i < n; ++i) {
       const fp8_quant_job_t& jb = jobs[i];
       const fp8_status_t st = quantize_impl(jb.x_bf16, jb.rows, jb.cols, jb.ld, jb.fmt, FP8_GRAN_TENSOR, jb.mode, jb.st,
@@ -362,6 +368,7 @@ fp8_status_t fp8_update_requantize_weights(void* w_master_bf16, const float* del
   if (K % 8 != 0 || N % 8 != 0 || (wqT_nk != nullptr && K % 16 != 0))
     return fail(FP8_ERR_UNSUPPORTED, "%s: K and N must be multiples of 8 (K of 16 with wqT)", who);
   if (K > (1ll << 31) || N > (1ll << 31)) return fail(FP8_ERR_UNSUPPORTED, "%s: dimension beyond 2^31", who);
+  if (tile_count(K, N) > INT32_MAX) return fail(FP8_ERR_UNSUPPORTED, "%s: more than 2^31 tiles", who);
   cudaError_t e = launch_update_quant_tensor(mode == FP8_SCALE_DELAYED, w_master_bf16, delta, K, N, wq_kn, wqT_nk,
                                              to_qs(st), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FP8_OK : cuda_fail(e, who);

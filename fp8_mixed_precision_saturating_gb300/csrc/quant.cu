@@ -205,10 +205,9 @@ __device__ __forceinline__ void update_patch(uint16_t* __restrict__ x, const flo
 }
 
 // The first tile index >= t0 that this CTA owns (tiles are dealt out t = blockIdx.x mod grid).
-__device__ __forceinline__ int64_t first_tile(int64_t t0) {
-  const int64_t g = gridDim.x;
-  const int64_t r = (static_cast<int64_t>(blockIdx.x) - t0 % g + g) % g;
-  return t0 + r;
+__device__ __forceinline__ uint32_t first_tile(uint32_t t0) {
+  const uint32_t g = gridDim.x;
+  return t0 + (blockIdx.x + g - t0 % g) % g;
 }
 
 // The history count and the window maximum of effective_amax, read by a whole warp in one
@@ -252,16 +251,19 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(uint16_t* 
   cg::grid_group grid = cg::this_grid();
   pdl_trigger();  // the next kernel may start its prologue as this one drains
   int it = 0;     // tiles written by this CTA (picks the transpose buffer)
-  const int64_t tiles_x = (cols + 127) / 128;
-  const int64_t ntiles = tiles_x * ((rows + 127) / 128);
+  // tile indices in 32 bits (the host keeps a tensor below 2^31 tiles): a 64-bit division
+  // is a long subroutine, and the first one stands between the CTA's start and its first load
+  const uint32_t tiles_x = static_cast<uint32_t>((cols + 127) / 128);
+  const uint32_t ntiles = tiles_x * static_cast<uint32_t>((rows + 127) / 128);
   const bool pass = needs_amax_pass(st, delayed);
   if (blockIdx.x == 0 && threadIdx.x == 0) *st.amax_cur = 0.0f;
   if (pass) {
     uint32_t m = 0;
-    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const uint32_t ty = t / tiles_x, tx = t - ty * tiles_x;
       uint4 v[8];
-      const bool in = load_patch(x, rows, cols, ld, t / tiles_x, t % tiles_x, v);
-      if constexpr (UPD) update_patch(x, delta, cols, ld, t / tiles_x, t % tiles_x, in, v);
+      const bool in = load_patch(x, rows, cols, ld, ty, tx, v);
+      if constexpr (UPD) update_patch(x, delta, cols, ld, ty, tx, in, v);
 #pragma unroll
       for (int i = 0; i < 8; ++i) m = absmax_v(m, v[i]);
     }
@@ -278,8 +280,8 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(uint16_t* 
   }
   const Scaler sc = make_scaler<FMT>(s, d);
   uint32_t ov = 0, un = 0, m = 0;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const int64_t ty = t / tiles_x, tx = t % tiles_x;
+  for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const uint32_t ty = t / tiles_x, tx = t - ty * tiles_x;
     uint4 v[8];
     const bool in = load_patch(x, rows, cols, ld, ty, tx, v);
     if constexpr (UPD) {
@@ -344,12 +346,14 @@ __global__ void __launch_bounds__(kThreads, 4) quant_tiles_many_kernel(const __g
       if (threadIdx.x == 0) s_max[j] = 0;
       if (j >= J.n || !((passmask >> j) & 1u)) continue;
       const TileJob& jb = J.j[j];
-      if (first_tile(jb.tile0) >= jb.tile0 + jb.ntiles) continue;  // no tile of this job here
+      const uint32_t t0 = static_cast<uint32_t>(jb.tile0), t1 = t0 + static_cast<uint32_t>(jb.ntiles);
+      const uint32_t tx_n = static_cast<uint32_t>(jb.tiles_x);
+      if (first_tile(t0) >= t1) continue;  // no tile of this job here
       uint32_t m = 0;
-      for (int64_t t = first_tile(jb.tile0); t < jb.tile0 + jb.ntiles; t += gridDim.x) {
-        const int64_t lt = t - jb.tile0;
+      for (uint32_t t = first_tile(t0); t < t1; t += gridDim.x) {
+        const uint32_t lt = t - t0, ty = lt / tx_n;
         uint4 v[8];
-        load_patch(jb.x, jb.rows, jb.cols, jb.ld, lt / jb.tiles_x, lt % jb.tiles_x, v);
+        load_patch(jb.x, jb.rows, jb.cols, jb.ld, ty, lt - ty * tx_n, v);
 #pragma unroll
         for (int i = 0; i < 8; ++i) m = absmax_v(m, v[i]);
       }
@@ -370,7 +374,9 @@ __global__ void __launch_bounds__(kThreads, 4) quant_tiles_many_kernel(const __g
     const bool pass = (passmask >> j) & 1u;
     any_delayed |= !pass;
     if (threadIdx.x == 0) s_max[j] = 0;
-    if (first_tile(jb.tile0) >= jb.tile0 + jb.ntiles) {  // no tile of this job here
+    const uint32_t t0 = static_cast<uint32_t>(jb.tile0), t1 = t0 + static_cast<uint32_t>(jb.ntiles);
+    const uint32_t tx_n = static_cast<uint32_t>(jb.tiles_x);
+    if (first_tile(t0) >= t1) {  // no tile of this job here
       if (blockIdx.x == 0 && threadIdx.x == 0) {        // (CTA 0 still publishes the scale)
         float sj, dj;
         scales_from_amax(pass ? *jb.st.amax_cur : s_ha[j], Fmt<FMT>::kMax, sj, dj);
@@ -387,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 4) quant_tiles_many_kernel(const __g
     }
     const Scaler sc = make_scaler<FMT>(sj, dj);
     uint32_t ov = 0, un = 0, m = 0;
-    for (int64_t t = first_tile(jb.tile0); t < jb.tile0 + jb.ntiles; t += gridDim.x) {
-      const int64_t lt = t - jb.tile0, ty = lt / jb.tiles_x, tx = lt % jb.tiles_x;
+    for (uint32_t t = first_tile(t0); t < t1; t += gridDim.x) {
+      const uint32_t lt = t - t0, ty = lt / tx_n, tx = lt - ty * tx_n;
       uint4 v[8];
       const bool in = load_patch(jb.x, jb.rows, jb.cols, jb.ld, ty, tx, v);
       uint2 c[8];
