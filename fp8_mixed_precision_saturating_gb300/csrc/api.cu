@@ -158,6 +158,7 @@ fp8_status_t quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld
   }
   if (gran == FP8_GRAN_TILE_1x128) {
     if (cols % 128 != 0) return fail(FP8_ERR_UNSUPPORTED, "%s: 1x128 tiles need cols %% 128 == 0", who);
+    if (rows * (cols / 128) > INT32_MAX) return fail(FP8_ERR_UNSUPPORTED, "%s: more than 2^31 tiles", who);
     if (qT != nullptr) return fail(FP8_ERR_UNSUPPORTED, "%s: 1x128 tiles write no transposed copy", who);
     if (q == nullptr && n > 0) return fail(FP8_ERR_INVALID_ARG, "%s: q_out is required", who);
     if (n == 0) return FP8_OK;

@@ -538,18 +538,20 @@ __global__ void __launch_bounds__(kThreads) cast_1x128_kernel(const uint16_t* __
   __shared__ uint32_t red[2 * kThreads / 32];
   pdl_wait();
   pdl_trigger();
-  const int64_t tiles_per_row = cols / 128;
-  const int64_t ntiles = rows * tiles_per_row;
+  // tile indices in 32 bits (the host keeps a tensor below 2^31 tiles): a 64-bit division
+  // per tile is a long subroutine
+  const uint32_t tiles_per_row = static_cast<uint32_t>(cols / 128);
+  const uint32_t ntiles = static_cast<uint32_t>(rows) * tiles_per_row;
   const int gl = threadIdx.x & 3;  // lane within the tile's group
-  const int64_t group = (blockIdx.x * (int64_t)kThreads + threadIdx.x) >> 2;
-  const int64_t ngroups = ((int64_t)gridDim.x * kThreads) >> 2;
+  const uint32_t group = (blockIdx.x * kThreads + threadIdx.x) >> 2;
+  const uint32_t ngroups = (gridDim.x * kThreads) >> 2;
   uint32_t ov = 0, un = 0, mall = 0;
   // every lane of a warp runs the same number of iterations (the shuffles need it)
-  const int64_t warp_first = (group & ~int64_t(7));
-  for (int64_t base = warp_first; base < ntiles; base += ngroups) {
-    const int64_t tile = base + (group & 7);
+  const uint32_t warp_first = group & ~7u;
+  for (uint32_t base = warp_first; base < ntiles; base += ngroups) {
+    const uint32_t tile = base + (group & 7);
     const bool ok = tile < ntiles;
-    const int64_t r = ok ? tile / tiles_per_row : 0, tc = ok ? tile % tiles_per_row : 0;
+    const uint32_t r = ok ? tile / tiles_per_row : 0, tc = ok ? tile - r * tiles_per_row : 0;
     const uint16_t* src = x + r * ld + tc * 128;
     uint4 v[4];
 #pragma unroll
