@@ -166,6 +166,7 @@ fp8_status_t quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld
   } else {
     if (rows % 128 != 0 || cols % 128 != 0)
       return fail(FP8_ERR_UNSUPPORTED, "%s: 128x128 blocks need rows and cols multiples of 128", who);
+    if (rows / 128 > 65535) return fail(FP8_ERR_UNSUPPORTED, "%s: 128x128 blocks: more than 65535 block rows", who);
     if (n == 0) return FP8_OK;
     e = launch_cast_blocks(fmt, x, rows, cols, ld, q, qT, unit_si, qs, stream);
   }

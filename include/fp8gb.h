@@ -118,7 +118,8 @@ typedef struct {
  *    cols % 16 == 0 is needed by the GEMM, not by this call.
  *  Alignment: x, q_out and qT_out 16-byte aligned; ld % 8 == 0 unless ld == cols.
  *  Size: rows, cols <= 2^31; with qT_out, tile or block scales, fewer than 2^31 units of
- *  128 x 128 (1 x 128 for tile scales), else FP8_ERR_UNSUPPORTED. */
+ *  128 x 128 (1 x 128 for tile scales); block scales at most 65535 block rows. Beyond these,
+ *  FP8_ERR_UNSUPPORTED. */
 fp8_status_t fp8_quantize(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld,
                           fp8_format_t fmt, fp8_gran_t gran, fp8_scaling_t mode,
                           const fp8_tensor_state_t* st, void* q_out, void* qT_out,
