@@ -383,7 +383,8 @@ fp8_status_t fp8_linear_fwd(const void* x_bf16, int64_t M, int64_t K, int64_t N,
   const char* who = "fp8_linear_fwd";
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M < 0 || K < 0 || N < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
-  if (xq_save == nullptr || y_bf16 == nullptr || wqT_nk == nullptr)
+  // a buffer may be null only when it holds no elements (an empty token batch)
+  if ((xq_save == nullptr && M * K > 0) || (y_bf16 == nullptr && M * N > 0) || (wqT_nk == nullptr && N * K > 0))
     return fail(FP8_ERR_INVALID_ARG, "%s: xq_save, y and wqT are required", who);
   fp8_status_t st;
   if (gran == FP8_GRAN_TENSOR) {
@@ -457,8 +458,10 @@ fp8_status_t linear_bwd_impl(const void* dy_bf16, int64_t M, int64_t K, int64_t 
                              void* dw_bf16, void* ws, int64_t ws_bytes, cudaStream_t s, const char* who) {
   if (M < 0 || K < 0 || N < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
   if (M % 16 || K % 16 || N % 16) return fail(FP8_ERR_UNSUPPORTED, "%s: M, K and N must be multiples of 16", who);
-  if (dyq_ws == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: dyq_ws is required", who);
-  if (dw_bf16 != nullptr && (dyqT_ws == nullptr || xqT_save == nullptr || x_st == nullptr || !x_st->scale_inv))
+  // a buffer may be null only when it holds no elements (an empty token batch)
+  if (dyq_ws == nullptr && M * N > 0) return fail(FP8_ERR_INVALID_ARG, "%s: dyq_ws is required", who);
+  if (dw_bf16 != nullptr && ((dyqT_ws == nullptr && M * N > 0) || (xqT_save == nullptr && M * K > 0) ||
+                             x_st == nullptr || !x_st->scale_inv))
     return fail(FP8_ERR_INVALID_ARG, "%s: wgrad needs dyqT_ws, xqT_save and x_st", who);
   if (dx_bf16 != nullptr && (wq_kn == nullptr || w_st == nullptr || !w_st->scale_inv))
     return fail(FP8_ERR_INVALID_ARG, "%s: dgrad needs wq_kn and w_st", who);

@@ -271,7 +271,8 @@ fp8_status_t fp8_update_requantize_weights(void* w_master_bf16, const float* del
  *  128x128 W blocks) uses w_block_scale_inv [K/128, N/128] and requires mode CURRENT.
  *  xqT_save [K,M] (nullable, gran TENSOR only) keeps the transposed codes for wgrad.
  *  x contiguous; K % 16 == 0 (K % 128 == 0 for gran BLOCK); M % 16 == 0 with xqT_save.
- *  x_st is required for gran TENSOR and optional otherwise. */
+ *  x_st is required for gran TENSOR and optional otherwise. An empty token batch (M == 0)
+ *  is valid: x, xq_save and y may then be NULL, nothing is written but x_st's unit scales. */
 fp8_status_t fp8_linear_fwd(const void* x_bf16, int64_t M, int64_t K, int64_t N,
                             const void* wqT_nk, const fp8_tensor_state_t* w_st,
                             const float* w_block_scale_inv, const fp8_tensor_state_t* x_st,
@@ -285,7 +286,8 @@ fp8_status_t fp8_linear_fwd(const void* x_bf16, int64_t M, int64_t K, int64_t N,
  *    dgrad  dx [M,K] = d_dy d_w  dyq  wq_kn^T      (contraction over N; wq_kn [K,N])
  *    wgrad  dW [K,N] = d_x  d_dy xqT_save dyqT_ws^T (contraction over M; xqT_save [K,M])
  *  dx and dw may each be NULL (that GEMM is skipped; dyqT_ws may then be NULL when dw is).
- *  Needs M, N, K multiples of 16. dy contiguous. */
+ *  Needs M, N, K multiples of 16. dy contiguous. An empty token batch (M == 0) is valid:
+ *  dy, the scratch, xqT_save and dx may then be NULL, and dW is written as zeros. */
 fp8_status_t fp8_linear_bwd(const void* dy_bf16, int64_t M, int64_t K, int64_t N,
                             const void* xqT_save, const fp8_tensor_state_t* x_st,
                             const void* wq_kn, const fp8_tensor_state_t* w_st,

@@ -88,6 +88,32 @@ def test_forward_backward_small(g, M, K, N):
     assert_close(host_bf16_f64(s.dw), dw, mdw)
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+def test_empty_token_batch(g, mode):
+    """M = 0 (a batch, or an expert, with no tokens): the layer calls accept empty buffers as
+    null pointers, the forward writes nothing, the weight gradient of no tokens is zero and
+    the x and dy states get unit scales and a zero amax."""
+    K, N = 256, 512
+    w = normal_bf16(9, (K, N), 0.02)
+    wd = dev_bf16(w)
+    wst, xst, gst = g.TensorState(), g.TensorState(), g.TensorState()
+    wq, wqT = empty_u8(K, N), empty_u8(N, K)
+    g.fp8_requantize_weights(wd, K, N, g.FP8_GRAN_TENSOR, mode, wst, wq, wqT)
+    xst.scale.fill_(5.0)
+    gst.scale.fill_(5.0)
+    g.fp8_linear_fwd(None, 0, K, N, wqT, wst, None, xst, g.FP8_GRAN_TENSOR, mode, None, None, None, None)
+    dx = torch.empty(0, K, dtype=torch.bfloat16, device="cuda")
+    dw = torch.full((K, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    g.fp8_linear_bwd(None, 0, K, N, None, xst, wq, wst, gst, mode, None, None, dx, dw)
+    torch.cuda.synchronize()
+    g.fp8_poll_device_error()
+    assert (dw.float() == 0).all()
+    for st in (xst, gst):
+        snap = st.snapshot()
+        assert snap["scale"] == 1.0 and snap["scale_inv"] == 1.0 and snap["amax_cur"] == 0.0
+        assert snap["overflow"] == 0 and snap["underflow"] == 0
+
+
 def test_tiny_forward_workload_in_full(g):
     w = workload_inputs("tiny_fwd")
     M, K, N = w["M"], w["K"], w["N"]
