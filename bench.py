@@ -37,8 +37,9 @@ METRIC = "FP8 up-proj GEMM TFLOP/s (% FP8 peak); quantize-cast GB/s (% HBM)"
 M, K, N = 8192, 768, 3072
 HIST = 16
 FLUSH_BYTES = 256 << 20
-# Peaks on this machine (measured): HBM copy GB/s and dense bf16 TFLOP/s (burst); the FP8
-# dense peak is the bf16 figure times the nominal fp8/bf16 ratio 4.5 / 2.25 = 2.
+# Roofline denominators: HBM copy GB/s and dense bf16 TFLOP/s (burst) from MEASURED_PEAKS.json,
+# else these earlier GB300 measurements; the FP8 dense peak is the bf16 figure times the
+# nominal fp8/bf16 ratio 4.5 / 2.25 = 2.
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
 
