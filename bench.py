@@ -548,9 +548,12 @@ def run_sweep(args):
             fn = lambda: g.fp8_scaled_mm_ws(A, fa, B, fb, m, n, k, k, k, gran, sa, sb, C, n, ws, wsb)
         ms = timed(fn, args.steps)
         tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
-        print(json.dumps({"sweep": "gemm", "name": name, "M": m, "N": n, "K": k, "block_scaled": blk,
-                          "split_k_workspace": wsb, "ms": round(ms, 5), "TFLOP/s": round(tf, 1),
-                          "frac_fp8_peak": round(tf / fp8_peak, 4)}))
+        out = {"sweep": "gemm", "name": name, "M": m, "N": n, "K": k, "block_scaled": blk,
+               "split_k_workspace": wsb, "ms": round(ms, 5), "TFLOP/s": round(tf, 1),
+               "frac_fp8_peak": round(tf / fp8_peak, 4)}
+        if not blk:  # context: the vendor library's FP8 GEMM (the pages' torch._scaled_mm) on the same shape
+            out["torch_scaled_mm"] = library_scaled_mm(torch, timed, A, fa, B, fb, m, n, k)
+        print(json.dumps(out))
         del A, B, C
     for name, r, c, fmt, gran, tr in SWEEP_CASTS:
         if only and name not in only:
@@ -589,6 +592,19 @@ def run_sweep(args):
     if only is None or "delayed_loop" in only:
         run_delayed_loop(g, torch, fp8_peak)
     g.fp8_poll_device_error()
+
+
+def library_scaled_mm(torch, timed, A, fa, B, fb, m, n, k):
+    """torch._scaled_mm (cuBLASLt) on the same codes, per-tensor unit scales, bf16 output,
+    timed like the sweep's own GEMMs; a comparison figure, not part of the library."""
+    dt = {0: torch.float8_e4m3fn, 1: torch.float8_e5m2}
+    try:
+        a, b = A.view(dt[fa]), B.view(dt[fb])
+        one = torch.ones((), device="cuda")
+        ms = timed(lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16), 15)
+        return {"ms": round(ms, 5), "TFLOP/s": round(2.0 * m * n * k / (ms * 1e-3) / 1e12, 1)}
+    except Exception as e:  # a format pair or shape the library does not take
+        return {"unavailable": str(e).splitlines()[0][:120]}
 
 
 def sweep_fused(g, torch, name, timed, codes, hbm, fp8_peak, steps):
