@@ -560,8 +560,9 @@ int64_t fp8_scaled_mm_grouped_workspace_bytes(const fp8_mm_problem_t* problems, 
 // ---------------------------------------------------------------------------------------
 // The backward casts dy to E5M2 twice (row-major for dgrad, transposed for wgrad) before the
 // two GEMMs read the codes. fp8_linear_bwd takes those two buffers from the caller; this
-// array stands in for them. It is part of the loaded library image, so every GPU that loads
-// the library holds these 64 MiB until the process exits, whether or not it is used.
+// array stands in for them. It lives in this file's device module beside the error word, so
+// a device holds these 64 MiB from the first call that loads the module there (any GEMM
+// launch or this entry point, under lazy loading) until the process exits.
 static constexpr size_t kBwdScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) uint8_t g_bwd_scratch[kBwdScratchBytes];
 

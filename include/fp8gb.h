@@ -321,8 +321,12 @@ int64_t fp8_linear_bwd_workspace_bytes(int64_t M, int64_t K, int64_t N);
  *   - size limit: M*N bytes when dw_bf16 is NULL, else M*N rounded up to 256 plus M*N
  *     bytes, at most 64 MiB (e.g. M*N <= 32 Mi elements with wgrad); larger shapes return
  *     FP8_ERR_UNSUPPORTED before anything is enqueued;
- *   - the array is part of the loaded library: every GPU that loads the library holds the
- *     64 MiB until the process exits;
+ *   - the array is part of the library's device code, so a device holds its 64 MiB from
+ *     the moment that code is loaded there until the process exits. With CUDA's lazy
+ *     module loading (the default) that is the first library call on the device that needs
+ *     it -- for example any call that launches a GEMM, fp8_poll_device_error, or this one --
+ *     and not only a call of this entry point; with eager loading it is context creation. That load fails with a
+ *     CUDA out-of-memory error (FP8_ERR_CUDA) on a device with less than 64 MiB free;
  *   - the first call on a device looks up the array's device address (cudaGetSymbolAddress)
  *     with that device current and caches it; make that first call before any stream capture;
  *   - all calls share one array, so calls whose work overlaps on the GPU (different streams,

@@ -3,12 +3,17 @@
 Bit-exact against the oracle on integer-valued products (every output is an integer below
 256 in magnitude, so the bf16 output is exact and the oracle quantises the same values
 independently): codes, amax, scale and counters with a delayed history (the fused epilogue)
-and with an empty history (the bootstrap cast). On random data the fused codes and state
-also equal fp8_quantize of the kernel's own bf16 output with the same delayed state."""
+and with an empty history (the bootstrap cast). At the delayed loop's forward shape
+(32768 x 6144, contraction 1536) on its real operands: the codes, amax, scales and counters
+against the oracle's delayed quantise of the kernel's own bf16 output (bootstrap, fused, and
+fused with a history that saturates), the bf16 output on sampled entries against the exact
+reference. On random data the fused codes and state also equal fp8_quantize of the kernel's
+own bf16 output with the same delayed state."""
 import numpy as np
 import pytest
 import torch
 
+from datagen import normal_bf16
 from oracle import fp8, gemm, quant
 
 from gpu_util import dev_u8, empty_u8, host_u8, host_bf16_f64
@@ -102,3 +107,63 @@ def test_fused_rejections(g):
     with pytest.raises(g.Fp8Error) as e:  # N must be a multiple of 16
         g.fp8_scaled_mm_quant(A, 0, A, 0, 16, 24, 32, 32, 32, one(1.0), one(1.0), C, 24, 0, st, Cq)
     assert e.value.status == g.FP8_ERR_ALIGNMENT
+
+
+def same_quant(snap, o, count):
+    assert np.float32(snap["amax_cur"]) == o["amax"]
+    assert np.float32(snap["scale"]) == o["s"] and np.float32(snap["scale_inv"]) == o["d"]
+    assert snap["count"] == count
+
+
+@pytest.mark.slow
+def test_fused_epilogue_against_oracle_at_the_loop_forward_shape(g):
+    """The delayed loop's forward: x [32768 x 1536] and W [1536 x 6144] (their seeds) cast per
+    tensor to E4M3 by the oracle, the GEMM's output cast to E4M3 in its epilogue."""
+    M, K, N = 32768, 1536, 6144
+    ox = quant.quantize_tensor(normal_bf16(5000, (M, K)), fp8.E4M3)
+    ow = quant.quantize_tensor(normal_bf16(5100, (K, N), 0.02), fp8.E4M3)
+    A, B = dev_u8(ox["q"]), dev_u8(ow["qT"])
+    da, db = one(ox["d"]), one(ow["d"])
+    st, ost = g.TensorState(hist_len=16), quant.DelayedState(16)
+
+    def call():
+        C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        Cq = empty_u8(M, N)
+        g.fp8_scaled_mm_quant(A, 0, B, 0, M, N, K, K, K, da, db, C, N, 0, st, Cq)
+        torch.cuda.synchronize()
+        g.fp8_poll_device_error()
+        return C, Cq
+
+    # 1. bootstrap (empty history): the output is cast from its own amax
+    C, Cq = call()
+    cbits = C.view(torch.int16).cpu().numpy().view(np.uint16)
+    rng = np.random.default_rng(17)
+    r, c = rng.integers(0, M, 4096), rng.integers(0, N, 4096)
+    ref, mag = gemm.scaled_mm_sampled(ox["q"], fp8.E4M3, ow["qT"], fp8.E4M3, ox["d"], ow["d"], r, c)
+    ok = gemm.within_bound(host_bf16_f64(C)[r, c], ref, mag)
+    assert ok.all(), f"{(~ok).sum()} outputs outside the bound"
+    o = ost.quantize(cbits, fp8.E4M3, delayed=True)
+    assert np.array_equal(host_u8(Cq), o["q"])
+    same_quant(st.snapshot(), o, 0)
+    assert st.snapshot()["overflow"] == o["overflow"] == 0 and st.snapshot()["underflow"] == o["underflow"]
+    # 2. the fused epilogue with the history [amax of step 1]: the same scale, so the same codes
+    g.fp8_history_commit(st)
+    ost.commit()
+    C2, Cq2 = call()
+    assert torch.equal(C2.view(torch.int16), C.view(torch.int16))
+    o2 = ost.quantize(cbits, fp8.E4M3, delayed=True)
+    assert np.array_equal(host_u8(Cq2), o2["q"])
+    snap = st.snapshot()
+    same_quant(snap, o2, 1)
+    assert snap["overflow"] == ost.overflow and snap["underflow"] == ost.underflow
+    # 3. a history whose maximum is an eighth of the output's amax: the tails saturate
+    small = np.float32(o["amax"] / 8)
+    st.amax_history[0] = float(small)
+    ost.hist[0] = small
+    C3, Cq3 = call()
+    o3 = ost.quantize(cbits, fp8.E4M3, delayed=True)
+    assert o3["overflow"] > 0
+    assert np.array_equal(host_u8(Cq3), o3["q"])
+    snap = st.snapshot()
+    same_quant(snap, o3, 1)
+    assert snap["overflow"] == ost.overflow and snap["underflow"] == ost.underflow

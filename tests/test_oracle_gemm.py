@@ -1,6 +1,8 @@
 """Pins of the oracle's scaled matmuls: exact rational brute force on tiny shapes with
-non-square operands, the identity operand, the bf16 rounding against torch's fp32->bf16
-conversion, the block-scaled form's reductions to the per-tensor form, and the bound."""
+non-square operands (full and sampled forms, every format pair), the identity operand, the
+bf16 rounding (fp64 and exact-rational forms) against torch's fp32->bf16 conversion, a sum
+whose small term fp64 summation loses, the block-scaled form's reductions to the
+per-tensor form, and the bound."""
 from fractions import Fraction
 
 import numpy as np
@@ -114,6 +116,13 @@ def test_block_scaled_rational_with_distinct_scales():
     rows = np.array([0, 1, 1]); cols = np.array([5, 130, 255])
     s, _ = gemm.block_scaled_mm_sampled(A, fp8.E5M2, da, B, fp8.E4M3, db, rows, cols)
     assert np.array_equal(s, blk[rows, cols])
+    for t, (i, j) in enumerate(zip(rows, cols)):
+        tot = Fraction(0)
+        for kb in range(2):
+            sc = Fraction(float(np.float32(da[i, kb] * db[kb, j // 128])))
+            tot += sc * sum(Fraction(fp8.decode(int(A[i, k]), fp8.E5M2)) * Fraction(fp8.decode(int(B[j, k]), fp8.E4M3))
+                            for k in range(kb * 128, kb * 128 + 128))
+        assert s[t] == gemm.bf16_round_exact(tot)
 
 
 def test_sampled_matches_full():
@@ -141,3 +150,58 @@ def test_bound_rejects_planted_errors():
     B = rand_codes(rng, (6, 32), fp8.E4M3)
     r, m, _ = gemm.scaled_mm(A, fp8.E4M3, B, fp8.E4M3, 1.0, 1.0)
     assert not gemm.within_bound(r.T, r, m).all()
+
+
+@pytest.mark.parametrize("fa,fb", [(fp8.E4M3, fp8.E4M3), (fp8.E5M2, fp8.E4M3), (fp8.E4M3, fp8.E5M2),
+                                   (fp8.E5M2, fp8.E5M2)])
+def test_exact_sampled_against_fraction(fa, fb):
+    """The sampled reference is the definition computed exactly: rational brute force over
+    random finite codes of every format pair (extremes included) and random fp32 scales."""
+    rng = np.random.default_rng(12)
+    M, N, K = 5, 6, 300
+    A = rand_codes(rng, (M, K), fa)
+    B = rand_codes(rng, (N, K), fb)
+    A[0, :4] = [0x7E if fa == fp8.E4M3 else 0x7B, 0x01, 0xFE if fa == fp8.E4M3 else 0xFB, 0x80]
+    d_a, d_b = np.float32(rng.uniform(1e-3, 10)), np.float32(rng.uniform(1e-3, 10))
+    rows = np.repeat(np.arange(M), N)
+    cols = np.tile(np.arange(N), M)
+    ref, mag = gemm.scaled_mm_sampled(A, fa, B, fb, d_a, d_b, rows, cols)
+    dd = Fraction(float(np.float32(d_a * d_b)))
+    for t, (i, j) in enumerate(zip(rows, cols)):
+        s = sum(Fraction(fp8.decode(int(A[i, k]), fa)) * Fraction(fp8.decode(int(B[j, k]), fb)) for k in range(K))
+        want = gemm.bf16_round_exact(dd * s)
+        assert ref[t] == want, (i, j)
+        m = sum(abs(Fraction(fp8.decode(int(A[i, k]), fa)) * Fraction(fp8.decode(int(B[j, k]), fb))) for k in range(K))
+        assert mag[t] == pytest.approx(float(m) * float(d_a) * float(d_b), rel=1e-12)
+
+
+def test_exact_sampled_keeps_a_term_fp64_summation_loses():
+    """Sixty-four E5M2-max x E4M3-max products, one product of the smallest subnormals, then
+    the negated large products: the real sum is 2^-25. fp64 summation in this order loses the
+    small term (the partial sum is near 2^30.6, whose fp64 spacing is 2^-22); the exact
+    reference keeps it."""
+    big_a, big_b = 0x7B, 0x7E                 # 57344 (E5M2) and 448 (E4M3)
+    A = np.array([[big_a] * 64 + [0x01] + [big_a | 0x80] * 64], dtype=np.uint8)
+    B = np.array([[big_b] * 64 + [0x01] + [big_b] * 64], dtype=np.uint8)
+    vals = [fp8.decode(int(a), fp8.E5M2) * fp8.decode(int(b), fp8.E4M3) for a, b in zip(A[0], B[0])]
+    acc = 0.0
+    for v in vals:                            # left-to-right fp64 summation
+        acc += v
+    assert acc == 0.0
+    ref, _ = gemm.scaled_mm_sampled(A, fp8.E5M2, B, fp8.E4M3, 1.0, 1.0, np.array([0]), np.array([0]))
+    assert ref[0] == 2.0 ** -25
+
+
+def test_bf16_round_exact_against_torch_and_ties():
+    rng = np.random.default_rng(13)
+    v = (rng.standard_normal(20000) * 10.0 ** rng.integers(-40, 38, 20000)).astype(np.float32)
+    v = np.concatenate([v[np.isfinite(v)], np.array([3.3895e38, 1e-40, -1e-40, 2 ** -133], dtype=np.float32)])
+    theirs = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    ours = np.array([gemm.bf16_round_exact(Fraction(float(x))) for x in v])
+    assert np.array_equal(ours, theirs)
+    # exact ties between bf16 neighbours (1 + 2^-8 lies halfway between 1 and 1 + 2^-7)
+    assert gemm.bf16_round_exact(Fraction(1) + Fraction(1, 256)) == 1.0
+    assert gemm.bf16_round_exact(Fraction(1) + Fraction(3, 256)) == 1.0 + 2 ** -6
+    assert gemm.bf16_round_exact(-(Fraction(1) + Fraction(1, 256) + Fraction(1, 2 ** 60))) == -(1.0 + 2 ** -7)
+    assert gemm.bf16_round_exact(Fraction(2) ** 128) == float("inf")
+    assert gemm.bf16_round_exact(Fraction(3, 2 ** 135)) == 2.0 ** -133      # 1.5 subnormal ulps -> even

@@ -7,9 +7,12 @@ codes of dy in a static array inside the library. This file is collected last so
 run stopping at its first failure has already run every other test.
 
 Two calls in a row (different dy, so the second call must not reuse the first call's codes)
-are compared with fp8_linear_bwd on the same inputs, through the C ABI: dx and dW within the
-tolerance the other GEMM tests use (1e-3 * sum|a b| d_a d_b + 1 bf16 ulp, magnitudes from the
-oracle) and the dy scaling state bit for bit. A shape beyond the static array is rejected."""
+are compared with fp8_linear_bwd on the same inputs, through the C ABI. Both run the same
+kernels on the same codes, so dx and dW must be bit-identical, and the dy scaling state
+too; both are also checked against the oracle's exact sampled reference within the GEMM
+bound (1e-3 * sum|a b| d_a d_b + 1 bf16 ulp). The dgrad-only form (no dW: no transposed
+codes) is checked the same way. A further call leaves the device's free memory unchanged.
+A shape beyond the static array is rejected."""
 import numpy as np
 import pytest
 import torch
@@ -33,42 +36,97 @@ def within(a, b, mag):
     assert ok.all(), f"{(~ok).sum()} of {ok.size} outside the bound"
 
 
-def test_noalloc_backward_matches_scratch_backward_twice(g):
-    M, K, N = 1024, 384, 1536
-    x_b = normal_bf16(7100, (M, K))
-    w_b = normal_bf16(7101, (K, N), 0.02)
-    x, w = dev_bf16(x_b), dev_bf16(w_b)
-    wst, xst = g.TensorState(), g.TensorState()
-    wq, wqT, xq, xqT = empty_u8(K, N), empty_u8(N, K), empty_u8(M, K), empty_u8(K, M)
-    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    T, C = g.FP8_GRAN_TENSOR, g.FP8_SCALE_CURRENT
-    g.fp8_requantize_weights(w, K, N, T, C, wst, wq, wqT)
-    g.fp8_linear_fwd(x, M, K, N, wqT, wst, None, xst, T, C, xq, xqT, None, y)
-    ox = quant.quantize_tensor(x_b, fp8.E4M3)
-    ow = quant.quantize_tensor(w_b, fp8.E4M3)
+def bits_equal(a, b):
+    return torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+class Forward:
+    """A layer whose forward ran: the cached weight codes and the saved x codes."""
+
+    def __init__(self, g, M, K, N, seed):
+        self.M, self.K, self.N = M, K, N
+        self.x_b = normal_bf16(seed, (M, K))
+        self.w_b = normal_bf16(seed + 1, (K, N), 0.02)
+        x, w = dev_bf16(self.x_b), dev_bf16(self.w_b)
+        self.wst, self.xst = g.TensorState(), g.TensorState()
+        self.wq, self.wqT, self.xq, self.xqT = empty_u8(K, N), empty_u8(N, K), empty_u8(M, K), empty_u8(K, M)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        T, C = g.FP8_GRAN_TENSOR, g.FP8_SCALE_CURRENT
+        g.fp8_requantize_weights(w, K, N, T, C, self.wst, self.wq, self.wqT)
+        g.fp8_linear_fwd(x, M, K, N, self.wqT, self.wst, None, self.xst, T, C, self.xq, self.xqT, None, y)
+        self.ox = quant.quantize_tensor(self.x_b, fp8.E4M3)
+        self.ow = quant.quantize_tensor(self.w_b, fp8.E4M3)
+
+
+def oracle_check(f, dy_b, dx, dw):
+    """dx (and dW) against the oracle's exact sampled reference."""
+    og = quant.quantize_tensor(dy_b, fp8.E5M2)
+    rng = np.random.default_rng(int(dy_b[0, 0]))
+    r, c = rng.integers(0, f.M, 2048), rng.integers(0, f.K, 2048)
+    ref, mag = gemm.scaled_mm_sampled(og["q"], fp8.E5M2, f.ow["q"], fp8.E4M3, og["d"], f.ow["d"], r, c)
+    within(host_bf16_f64(dx)[r, c], ref, mag)
+    if dw is not None:
+        r, c = rng.integers(0, f.K, 2048), rng.integers(0, f.N, 2048)
+        ref, mag = gemm.scaled_mm_sampled(f.ox["qT"], fp8.E4M3, og["qT"], fp8.E5M2, f.ox["d"], og["d"], r, c)
+        within(host_bf16_f64(dw)[r, c], ref, mag)
+
+
+def run_pair(g, f, dy_b, with_dw):
+    """fp8_linear_bwd (caller scratch) and fp8_linear_bwd_noalloc on the same dy."""
+    M, K, N = f.M, f.K, f.N
+    C = g.FP8_SCALE_CURRENT
     bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
-    for call, seed in enumerate((7102, 7103)):
-        dy_b = lognormal_grad_bf16(seed, (M, N))
-        dy = dev_bf16(dy_b)
-        # existing entry point, caller-provided scratch
-        st_ref = g.TensorState()
-        dyq, dyqT = empty_u8(M, N), empty_u8(N, M)
-        dx_ref, dw_ref = bf(M, K), bf(K, N)
-        g.fp8_linear_bwd(dy, M, K, N, xqT, xst, wq, wst, st_ref, C, dyq, dyqT, dx_ref, dw_ref)
-        # allocation-free entry point
-        st_na = g.TensorState()
-        dx_na, dw_na = bf(M, K), bf(K, N)
-        g.fp8_linear_bwd_noalloc(dy, M, K, N, xqT, xst, wq, wst, st_na, C, dx_na, dw_na)
-        torch.cuda.synchronize()
-        g.fp8_poll_device_error()
-        a, b = st_ref.snapshot(), st_na.snapshot()
-        for k in ("scale", "scale_inv", "amax_cur", "overflow", "underflow"):
-            assert a[k] == b[k], (call, k)
-        og = quant.quantize_tensor(dy_b, fp8.E5M2)
-        _, mag_dx, _ = gemm.scaled_mm(og["q"], fp8.E5M2, ow["q"], fp8.E4M3, og["d"], ow["d"])
-        _, mag_dw, _ = gemm.scaled_mm(ox["qT"], fp8.E4M3, og["qT"], fp8.E5M2, ox["d"], og["d"])
-        within(host_bf16_f64(dx_na), host_bf16_f64(dx_ref), mag_dx)
-        within(host_bf16_f64(dw_na), host_bf16_f64(dw_ref), mag_dw)
+    dy = dev_bf16(dy_b)
+    st_ref, st_na = g.TensorState(), g.TensorState()
+    dyq, dyqT = empty_u8(M, N), (empty_u8(N, M) if with_dw else None)
+    dx_ref, dx_na = bf(M, K), bf(M, K)
+    dw_ref, dw_na = (bf(K, N), bf(K, N)) if with_dw else (None, None)
+    g.fp8_linear_bwd(dy, M, K, N, f.xqT, f.xst, f.wq, f.wst, st_ref, C, dyq, dyqT, dx_ref, dw_ref)
+    g.fp8_linear_bwd_noalloc(dy, M, K, N, f.xqT, f.xst, f.wq, f.wst, st_na, C, dx_na, dw_na)
+    torch.cuda.synchronize()
+    g.fp8_poll_device_error()
+    a, b = st_ref.snapshot(), st_na.snapshot()
+    for k in ("scale", "scale_inv", "amax_cur", "overflow", "underflow"):
+        assert a[k] == b[k], k
+    assert bits_equal(dx_na, dx_ref)
+    if with_dw:
+        assert bits_equal(dw_na, dw_ref)
+    return dx_na, dw_na
+
+
+def test_noalloc_backward_matches_scratch_backward_twice(g):
+    f = Forward(g, 1024, 384, 1536, 7100)
+    for seed in (7102, 7103):
+        dy_b = lognormal_grad_bf16(seed, (f.M, f.N))
+        dx, dw = run_pair(g, f, dy_b, with_dw=True)
+        oracle_check(f, dy_b, dx, dw)
+
+
+def test_noalloc_dgrad_only_matches_scratch_backward_twice(g):
+    """dW not requested: the array holds only the row-major dy codes (a larger M*N fits)."""
+    f = Forward(g, 2048, 256, 2048, 7200)
+    for seed in (7202, 7203):
+        dy_b = lognormal_grad_bf16(seed, (f.M, f.N))
+        dx, _ = run_pair(g, f, dy_b, with_dw=False)
+        oracle_check(f, dy_b, dx, None)
+
+
+def test_noalloc_backward_allocates_no_device_memory(g):
+    """After a first call (which looks up the array's address), a second call changes the
+    device's free memory by nothing."""
+    f = Forward(g, 512, 256, 1024, 7300)
+    dy = dev_bf16(lognormal_grad_bf16(7302, (f.M, f.N)))
+    bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
+    dx, dw, st = bf(f.M, f.K), bf(f.K, f.N), g.TensorState()
+    C = g.FP8_SCALE_CURRENT
+    g.fp8_linear_bwd_noalloc(dy, f.M, f.K, f.N, f.xqT, f.xst, f.wq, f.wst, st, C, dx, dw)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    g.fp8_linear_bwd_noalloc(dy, f.M, f.K, f.N, f.xqT, f.xst, f.wq, f.wst, st, C, dx, dw)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    g.fp8_poll_device_error()
+    assert free1 == free0
 
 
 def test_noalloc_backward_rejects_shapes_beyond_the_static_array(g):
