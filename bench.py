@@ -1,22 +1,28 @@
 #!/usr/bin/env python
-"""Benchmark of the FP8 up-projection training step on GB300.
+"""Benchmark of the FP8 up-projection hot path on GB300.
 
-Workload (GPT-2-small-shaped MLP up-projection): x [8192 x 768] ~ N(0,1) with 0.1 % of
-the entries x100, W [768 x 3072] ~ N(0, 0.02), dy [8192 x 3072] log-normal (median 1e-4,
-sigma_log 2, random sign). One step = one pass of the whole hot path with per-tensor
-delayed scaling (amax history of 16):
-  requantise W (amax, scale, E4M3 cast into W_q [K,N] and W_q^T [N,K])
-  quantise x (E4M3, x_q and x_q^T)          forward GEMM  y  = x W         (tcgen05)
-  quantise dy (E5M2, dy_q and dy_q^T)       dgrad GEMM    dx = dy W^T
-                                            wgrad GEMM    dW = x^T dy
-  push the x, W and dy amaxes into their histories.
-The step is captured into a CUDA graph; each timed step replays it with CUDA events around
-the launch, after writing a 256 MiB buffer to flush the 129 MB L2 (not timed). Per-kernel
-times come from the same stages launched eagerly in the same loop, each behind a flush. value = the step's GEMM FLOPs (3 x 2MNK) over the
-measured step time, summed over ranks (each rank its own batch: weak scaling).
+Headline (the JSON line's value): the fine-grained-scaling forward at its full size.
+  x bf16 [16384 x 4096] = z * std_c (z ~ N(0,1), std_c = 10^U(-1,1) per channel),
+  W bf16 [4096 x 14336] ~ N(0, 0.02). One step is one pass of the hot path:
+    W's E4M3 cast with one scale per 128 x 128 block into W_q^T [14336 x 4096] (the weight
+      cache refresh)                                         || on a second stream
+    x's E4M3 cast with one scale per 1 x 128 row tile into x_q [16384 x 4096]
+    the block-scaled GEMM y = bf16( sum_kb d_x[i,kb] d_w[kb,j/128] P_ij,kb ) [16384 x 14336]
+  value = the GEMM's 2MNK over the step time; the roofline is the block-scaled GEMM's.
+The step is captured into a CUDA graph; each timed step replays it between CUDA events after
+writing a 256 MiB buffer (the L2 flush, not timed). Per-kernel times come from the same stages
+launched eagerly in the same loop, each behind a flush.
+
+Sub-records in the same line, each with its own roofline, kernel times and oracle CPU baseline:
+  backward_upproj   M=16384, K=1024, N=4096: dy's E5M2 cast (current scaling, dy_q and dy_q^T),
+                    dgrad and wgrad in one grouped launch
+  delayed_loop      32768 tokens, d 1536 -> 6144, history 16: one layer-step (optimizer step
+                    fused with W's refresh, x cast, forward, dy cast, dgrad + wgrad, commit)
+                    and the 12-layer step
+  gpt2s_train_step  8192 tokens, d 768 -> 3072: the whole training step with delayed scaling
 
 --impl reference times the CPU oracle (test infrastructure) on a bounded sample of the
-same step on the host cores.
+headline's step on the host cores.
 """
 from __future__ import annotations
 
@@ -34,8 +40,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "FP8 up-proj GEMM TFLOP/s (% FP8 peak); quantize-cast GB/s (% HBM)"
-M, K, N = 8192, 768, 3072
-HIST = 16
+# the fine-grained forward (headline), the backward, the delayed loop and GPT-2 small
+FINE = dict(M=16384, K=4096, N=14336)
+BWD = dict(M=16384, K=1024, N=4096)
+LOOP = dict(M=32768, K=1536, N=6144, layers=12, hist=16)
+GPT2 = dict(M=8192, K=768, N=3072, hist=16)
 FLUSH_BYTES = 256 << 20
 # Roofline denominators: HBM copy GB/s and dense bf16 TFLOP/s (burst) from MEASURED_PEAKS.json,
 # else these earlier GB300 measurements; the FP8 dense peak is the bf16 figure times the
@@ -109,15 +118,25 @@ class Clocks:
 
 
 # --------------------------------------------------------------------------------------
-# GPU arm
+# per-launch DRAM counters (profiles/traffic_per_launch.txt)
 # --------------------------------------------------------------------------------------
 # The sources that decide each stage's kernel and launch (kernel body, its headers, the
 # host code that picks and launches it): a stage's DRAM counters stay valid while these hash
 # the same as when the counters were taken.
 _CAST_SOURCES = ("quant.cu", "cast.cuh", "ptx.cuh", "kernels.h", "api.cu")
 _GEMM_SOURCES = ("gemm.cu", "cast.cuh", "ptx.cuh", "kernels.h", "api.cu")
-STAGE_SOURCES = {"requant_w": _CAST_SOURCES, "quant_x": _CAST_SOURCES, "quant_dy": _CAST_SOURCES,
-                 "gemm_fwd": _GEMM_SOURCES, "gemm_bwd": _GEMM_SOURCES}
+STAGE_SOURCES = {
+    # GPT-2-small training step
+    "requant_w": _CAST_SOURCES, "quant_x": _CAST_SOURCES, "quant_dy": _CAST_SOURCES,
+    "gemm_fwd": _GEMM_SOURCES, "gemm_bwd": _GEMM_SOURCES,
+    # fine-grained forward (headline)
+    "fine_cast_w": _CAST_SOURCES, "fine_cast_x": _CAST_SOURCES, "fine_gemm": _GEMM_SOURCES,
+    # backward
+    "bwd_cast_dy": _CAST_SOURCES, "bwd_gemm": _GEMM_SOURCES,
+    # delayed loop, one layer-step
+    "loop_update_w": _CAST_SOURCES, "loop_cast_x": _CAST_SOURCES, "loop_gemm_fwd": _GEMM_SOURCES,
+    "loop_cast_dy": _CAST_SOURCES, "loop_gemm_bwd": _GEMM_SOURCES,
+}
 
 
 def traffic_table():
@@ -147,8 +166,8 @@ def source_hash(files, read=None):
 
 
 def rank_seeds(rank: int):
-    """Seeds of rank r's own batch (x, dy): rank 0 uses the workload's seeds."""
-    return (1000 * 2 + 0, 2002) if rank == 0 else (2000 + 10 * rank, 2002 + 10 * rank)
+    """Seed offset of rank r's own batch: rank 0 uses the workloads' own seeds."""
+    return (0, 0) if rank == 0 else (10 * rank, 10 * rank + 1)
 
 
 def max_over_ranks(total_ms: float, world: int, device) -> float:
@@ -167,11 +186,111 @@ def weak_scaling_value(step_flops: float, steps: int, world: int, total_ms: floa
     return step_flops * steps * world / (total_ms * 1e-3) / 1e12
 
 
-def run_gpu(args):
+# --------------------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------------------
+class Stage:
+    """One launch of a step: name (a STAGE_SOURCES key), the call, the kernels it launches and
+    its algorithmic work (GEMM FLOPs, or bytes a cast must move)."""
+
+    def __init__(self, name, fn, launches, flops=0.0, nbytes=0.0):
+        self.name, self.fn, self.launches, self.flops, self.nbytes = name, fn, launches, flops, nbytes
+
+
+def time_step(torch, stream, flush, enqueue_step, stages, steps, warmup, before_replays=None, clocks=None):
+    """Capture enqueue_step() (the whole step, possibly on several streams) into one CUDA graph
+    on `stream`, then run warmup + steps iterations. An iteration: flush L2 (untimed), replay
+    the graph between two events on `stream`; then launch every stage eagerly, each behind its
+    own flush and between its own events (cold L2, per-kernel times). Returns per-step graph
+    times (ms), per-stage mean times (ms) and the wall time of the timed iterations."""
+    with torch.cuda.stream(stream):
+        for st in stages:  # eager pass: kernel attributes, plans and caches
+            st.fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            enqueue_step()
+        if before_replays is not None:
+            before_replays()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in stages]
+
+        def one():
+            flush.zero_()
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            for (a, b), st in zip(ev, stages):
+                flush.zero_()
+                a.record(stream)
+                st.fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1), [a.elapsed_time(b) for a, b in ev]
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        if clocks is not None:
+            clocks.start()
+            time.sleep(0.3)  # let the sampler see the first samples
+        wall0 = time.perf_counter()
+        res = [one() for _ in range(steps)]
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    step_ms = [t for t, _ in res]
+    stage_ms = [sum(r[1][i] for r in res) / steps for i in range(len(stages))]
+    return step_ms, stage_ms, wall
+
+
+def kernel_records(stages, stage_ms, hbm, fp8_peak):
+    out = {}
+    for st, ms in zip(stages, stage_ms):
+        kd = {"ms": round(ms, 5), "launches": st.launches}
+        if st.flops:
+            tf = st.flops / (ms * 1e-3) / 1e12
+            kd.update(achieved=round(tf, 1), unit="TFLOP/s", frac=round(tf / fp8_peak, 4))
+        elif st.nbytes:
+            gbs = st.nbytes / (ms * 1e-3) / 1e9
+            kd.update(achieved=round(gbs, 1), unit="GB/s", frac=round(gbs / hbm, 4))
+        out[st.name] = kd
+    return out
+
+
+def roofline(stages, stage_ms, hbm, bf16_tf, peak_src, name=None):
+    """The roofline object of one stage: the named one, else the one with algorithmic work that
+    took longest. achieved = algorithmic work of one launch / its mean CUDA-event duration."""
+    fp8_peak = 2.0 * bf16_tf
+    idx = [i for i, st in enumerate(stages) if st.flops or st.nbytes]
+    if name is not None:
+        i = next(i for i in idx if stages[i].name == name)
+    else:
+        i = max(idx, key=lambda j: stage_ms[j])
+    st, ms = stages[i], stage_ms[i]
+    if st.flops:
+        r = {"kernel": st.name, "bound": "tensor", "achieved": round(st.flops / (ms * 1e-3) / 1e12, 1),
+             "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+             "peak_source": f"{peak_src}: fp8 = 2 x bf16 burst {bf16_tf} TF/s"}
+    else:
+        r = {"kernel": st.name, "bound": "hbm", "achieved": round(st.nbytes / (ms * 1e-3) / 1e9, 1),
+             "peak": round(hbm, 1), "unit": "GB/s", "peak_source": f"{peak_src}: HBM copy {hbm} GB/s"}
+    r["frac"] = round(r["achieved"] / r["peak"], 4)
+    r["traffic"] = traffic_table().get(st.name)
+    return r
+
+
+def dev_bf16(torch, bits):
     import numpy as np
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def run_gpu(args):
+    rank, local_rank, world = env_rank()
+    # the oracle's CPU legs run first, in child processes, before this process touches the GPU
+    cpu = cpu_baselines() if (rank == 0 and world == 1 and not args.no_cpu_baseline) else {}
     import torch
 
-    rank, local_rank, world = env_rank()
     torch.cuda.set_device(local_rank)
     if world > 1:
         import torch.distributed as dist
@@ -179,232 +298,130 @@ def run_gpu(args):
     import __graft_entry__
     __graft_entry__.build()
     import fp8_mixed_precision_saturating_gb300 as g
-    from datagen import workload_inputs, lognormal_grad_bf16, outlier_normal_bf16
-
-    w = workload_inputs("gpt2s_upproj_fwd")
-    sx, sdy = rank_seeds(rank)
-    x_h = w["x"] if rank == 0 else outlier_normal_bf16(sx, (M, K))
-    w_h = w["w"]
-    dy_h = lognormal_grad_bf16(sdy, (M, N))
-
-    def dev(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
-
-    x, wm, dy = dev(x_h), dev(w_h), dev(dy_h)
-    u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device="cuda")
-    bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
-    wst, xst, gst = g.TensorState(HIST), g.TensorState(HIST), g.TensorState(HIST)
-    wq, wqT, xq, xqT, dyq, dyqT = u8(K, N), u8(N, K), u8(M, K), u8(K, M), u8(M, N), u8(N, M)
-    y, dx, dw = bf(M, N), bf(M, K), bf(K, N)
-    D = g.FP8_SCALE_DELAYED
-    T = g.FP8_GRAN_TENSOR
-    gemm_flops = 2.0 * M * N * K
-
-    # the backward's two GEMMs run as one grouped launch (wgrad split over its tokens through
-    # the workspace, dgrad beside it); the forward GEMM gets the same workspace (unused: its
-    # 384 tiles fill the GPU)
-    bwd = [g.mm_problem(xqT, 0, dyqT, 1, K, N, M, M, M, xst.scale_inv, gst.scale_inv, dw, N),
-           g.mm_problem(dyq, 1, wq, 0, M, K, N, N, N, gst.scale_inv, wst.scale_inv, dx, K)]
-    ws_bytes = max(g.fp8_scaled_mm_grouped_workspace_bytes(bwd), g.fp8_scaled_mm_workspace_bytes(M, N, K))
-    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
-    # (name, call, kernels launched, algorithmic flops, algorithmic bytes)
-    stages = [
-        ("requant_w", lambda: g.fp8_requantize_weights(wm, K, N, T, D, wst, wq, wqT), 1, 0.0, K * N * 4.0),
-        ("quant_x", lambda: g.fp8_quantize(x, M, K, K, g.FP8_E4M3, T, D, xst, xq, xqT), 1, 0.0, M * K * 4.0),
-        ("gemm_fwd", lambda: g.fp8_scaled_mm_ws(xq, 0, wqT, 0, M, N, K, K, K, T, xst.scale_inv, wst.scale_inv, y, N,
-                                                ws, ws_bytes), 1, gemm_flops, 0.0),
-        ("quant_dy", lambda: g.fp8_quantize(dy, M, N, N, g.FP8_E5M2, T, D, gst, dyq, dyqT), 1, 0.0, M * N * 4.0),
-        ("gemm_bwd", lambda: g.fp8_scaled_mm_grouped(bwd, ws, ws_bytes), 1, 2 * gemm_flops, 0.0),
-        ("commit", lambda: g.fp8_history_commit_many([wst, xst, gst]), 1, 0.0, 0.0),
-    ]
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    stream = torch.cuda.Stream()
-    with torch.cuda.stream(stream):
-        for _, fn, *_ in stages:  # eager pass: sets kernel attributes and caches
-            fn()
-        torch.cuda.synchronize()
-        # the step is one CUDA graph, replayed once per timed step with CUDA events around the
-        # launch (the graph launch itself counts). Per-kernel times come from the same stages
-        # launched eagerly in the same loop, each behind an L2 flush: the GPU is still busy
-        # with the flush while the host enqueues the stage, so the events bracket only the
-        # kernel (cold L2, no event nodes inside a graph).
-        # the step's dependency graph: W's refresh beside x's cast on two streams (measured
-        # 2 us faster per step than the one-launch fp8_quantize_many of both), then the
-        # forward GEMM, dy's cast, the grouped backward GEMMs and the history commit
-        side = torch.cuda.Stream()
-        fn = {name: f for name, f, *_ in stages}
-        plain = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(plain, stream=stream):
-            side.wait_stream(stream)
-            fn["requant_w"]()
-            with torch.cuda.stream(side):
-                fn["quant_x"]()
-            stream.wait_stream(side)
-            fn["gemm_fwd"]()
-            fn["quant_dy"]()
-            fn["gemm_bwd"]()
-            fn["commit"]()
-        for st in (wst, xst, gst):
-            st.reset()  # the delayed-scaling state starts empty (bootstrap step first)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in stages]
-
-        def step():
-            flush.zero_()  # L2 flush, outside the timed events
-            e0.record(stream)
-            plain.replay()
-            e1.record(stream)
-            for (a, b), (_, fn, *_) in zip(ev, stages):
-                flush.zero_()
-                a.record(stream)
-                fn()
-                b.record(stream)
-            torch.cuda.synchronize()
-            return e0.elapsed_time(e1), [a.elapsed_time(b) for a, b in ev]
-
-        for _ in range(args.warmup):
-            step()
-        clocks = Clocks(local_rank)
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        clocks.start()
-        time.sleep(0.3)  # let the sampler see the first samples
-        wall0 = time.perf_counter()
-        per_step = [step() for _ in range(args.steps)]
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
-        if world > 1:
-            torch.distributed.barrier()
-        clk = clocks.stop()
-        g.fp8_poll_device_error()
-
-    step_ms = [t for t, _ in per_step]
-    stage_ms = [sum(t[i] for _, t in per_step) / args.steps for i in range(len(stages))]
-    probe_step_ms = sum(stage_ms)
-    total_ms = max_over_ranks(sum(step_ms), world, "cuda")
-    step_flops = sum(s[3] for s in stages)
-    value = weak_scaling_value(step_flops, args.steps, world, total_ms)
 
     hbm, bf16_tf, peak_src = load_peaks()
-    fp8_peak = bf16_tf * 2.0
-    traffic = traffic_table()
-    kernels = {}
-    for (name, _, nk, fl, by), ms in zip(stages, stage_ms):
-        kd = {"ms": round(ms, 5), "launches": nk}
-        if fl:
-            kd.update(achieved=round(fl / (ms * 1e-3) / 1e12, 1), unit="TFLOP/s", frac=round(fl / (ms * 1e-3) / 1e12 / fp8_peak, 4))
-        elif by:
-            kd.update(achieved=round(by / (ms * 1e-3) / 1e9, 1), unit="GB/s", frac=round(by / (ms * 1e-3) / 1e9 / hbm, 4))
-        kernels[name] = kd
-    dom_i = max(range(len(stages)), key=lambda i: stage_ms[i] if (stages[i][3] or stages[i][4]) else -1)
-    dname, _, _, dfl, dby = stages[dom_i]
-    dms = stage_ms[dom_i]
-    if dfl:
-        roof = {"kernel": dname, "bound": "tensor", "achieved": round(dfl / (dms * 1e-3) / 1e12, 1),
-                "peak": round(fp8_peak, 1), "unit": "TFLOP/s"}
-    else:
-        roof = {"kernel": dname, "bound": "hbm", "achieved": round(dby / (dms * 1e-3) / 1e9, 1),
-                "peak": round(hbm, 1), "unit": "GB/s"}
-    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = traffic.get(dname)
-    roof["peak_source"] = (f"{peak_src}: fp8 = 2 x bf16 burst {bf16_tf} TF/s" if dfl else f"{peak_src}: HBM copy {hbm} GB/s")
+    fp8_peak = 2.0 * bf16_tf
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    ctx = dict(torch=torch, g=g, stream=stream, flush=flush, hbm=hbm, bf16_tf=bf16_tf, peak_src=peak_src,
+               fp8_peak=fp8_peak, rank=rank, world=world)
 
-    # block-scaled forward at the same shapes (1x128 x tiles, 128x128 W blocks), timed alone
-    blk = run_block_scaled(g, torch, x, wm, stream, flush, args.steps)
-    # end to end through the public API with host buffers
-    e2e = run_e2e(g, torch, x_h, w_h, dy_h, stream, args.steps, step_flops)
+    # ---- headline: the fine-grained forward at full size
+    clocks = Clocks(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    head = bench_finegrained(ctx, args.steps, args.warmup, clocks)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    total_ms = max_over_ranks(sum(head["step_ms"]), world, "cuda")
+    value = weak_scaling_value(head["step_flops"], args.steps, world, total_ms)
 
-    launches = sum(s[2] for s in stages) * args.steps
+    # ---- sub-records (rank 0 reports them; every rank runs the same work)
+    subs = {}
+    if not args.headline_only:
+        subs["backward_upproj"] = bench_backward(ctx, max(5, args.steps // 2), args.warmup)
+        subs["delayed_loop"] = bench_delayed_loop(ctx, max(3, args.steps // 4), args.warmup)
+        subs["gpt2s_train_step"] = bench_gpt2(ctx, args.steps, args.warmup)
+        for k, v in subs.items():
+            if k in cpu:
+                v["cpu_baseline"] = cpu[k]
+    g.fp8_poll_device_error()
+
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/e5m2 x fp32-accumulate -> bf16", "data": "synthetic",
-        "config": {"workload": "gpt2s_upproj_train_step", "M_tokens": M, "d_model": K, "d_ff": N,
-                   "step": "(requantise W || quantise x), fwd GEMM, quantise dy, dgrad + wgrad in one grouped launch, 3 history commits; one CUDA graph on two streams",
-                   "scaling": "per-tensor delayed, amax history 16", "global_batch_tokens": M * world,
-                   "l2": "256 MiB buffer written between timed steps (flush)", "parallelism": f"dp{world} (independent batches)"},
-        "roofline": roof,
-        "kernels": kernels,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3, fp32 accumulate and fp32 block scales -> bf16",
+        "data": "synthetic",
+        "config": {"workload": "finegrained_upproj_fwd", "M_tokens": FINE["M"], "d_model": FINE["K"],
+                   "d_ff": FINE["N"],
+                   "x": "bf16 z * 10^U(-1,1) per channel; E4M3 with one fp32 scale per 1x128 row tile",
+                   "W": "bf16 N(0, 0.02); E4M3 with one fp32 scale per 128x128 block, cached as W_q^T",
+                   "step": "(W block cast || x tile cast on two streams), block-scaled GEMM; one CUDA graph",
+                   "global_batch_tokens": FINE["M"] * world,
+                   "l2": "256 MiB buffer written before every timed step and stage (flush); inputs 134 + 117 MB",
+                   "parallelism": f"dp{world} (independent batches)"},
+        "roofline": head["roofline"],
+        "kernels": head["kernels"],
         "kernels_note": "per-stage CUDA-event times of the same stages launched eagerly in the timed loop, each "
-                        "behind an L2 flush (cold L2; sum %.4f ms vs the graph step)" % probe_step_ms,
-        "block_scaled_fwd": blk,
-        "e2e": e2e,
-        "gpu_launches": launches,
+                        "behind an L2 flush (cold L2)",
+        "e2e": head["e2e"],
+        "gpu_launches": head["launches"],
         "clocks": clk,
-        "wall_s_timed": round(wall, 4),
+        "wall_s_timed": round(head["wall"], 4),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_full_step()
+    line.update(subs)
+    if "finegrained" in cpu:
+        line["cpu_baseline"] = cpu["finegrained"]
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
-def run_block_scaled(g, torch, x, wm, stream, flush, steps):
+def bench_finegrained(ctx, steps, warmup, clocks):
+    """The headline step; its e2e leg through the public API with host buffers."""
+    import numpy as np
+    from datagen import workload_inputs, channel_scaled_bf16
+    torch, g, stream, flush = ctx["torch"], ctx["g"], ctx["stream"], ctx["flush"]
+    M, K, N = FINE["M"], FINE["K"], FINE["N"]
+    w_in = workload_inputs("finegrained_fwd")
+    x_h = w_in["x"] if ctx["rank"] == 0 else channel_scaled_bf16(4000 + rank_seeds(ctx["rank"])[0], (M, K))
+    w_h = w_in["w"]
+    x, wm = dev_bf16(torch, x_h), dev_bf16(torch, w_h)
     u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device="cuda")
-    xq, wq, wqT = u8(M, K), u8(K, N), u8(N, K)
+    xq, wqT = u8(M, K), u8(N, K)
     xsi = torch.empty(M, K // 128, dtype=torch.float32, device="cuda")
     wsi = torch.empty(K // 128, N // 128, dtype=torch.float32, device="cuda")
     y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    B = g.FP8_GRAN_BLOCK_128x128
-    calls = [
-        ("requant_w_block", lambda: g.fp8_requantize_weights(wm, K, N, B, 0, None, wq, wqT, wsi), 0.0, K * N * 4.0),
-        ("quant_x_1x128", lambda: g.fp8_quantize(x, M, K, K, 0, g.FP8_GRAN_TILE_1x128, 0, None, xq, None, xsi),
-         0.0, M * K * 3.0 + M * K / 128 * 4),
-        ("gemm_fwd_block_scaled", lambda: g.fp8_scaled_mm(xq, 0, wqT, 0, M, N, K, K, K, B, xsi, wsi, y, N),
-         2.0 * M * N * K, 0.0),
+    B, TL, CUR = g.FP8_GRAN_BLOCK_128x128, g.FP8_GRAN_TILE_1x128, g.FP8_SCALE_CURRENT
+    flops = 2.0 * M * N * K
+    stages = [
+        Stage("fine_cast_w", lambda: g.fp8_requantize_weights(wm, K, N, B, CUR, None, None, wqT, wsi), 1,
+              nbytes=K * N * 3.0 + (K // 128) * (N // 128) * 4),
+        Stage("fine_cast_x", lambda: g.fp8_quantize(x, M, K, K, g.FP8_E4M3, TL, CUR, None, xq, None, xsi), 1,
+              nbytes=M * K * 3.0 + M * (K // 128) * 4),
+        Stage("fine_gemm", lambda: g.fp8_scaled_mm(xq, 0, wqT, 0, M, N, K, K, K, B, xsi, wsi, y, N), 1, flops=flops),
     ]
-    with torch.cuda.stream(stream):
-        for _, fn, _, _ in calls:
-            fn()
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(steps)]
-        for k in range(steps):
-            flush.zero_()
-            ev[k][0].record(stream)
-            for i, (_, fn, _, _) in enumerate(calls):
-                fn()
-                ev[k][i + 1].record(stream)
-        torch.cuda.synchronize()
-    out = {}
-    hbm, bf16_tf, _ = load_peaks()
-    for i, (name, _, fl, by) in enumerate(calls):
-        ms = sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(steps)) / steps
-        d = {"ms": round(ms, 5)}
-        if fl:
-            d.update(achieved=round(fl / (ms * 1e-3) / 1e12, 1), unit="TFLOP/s", frac=round(fl / (ms * 1e-3) / 1e12 / (2 * bf16_tf), 4))
-        else:
-            d.update(achieved=round(by / (ms * 1e-3) / 1e9, 1), unit="GB/s", frac=round(by / (ms * 1e-3) / 1e9 / hbm, 4))
-        out[name] = d
-    return out
+    side = torch.cuda.Stream()
+
+    def enqueue():
+        side.wait_stream(stream)
+        stages[0].fn()
+        with torch.cuda.stream(side):
+            stages[1].fn()
+        stream.wait_stream(side)
+        stages[2].fn()
+
+    step_ms, stage_ms, wall = time_step(torch, stream, flush, enqueue, stages, steps, warmup, clocks=clocks)
+    e2e = e2e_finegrained(ctx, x_h, w_h, steps, flops)
+    return {"step_ms": step_ms, "step_flops": flops, "wall": wall,
+            "kernels": kernel_records(stages, stage_ms, ctx["hbm"], ctx["fp8_peak"]),
+            "roofline": roofline(stages, stage_ms, ctx["hbm"], ctx["bf16_tf"], ctx["peak_src"], name="fine_gemm"),
+            "e2e": e2e, "launches": 2 * len(stages) * steps}
 
 
-def run_e2e(g, torch, x_h, w_h, dy_h, stream, steps, step_flops):
-    """The same step through the public API (requantise + linear forward + linear backward
-    + commits) with host inputs: pinned host -> device copies of x, W and dy and device ->
-    host copies of y, dx and dW inside the timed region, every step. Steps alternate between
-    two sets of device inputs and outputs (and host result buffers), so one step's uploads
-    and compute overlap the previous step's downloads."""
+def e2e_finegrained(ctx, x_h, w_h, steps, step_flops):
+    """The headline step through the public API (fp8_requantize_weights + fp8_linear_fwd with
+    block scaling) from pinned host buffers: x and W copied up and y copied down every step,
+    inside the timed region. Steps alternate between two sets of device buffers (and host
+    result buffers), so one step's uploads and compute overlap the previous step's download."""
     import numpy as np
+    torch, g, stream = ctx["torch"], ctx["g"], ctx["stream"]
+    M, K, N = FINE["M"], FINE["K"], FINE["N"]
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
-    xh, wh, dyh = pin(x_h), pin(w_h), pin(dy_h)
+    xh, wh = pin(x_h), pin(w_h)
     bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
     u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device="cuda")
+    B, CUR = g.FP8_GRAN_BLOCK_128x128, g.FP8_SCALE_CURRENT
     sets = []
     for _ in range(2):
-        sets.append(dict(x=bf(M, K), wm=bf(K, N), dy=bf(M, N), y=bf(M, N), dx=bf(M, K), dw=bf(K, N),
+        sets.append(dict(x=bf(M, K), wm=bf(K, N), y=bf(M, N),
                          yh=torch.empty(M, N, dtype=torch.bfloat16).pin_memory(),
-                         dxh=torch.empty(M, K, dtype=torch.bfloat16).pin_memory(),
-                         dwh=torch.empty(K, N, dtype=torch.bfloat16).pin_memory(),
-                         ev_xw=torch.cuda.Event(), ev_dy=torch.cuda.Event(), ev_fwd=torch.cuda.Event(),
-                         ev_done=torch.cuda.Event(), ev_out=torch.cuda.Event(), used=False))
-    wq, wqT, xq, xqT, dyq, dyqT = u8(K, N), u8(N, K), u8(M, K), u8(K, M), u8(M, N), u8(N, M)
-    wst, xst, gst = g.TensorState(HIST), g.TensorState(HIST), g.TensorState(HIST)
-    D, T = g.FP8_SCALE_DELAYED, g.FP8_GRAN_TENSOR
-    wsb = g.fp8_linear_bwd_workspace_bytes(M, K, N)
-    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
+                         ev_in=torch.cuda.Event(), ev_done=torch.cuda.Event(), ev_out=torch.cuda.Event(), used=False))
+    xq, wqT = u8(M, K), u8(N, K)
+    xsi = torch.empty(M, K // 128, dtype=torch.float32, device="cuda")
+    wsi = torch.empty(K // 128, N // 128, dtype=torch.float32, device="cuda")
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     count = [0]
 
@@ -413,29 +430,19 @@ def run_e2e(g, torch, x_h, w_h, dy_h, stream, steps, step_flops):
         count[0] += 1
         if b["used"]:
             s_in.wait_event(b["ev_done"])  # this set's previous step has read its inputs
-            stream.wait_event(b["ev_out"])  # ... and its outputs are on the host
+            stream.wait_event(b["ev_out"])  # ... and its output is on the host
         b["used"] = True
         with torch.cuda.stream(s_in):
-            b["x"].copy_(xh, non_blocking=True)
             b["wm"].copy_(wh, non_blocking=True)
-            b["ev_xw"].record(s_in)
-            b["dy"].copy_(dyh, non_blocking=True)
-            b["ev_dy"].record(s_in)
-        stream.wait_event(b["ev_xw"])
-        g.fp8_requantize_weights(b["wm"], K, N, T, D, wst, wq, wqT)
-        g.fp8_linear_fwd(b["x"], M, K, N, wqT, wst, None, xst, T, D, xq, xqT, None, b["y"])
-        b["ev_fwd"].record(stream)
-        stream.wait_event(b["ev_dy"])
-        g.fp8_linear_bwd_ws(b["dy"], M, K, N, xqT, xst, wq, wst, gst, D, dyq, dyqT, b["dx"], b["dw"], ws, wsb)
-        g.fp8_history_commit_many([wst, xst, gst])
+            b["x"].copy_(xh, non_blocking=True)
+            b["ev_in"].record(s_in)
+        stream.wait_event(b["ev_in"])
+        g.fp8_requantize_weights(b["wm"], K, N, B, CUR, None, None, wqT, wsi)
+        g.fp8_linear_fwd(b["x"], M, K, N, wqT, None, wsi, None, B, CUR, xq, None, xsi, b["y"])
         b["ev_done"].record(stream)
-        s_out.wait_event(b["ev_fwd"])
-        with torch.cuda.stream(s_out):
-            b["yh"].copy_(b["y"], non_blocking=True)
         s_out.wait_event(b["ev_done"])
         with torch.cuda.stream(s_out):
-            b["dxh"].copy_(b["dx"], non_blocking=True)
-            b["dwh"].copy_(b["dw"], non_blocking=True)
+            b["yh"].copy_(b["y"], non_blocking=True)
             b["ev_out"].record(s_out)
 
     with torch.cuda.stream(stream):
@@ -448,13 +455,192 @@ def run_e2e(g, torch, x_h, w_h, dy_h, stream, steps, step_flops):
         s_out.wait_stream(stream)
         for _ in range(steps):
             one()
-        stream.wait_stream(s_out)  # the last step's results are on the host
+        stream.wait_stream(s_out)  # the last step's result is on the host
         e1.record(stream)
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     return {"value": round(step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
-            "h2d_bytes_per_step": int(2 * (M * K + K * N + M * N)),
-            "d2h_bytes_per_step": int(2 * (M * N + M * K + K * N))}
+            "h2d_bytes_per_step": int(2 * (M * K + K * N)), "d2h_bytes_per_step": int(2 * M * N),
+            "api": "fp8_requantize_weights + fp8_linear_fwd (block scaling), pinned host buffers"}
+
+
+def bench_backward(ctx, steps, warmup):
+    """dy's per-tensor E5M2 cast (current scaling: amax pass, then dy_q and dy_q^T in one pass)
+    and the grouped dgrad + wgrad launch, with x's and W's saved codes cast once beforehand."""
+    from datagen import workload_inputs
+    torch, g, stream, flush = ctx["torch"], ctx["g"], ctx["stream"], ctx["flush"]
+    M, K, N = BWD["M"], BWD["K"], BWD["N"]
+    w_in = workload_inputs("upproj_bwd")
+    x, wm, dy = dev_bf16(torch, w_in["x"]), dev_bf16(torch, w_in["w"]), dev_bf16(torch, w_in["dy"])
+    u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device="cuda")
+    bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
+    T, CUR = g.FP8_GRAN_TENSOR, g.FP8_SCALE_CURRENT
+    xst, wst, gst = g.TensorState(), g.TensorState(), g.TensorState()
+    wq, wqT, xq, xqT, dyq, dyqT = u8(K, N), u8(N, K), u8(M, K), u8(K, M), u8(M, N), u8(N, M)
+    dx, dw = bf(M, K), bf(K, N)
+    with torch.cuda.stream(stream):
+        g.fp8_requantize_weights(wm, K, N, T, CUR, wst, wq, wqT)
+        g.fp8_quantize(x, M, K, K, g.FP8_E4M3, T, CUR, xst, xq, xqT)
+    bwd = [g.mm_problem(xqT, 0, dyqT, 1, K, N, M, M, M, xst.scale_inv, gst.scale_inv, dw, N),
+           g.mm_problem(dyq, 1, wq, 0, M, K, N, N, N, gst.scale_inv, wst.scale_inv, dx, K)]
+    wsb = g.fp8_scaled_mm_grouped_workspace_bytes(bwd)
+    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    flops = 2 * 2.0 * M * N * K
+    stages = [
+        Stage("bwd_cast_dy", lambda: g.fp8_quantize(dy, M, N, N, g.FP8_E5M2, T, CUR, gst, dyq, dyqT), 1,
+              nbytes=M * N * 4.0),
+        Stage("bwd_gemm", lambda: g.fp8_scaled_mm_grouped(bwd, ws, wsb), 1, flops=flops),
+    ]
+
+    def enqueue():
+        for st in stages:
+            st.fn()
+
+    step_ms, stage_ms, _ = time_step(torch, stream, flush, enqueue, stages, steps, warmup)
+    ms = sum(step_ms) / steps
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
+            "steps": steps, "config": {"workload": "upproj_bwd", "M_tokens": M, "d_model": K, "d_ff": N,
+                                       "dy": "bf16 sign * 1e-4 * exp(2 z); E5M2 per tensor, current scaling",
+                                       "step": "dy cast (dy_q, dy_q^T), dgrad + wgrad in one grouped launch"},
+            "roofline": roofline(stages, stage_ms, ctx["hbm"], ctx["bf16_tf"], ctx["peak_src"], name="bwd_gemm"),
+            "kernels": kernel_records(stages, stage_ms, ctx["hbm"], ctx["fp8_peak"])}
+
+
+def bench_delayed_loop(ctx, steps, warmup):
+    """One layer-step of the delayed-scaling loop at full size, and the step of all 12 layers,
+    through the layer API: the optimizer step fused with W's refresh (delta drawn once per
+    layer), x's cast and the forward GEMM, dy's cast and the grouped dgrad + wgrad, the
+    history commit. x and dy are the loop's (drawn once, shared by all layers)."""
+    from datagen import workload_inputs, normal_bf16, perturbation_f32
+    import numpy as np
+    torch, g, stream, flush = ctx["torch"], ctx["g"], ctx["stream"], ctx["flush"]
+    M, K, N, L, H = LOOP["M"], LOOP["K"], LOOP["N"], LOOP["layers"], LOOP["hist"]
+    w_in = workload_inputs("delayed_loop")
+    x, dy = dev_bf16(torch, w_in["x"]), dev_bf16(torch, w_in["dy"])
+    W = [dev_bf16(torch, w) for w in w_in["w"]]
+    delta = [torch.from_numpy(perturbation_f32(w_in["perturb_seed"](l, 1), (K, N), 1e-3)).cuda() for l in range(L)]
+    u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device="cuda")
+    bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
+    D, T = g.FP8_SCALE_DELAYED, g.FP8_GRAN_TENSOR
+    st = [[g.TensorState(H) for _ in range(3)] for _ in range(L)]
+    wq, wqT = [u8(K, N) for _ in range(L)], [u8(N, K) for _ in range(L)]
+    xq, xqT, dyq, dyqT = u8(M, K), u8(K, M), u8(M, N), u8(N, M)
+    y, dx, dw = bf(M, N), bf(M, K), bf(K, N)
+    wsb = g.fp8_linear_bwd_workspace_bytes(M, K, N)
+    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
+
+    def layer_step(l):  # 6 launches: update + requantise, x cast, forward GEMM, dy cast, grouped bwd, commit
+        ws_, xs, gs = st[l]
+        g.fp8_update_requantize_weights(W[l], delta[l], K, N, D, ws_, wq[l], wqT[l])
+        g.fp8_linear_fwd(x, M, K, N, wqT[l], ws_, None, xs, T, D, xq, xqT, None, y)
+        g.fp8_linear_bwd_ws(dy, M, K, N, xqT, xs, wq[l], ws_, gs, D, dyq, dyqT, dx, dw, ws, wsb)
+        g.fp8_history_commit_many([ws_, xs, gs])
+
+    with torch.cuda.stream(stream):
+        for l in range(L):  # the bootstrap step (current amaxes), untimed
+            layer_step(l)
+        torch.cuda.synchronize()
+    ws0, xs0, gs0 = st[0]
+    bwd = [g.mm_problem(xqT, 0, dyqT, 1, K, N, M, M, M, xs0.scale_inv, gs0.scale_inv, dw, N),
+           g.mm_problem(dyq, 1, wq[0], 0, M, K, N, N, N, gs0.scale_inv, ws0.scale_inv, dx, K)]
+    fl = 2.0 * M * N * K
+    stages = [
+        Stage("loop_update_w", lambda: g.fp8_update_requantize_weights(W[0], delta[0], K, N, D, ws0, wq[0], wqT[0]), 1,
+              nbytes=K * N * 10.0),
+        Stage("loop_cast_x", lambda: g.fp8_quantize(x, M, K, K, g.FP8_E4M3, T, D, xs0, xq, xqT), 1, nbytes=M * K * 4.0),
+        Stage("loop_gemm_fwd", lambda: g.fp8_scaled_mm_ws(xq, 0, wqT[0], 0, M, N, K, K, K, T, xs0.scale_inv,
+                                                            ws0.scale_inv, y, N, ws, wsb), 1, flops=fl),
+        Stage("loop_cast_dy", lambda: g.fp8_quantize(dy, M, N, N, g.FP8_E5M2, T, D, gs0, dyq, dyqT), 1,
+              nbytes=M * N * 4.0),
+        Stage("loop_gemm_bwd", lambda: g.fp8_scaled_mm_grouped(bwd, ws, wsb), 1, flops=2 * fl),
+        Stage("loop_commit", lambda: g.fp8_history_commit_many([ws0, xs0, gs0]), 1),
+    ]
+    step_ms, stage_ms, _ = time_step(torch, stream, flush, lambda: layer_step(0), stages, steps, warmup)
+    layer_ms = sum(step_ms) / steps
+    # the 12-layer step: one graph of all layers' launches, replayed behind a flush
+    with torch.cuda.stream(stream):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for l in range(L):
+                layer_step(l)
+        ts = []
+        for _ in range(warmup + steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+    full_ms = sum(ts[warmup:]) / steps
+    ov = sum(int(s.counters[0]) for lay in st for s in lay)
+    return {"value": round(3 * fl / (layer_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_layer_step": round(layer_ms, 5), "ms_per_12_layer_step": round(full_ms, 4),
+            "value_12_layer_step": round(L * 3 * fl / (full_ms * 1e-3) / 1e12, 2), "steps": steps,
+            "launches_per_layer_step": 6,
+            "config": {"workload": "delayed_loop", "M_tokens": M, "d_model": K, "d_ff": N, "layers": L,
+                       "scaling": "per-tensor delayed, amax history 16 (after one untimed bootstrap step)",
+                       "delta": "optimizer step N(0, 1e-3) per element, drawn once per layer"},
+            "overflow_counts_total": ov,
+            "roofline": roofline(stages, stage_ms, ctx["hbm"], ctx["bf16_tf"], ctx["peak_src"]),
+            "kernels": kernel_records(stages, stage_ms, ctx["hbm"], ctx["fp8_peak"])}
+
+
+def bench_gpt2(ctx, steps, warmup):
+    """The GPT-2-small-shaped training step with delayed scaling: (W's refresh || x's cast on
+    two streams), the forward GEMM, dy's cast, dgrad + wgrad in one grouped launch, the three
+    history commits; the states start empty, so the first replay is the bootstrap step."""
+    from datagen import workload_inputs, lognormal_grad_bf16
+    torch, g, stream, flush = ctx["torch"], ctx["g"], ctx["stream"], ctx["flush"]
+    M, K, N, H = GPT2["M"], GPT2["K"], GPT2["N"], GPT2["hist"]
+    w_in = workload_inputs("gpt2s_upproj_fwd")
+    x, wm = dev_bf16(torch, w_in["x"]), dev_bf16(torch, w_in["w"])
+    dy = dev_bf16(torch, lognormal_grad_bf16(2002, (M, N)))
+    u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device="cuda")
+    bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
+    wst, xst, gst = g.TensorState(H), g.TensorState(H), g.TensorState(H)
+    wq, wqT, xq, xqT, dyq, dyqT = u8(K, N), u8(N, K), u8(M, K), u8(K, M), u8(M, N), u8(N, M)
+    y, dx, dw = bf(M, N), bf(M, K), bf(K, N)
+    D, T = g.FP8_SCALE_DELAYED, g.FP8_GRAN_TENSOR
+    fl = 2.0 * M * N * K
+    bwd = [g.mm_problem(xqT, 0, dyqT, 1, K, N, M, M, M, xst.scale_inv, gst.scale_inv, dw, N),
+           g.mm_problem(dyq, 1, wq, 0, M, K, N, N, N, gst.scale_inv, wst.scale_inv, dx, K)]
+    wsb = max(g.fp8_scaled_mm_grouped_workspace_bytes(bwd), g.fp8_scaled_mm_workspace_bytes(M, N, K))
+    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    stages = [
+        Stage("requant_w", lambda: g.fp8_requantize_weights(wm, K, N, T, D, wst, wq, wqT), 1, nbytes=K * N * 4.0),
+        Stage("quant_x", lambda: g.fp8_quantize(x, M, K, K, g.FP8_E4M3, T, D, xst, xq, xqT), 1, nbytes=M * K * 4.0),
+        Stage("gemm_fwd", lambda: g.fp8_scaled_mm_ws(xq, 0, wqT, 0, M, N, K, K, K, T, xst.scale_inv, wst.scale_inv,
+                                                     y, N, ws, wsb), 1, flops=fl),
+        Stage("quant_dy", lambda: g.fp8_quantize(dy, M, N, N, g.FP8_E5M2, T, D, gst, dyq, dyqT), 1, nbytes=M * N * 4.0),
+        Stage("gemm_bwd", lambda: g.fp8_scaled_mm_grouped(bwd, ws, wsb), 1, flops=2 * fl),
+        Stage("commit", lambda: g.fp8_history_commit_many([wst, xst, gst]), 1),
+    ]
+    side = torch.cuda.Stream()
+
+    def enqueue():
+        side.wait_stream(stream)
+        stages[0].fn()
+        with torch.cuda.stream(side):
+            stages[1].fn()
+        stream.wait_stream(side)
+        for st in stages[2:]:
+            st.fn()
+
+    def reset():
+        for s in (wst, xst, gst):
+            s.reset()  # the delayed-scaling state starts empty (bootstrap step first)
+
+    step_ms, stage_ms, _ = time_step(torch, stream, flush, enqueue, stages, steps, warmup, before_replays=reset)
+    ms = sum(step_ms) / steps
+    return {"value": round(3 * fl / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
+            "steps": steps,
+            "config": {"workload": "gpt2s_upproj_train_step", "M_tokens": M, "d_model": K, "d_ff": N,
+                       "scaling": "per-tensor delayed, amax history 16",
+                       "step": "(requantise W || quantise x), fwd GEMM, quantise dy, dgrad + wgrad in one grouped "
+                               "launch, 3 history commits; one CUDA graph on two streams"},
+            "roofline": roofline(stages, stage_ms, ctx["hbm"], ctx["bf16_tf"], ctx["peak_src"]),
+            "kernels": kernel_records(stages, stage_ms, ctx["hbm"], ctx["fp8_peak"])}
 
 
 # --------------------------------------------------------------------------------------
@@ -701,55 +887,192 @@ def run_delayed_loop(g, torch, fp8_peak, layers=12, steps=50, tokens=32768, d=15
 # --------------------------------------------------------------------------------------
 # CPU oracle arm
 # --------------------------------------------------------------------------------------
-def oracle_step(tokens: int):
-    """One oracle pass of the step's arithmetic on `tokens` of the M tokens (W in full).
-    Returns the GEMM FLOPs it covered."""
-    from datagen import workload_inputs, lognormal_grad_bf16
-    from oracle import fp8, gemm, quant
-    w = oracle_step.cache if hasattr(oracle_step, "cache") else None
-    if w is None:
-        w = workload_inputs("gpt2s_upproj_fwd")
-        w["dy"] = lognormal_grad_bf16(2002, (M, N))
-        oracle_step.cache = w
-    x, dy = w["x"][:tokens], w["dy"][:tokens]
-    ow = quant.quantize_tensor(w["w"], fp8.E4M3)
-    ox = quant.quantize_tensor(x, fp8.E4M3)
-    og = quant.quantize_tensor(dy, fp8.E5M2)
-    gemm.scaled_mm(ox["q"], fp8.E4M3, ow["qT"], fp8.E4M3, ox["d"], ow["d"])
-    gemm.scaled_mm(og["q"], fp8.E5M2, ow["q"], fp8.E4M3, og["d"], ow["d"])
-    gemm.scaled_mm(ox["qT"], fp8.E4M3, og["qT"], fp8.E5M2, ox["d"], og["d"])
-    return 3 * 2.0 * tokens * N * K
-
-
-def cpu_baseline_full_step(steps: int = 3):
-    oracle_step(64)  # load inputs
+# Each leg times the oracle (as it stands: numpy, fp64 matmuls through the BLAS) on bounded
+# slabs of one workload's step and extrapolates linearly to the full step: the casts are
+# per-element work and the GEMM slabs cover a fraction of the output rows (or of the
+# contraction), so time scales with the slab. The numpy casts run on one thread; the
+# matmuls on as many threads as the BLAS is given.
+def _t(fn):
     t0 = time.perf_counter()
-    fl = sum(oracle_step(M) for _ in range(steps))
-    dt = time.perf_counter() - t0
-    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{steps} full steps ({M} tokens each): numpy oracle casts (one thread) and fp64 BLAS "
-                      f"matmuls (all cores); {dt:.1f} s"}
+    out = fn()
+    return time.perf_counter() - t0, out
+
+
+FINE_SLAB_COLS = 1792  # 14 of the 112 column blocks of W (and of y)
+
+
+def finegrained_slab(rows: int):
+    """The first `rows` rows of the headline's x and the first FINE_SLAB_COLS columns of its W
+    (the workload's own draws)."""
+    import numpy as np
+    from datagen import workload_inputs
+    w_in = workload_inputs("finegrained_fwd", M=rows)  # the first rows of the full x
+    return w_in["x"], np.ascontiguousarray(w_in["w"][:, :FINE_SLAB_COLS])
+
+
+def leg_finegrained(rows: int):
+    """x's 1x128 cast on `rows` of 16384 rows, W's 128x128 cast on 1792 of 14336 columns, the
+    block-scaled GEMM on the rows x 1792 output slab they give."""
+    from oracle import fp8, gemm, quant
+    M, K, N = FINE["M"], FINE["K"], FINE["N"]
+    x, w = finegrained_slab(rows)
+    t_x, ox = _t(lambda: quant.quantize_tile_1x128(x, fp8.E4M3))
+    t_w, ow = _t(lambda: quant.quantize_block_128x128(w, fp8.E4M3))
+    t_g, _ = _t(lambda: gemm.block_scaled_mm(ox["q"], fp8.E4M3, ox["d"], ow["qT"], fp8.E4M3, ow["d"]))
+    c = FINE_SLAB_COLS
+    parts = {"cast_x_1x128": t_x * M / rows, "cast_w_128x128": t_w * N / c, "gemm_block_scaled": t_g * (M / rows) * (N / c)}
+    return 2.0 * M * N * K, parts, (f"x 1x128 cast of {rows} of {M} rows, W 128x128 cast of {c} of {N} columns, "
+                                     f"block-scaled GEMM on the {rows} x {c} output slab; extrapolated linearly")
+
+
+def leg_backward(rows: int):
+    """dy's per-tensor E5M2 cast (current scaling) on `rows` of the 16384 rows; dgrad on `rows`
+    output rows; wgrad over `rows` of the 16384 tokens of its contraction."""
+    from datagen import normal_bf16, lognormal_grad_bf16
+    from oracle import fp8, gemm, quant
+    M, K, N = BWD["M"], BWD["K"], BWD["N"]
+    base = 3000
+    x = normal_bf16(base + 0, (rows, K))                 # the first rows of the workload's x
+    w = normal_bf16(base + 1, (K, N), 0.02)
+    dy = lognormal_grad_bf16(base + 2, (rows, N))        # the first rows of its dy
+    ow = quant.quantize_tensor(w, fp8.E4M3)
+    ox = quant.quantize_tensor(x, fp8.E4M3)
+    t_c, og = _t(lambda: quant.quantize_tensor(dy, fp8.E5M2))
+    t_d, _ = _t(lambda: gemm.scaled_mm(og["q"], fp8.E5M2, ow["q"], fp8.E4M3, og["d"], ow["d"]))
+    t_w, _ = _t(lambda: gemm.scaled_mm(ox["qT"], fp8.E4M3, og["qT"], fp8.E5M2, ox["d"], og["d"]))
+    f = M / rows
+    parts = {"cast_dy": t_c * f, "gemm_dgrad": t_d * f, "gemm_wgrad": t_w * f}
+    return 2 * 2.0 * M * N * K, parts, (f"dy cast on {rows} of {M} rows, dgrad on {rows} output rows, wgrad over "
+                                        f"{rows} of {M} tokens; extrapolated linearly")
+
+
+def leg_delayed_loop(rows: int):
+    """One layer-step with delayed scaling (states after one bootstrap step): the optimizer
+    step and W's full cast, x's and dy's casts on `rows` of the 32768 tokens, the forward and
+    dgrad on `rows` output rows, wgrad over `rows` tokens of its contraction."""
+    from datagen import normal_bf16, lognormal_grad_bf16, perturbation_f32
+    from oracle import fp8, gemm, linear, quant
+    M, K, N, H = LOOP["M"], LOOP["K"], LOOP["N"], LOOP["hist"]
+    base = 5000
+    x = normal_bf16(base + 0, (rows, K))
+    dy = lognormal_grad_bf16(base + 2, (rows, N))
+    w = normal_bf16(base + 100, (K, N), 0.02)
+    delta = perturbation_f32(base + 10_000 + 100 + 0, (K, N), 1e-3)
+    ws, xs, gs = quant.DelayedState(H), quant.DelayedState(H), quant.DelayedState(H)
+    for st, t, f in ((ws, w, fp8.E4M3), (xs, x, fp8.E4M3), (gs, dy, fp8.E5M2)):  # bootstrap step
+        st.quantize(t, f)
+        st.commit()
+    t_w, wo = _t(lambda: ws.quantize(linear.perturb_master(w, delta), fp8.E4M3))
+    t_x, xo = _t(lambda: xs.quantize(x, fp8.E4M3))
+    t_c, go = _t(lambda: gs.quantize(dy, fp8.E5M2))
+    t_f, _ = _t(lambda: gemm.scaled_mm(xo["q"], fp8.E4M3, wo["qT"], fp8.E4M3, xo["d"], wo["d"]))
+    t_d, _ = _t(lambda: gemm.scaled_mm(go["q"], fp8.E5M2, wo["q"], fp8.E4M3, go["d"], wo["d"]))
+    t_g, _ = _t(lambda: gemm.scaled_mm(xo["qT"], fp8.E4M3, go["qT"], fp8.E5M2, xo["d"], go["d"]))
+    f = M / rows
+    parts = {"update_cast_w": t_w, "cast_x": t_x * f, "cast_dy": t_c * f, "gemm_fwd": t_f * f,
+             "gemm_dgrad": t_d * f, "gemm_wgrad": t_g * f}
+    return 3 * 2.0 * M * N * K, parts, (f"one layer-step: W update + cast in full; x, dy casts on {rows} of {M} "
+                                        f"tokens; GEMMs on {rows} output rows (wgrad: {rows} tokens of its "
+                                        f"contraction); extrapolated linearly")
+
+
+def leg_gpt2(rows: int):
+    """The GPT-2-small step's arithmetic (current scaling) with the GEMMs on `rows` of the
+    8192 tokens; W's cast in full."""
+    from datagen import outlier_normal_bf16, normal_bf16, lognormal_grad_bf16
+    from oracle import fp8, gemm, quant
+    M, K, N = GPT2["M"], GPT2["K"], GPT2["N"]
+    x = outlier_normal_bf16(2000, (M, K))[:rows]
+    w = normal_bf16(2001, (K, N), 0.02)
+    dy = lognormal_grad_bf16(2002, (rows, N))
+    t_w, ow = _t(lambda: quant.quantize_tensor(w, fp8.E4M3))
+    t_x, ox = _t(lambda: quant.quantize_tensor(x, fp8.E4M3))
+    t_c, og = _t(lambda: quant.quantize_tensor(dy, fp8.E5M2))
+    t_f, _ = _t(lambda: gemm.scaled_mm(ox["q"], fp8.E4M3, ow["qT"], fp8.E4M3, ox["d"], ow["d"]))
+    t_d, _ = _t(lambda: gemm.scaled_mm(og["q"], fp8.E5M2, ow["q"], fp8.E4M3, og["d"], ow["d"]))
+    t_g, _ = _t(lambda: gemm.scaled_mm(ox["qT"], fp8.E4M3, og["qT"], fp8.E5M2, ox["d"], og["d"]))
+    f = M / rows
+    parts = {"cast_w": t_w, "cast_x": t_x * f, "cast_dy": t_c * f, "gemm_fwd": t_f * f, "gemm_dgrad": t_d * f,
+             "gemm_wgrad": t_g * f}
+    return 3 * 2.0 * M * N * K, parts, (f"W cast in full; x, dy casts and the GEMMs on {rows} of {M} tokens; "
+                                        f"extrapolated linearly (current scaling)")
+
+
+# leg name -> (function, slab rows with all cores, slab rows on one core)
+CPU_LEGS = {"finegrained": (leg_finegrained, 128, 64), "backward_upproj": (leg_backward, 1024, 256),
+            "delayed_loop": (leg_delayed_loop, 1024, 256), "gpt2s_train_step": (leg_gpt2, 2048, 512)}
+
+
+def run_cpu_leg(name: str, rows: int):
+    fn = CPU_LEGS[name][0]
+    t0 = time.perf_counter()
+    flops, parts, sample = fn(rows)
+    step_s = sum(parts.values())
+    return {"value": round(flops / step_s / 1e12, 6), "unit": "TFLOP/s", "step_s_extrapolated": round(step_s, 3),
+            "parts_s": {k: round(v, 4) for k, v in parts.items()}, "sample": sample,
+            "leg_wall_s": round(time.perf_counter() - t0, 2)}
+
+
+def cpu_baselines():
+    """Every leg twice, in child processes (started before this process uses the GPU): with the
+    BLAS on all host cores and on one core."""
+    out = {}
+    ncpu = os.cpu_count() or 1
+    for name, (_, rows_all, rows_one) in CPU_LEGS.items():
+        rec = {}
+        for threads, rows in ((ncpu, rows_all), (1, rows_one)):
+            env = dict(os.environ)
+            for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+                env[v] = str(threads)
+            env["CUDA_VISIBLE_DEVICES"] = ""
+            r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-leg", name, "--rows", str(rows)],
+                               capture_output=True, text=True, env=env, timeout=600)
+            try:
+                rec[threads] = json.loads(r.stdout.strip().splitlines()[-1])
+            except (IndexError, json.JSONDecodeError):
+                rec[threads] = {"error": (r.stderr or r.stdout)[-300:]}
+        a, o = rec[ncpu], rec[1]
+        out[name] = {"value": a.get("value"), "unit": "TFLOP/s", "cores": ncpu, "kind": "oracle",
+                     "sample": a.get("sample", "") + f"; numpy casts on one thread, fp64 BLAS matmuls on {ncpu} cores",
+                     "step_s_extrapolated": a.get("step_s_extrapolated"), "parts_s": a.get("parts_s"),
+                     "one_core": {"value": o.get("value"), "cores": 1, "sample": o.get("sample"),
+                                  "step_s_extrapolated": o.get("step_s_extrapolated")}}
+    return out
 
 
 def run_reference(args):
+    """The reference arm: the oracle on a bounded sample of the headline step per timed step
+    (x's 1x128 cast on 64 rows, W's 128x128 cast on 1792 columns, the block-scaled GEMM on the
+    64 x 1792 output slab), on the host cores; value = the GEMM FLOPs the sample covers per
+    second."""
     rank, _, world = env_rank()
     if rank != 0:
         return
-    tokens = 2048
+    from oracle import fp8, gemm, quant
+    M, K, N = FINE["M"], FINE["K"], FINE["N"]
+    rows, cols = 64, FINE_SLAB_COLS
+    x, w = finegrained_slab(rows)
+
+    def step():
+        ox = quant.quantize_tile_1x128(x, fp8.E4M3)
+        ow = quant.quantize_block_128x128(w, fp8.E4M3)
+        gemm.block_scaled_mm(ox["q"], fp8.E4M3, ox["d"], ow["qT"], fp8.E4M3, ow["d"])
+        return 2.0 * rows * cols * K
+
     for _ in range(args.warmup):
-        oracle_step(tokens)
+        step()
     t0 = time.perf_counter()
-    fl = 0.0
-    for _ in range(args.steps):
-        fl += oracle_step(tokens)
+    fl = sum(step() for _ in range(args.steps))
     dt = time.perf_counter() - t0
     value = fl / dt / 1e12
-    sample = f"{tokens} of {M} tokens per step (W in full), numpy oracle, fp64 BLAS matmuls"
+    sample = (f"per step: x 1x128 cast of {rows} of {M} rows, W 128x128 cast of {cols} of {N} columns, block-scaled "
+              f"GEMM on the {rows} x {cols} output slab; numpy oracle (casts on one thread), fp64 BLAS matmuls "
+              f"on all cores")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-        "config": {"workload": "gpt2s_upproj_train_step", "M_tokens": M, "d_model": K, "d_ff": N},
+        "config": {"workload": "finegrained_upproj_fwd", "M_tokens": M, "d_model": K, "d_ff": N},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -763,12 +1086,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true", help="time the headline step only (no sub-records)")
     ap.add_argument("--sweep", action="store_true", help="time every workload's GEMM and cast shapes instead")
     ap.add_argument("--only", default="", help="comma-separated sweep entries")
+    ap.add_argument("--cpu-leg", default="", help=argparse.SUPPRESS)
+    ap.add_argument("--rows", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.sweep:
+    if args.cpu_leg:
+        print(json.dumps(run_cpu_leg(args.cpu_leg, args.rows)))
+    elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -697,6 +697,309 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------------------
+// Block-scaled GEMM with 256-wide tiles: the fold keeps the whole tile in registers
+// ---------------------------------------------------------------------------------------
+// C[m, n] = bf16( sum_kb fl32(d_a[m, kb] d_b[kb, n/128]) P_kb[m, n] ): every 128-deep K block
+// is accumulated by the tensor cores in a fresh TMEM buffer (two of BN columns, alternating),
+// and eight fold warps multiply it by its scale product and add it into fp32 registers.
+// Warpgroup 0 holds the TMA producer (warp 0) and the MMA issuer (warp 1; warps 2-3 idle) and
+// gives registers up (setmaxnreg) to the fold warpgroups 1-2, whose threads each hold BN/2
+// accumulators: the two warps of a TMEM lane quarter split the tile's columns in halves, and
+// each half lies in one 128-column scale block of B. A thread loads its columns from TMEM in
+// 32-column chunks, the next chunk in flight while the current one is folded with packed
+// fp32 FMAs, and releases the TMEM buffer as soon as the block's last chunk is in registers.
+// With PAIR, two CTAs of a cluster share a 256 x BN tile through the CTA-pair MMA (each holds
+// its 128 rows of A and half of B's rows) and each folds its own 128 rows.
+template <int BN, bool PAIR>
+struct BlkCfg {
+  static_assert(BN == 128 || BN == 256, "tile width");
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;
+  static constexpr int B_BYTES = B_ROWS * BK;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int FOLD_WARPS = 8;
+  static constexpr int COLS = BN / 2;  // accumulator columns per fold thread
+  static constexpr int NCH = COLS / 32;
+  static constexpr int THREADS = 384;  // three warpgroups
+  static constexpr int STG = FOLD_WARPS * STG_BYTES;
+  static constexpr int STAGES_FIT = (230000 - STG) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT < (192 * 1024) / STAGE_BYTES ? STAGES_FIT : (192 * 1024) / STAGE_BYTES;
+  static constexpr int ACC = 512 / BN;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr int OFF_STG = STAGES * STAGE_BYTES;
+  static constexpr int OFF_BAR = OFF_STG + STG;
+  static constexpr int NBAR = 2 * STAGES + 2 * ACC + 1;  // full[S], empty[S], tfull[ACC], tempty[ACC], final
+  static constexpr int OFF_TMEM_SLOT = OFF_BAR + 8 * NBAR;
+  static constexpr int SMEM = OFF_TMEM_SLOT + 16 + 1024;
+  static constexpr int TEMPTY_COUNT = (PAIR ? 2 : 1) * FOLD_WARPS;
+  // register split: a CTA is launched with THREADS x LAUNCH_REGS registers; warpgroup 0 keeps
+  // CTRL_REGS per thread and the two fold warpgroups take FOLD_REGS (0: no split)
+  static constexpr int LAUNCH_REGS = 168;
+  static constexpr int CTRL_REGS = 56;
+  static constexpr int FOLD_REGS = BN == 256 ? 224 : 0;
+  static_assert(FOLD_REGS == 0 || 128 * CTRL_REGS + 256 * FOLD_REGS <= THREADS * LAUNCH_REGS, "register split");
+  static_assert(SMEM <= 232448, "shared memory");
+  static_assert(STAGES >= 3, "ring depth");
+};
+
+// acc[i], acc[i+1] += v[i], v[i+1] times s (two fp32 FMAs, round to nearest each).
+__device__ __forceinline__ void fma2(float& a0, float& a1, uint32_t v0, uint32_t v1, uint64_t ss) {
+  uint64_t acc = (static_cast<uint64_t>(__float_as_uint(a1)) << 32) | __float_as_uint(a0);
+  const uint64_t v = (static_cast<uint64_t>(v1) << 32) | v0;
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(v), "l"(ss));
+  a0 = __uint_as_float(static_cast<uint32_t>(acc));
+  a1 = __uint_as_float(static_cast<uint32_t>(acc >> 32));
+}
+
+template <int BN, bool PAIR>
+__global__ void __launch_bounds__(BlkCfg<BN, PAIR>::THREADS, 1)
+    gemm_blk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
+  using C = BlkCfg<BN, PAIR>;
+  constexpr int STAGES = C::STAGES;
+  constexpr int ACC = C::ACC;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar_full = sbase + C::OFF_BAR;
+  const uint32_t bar_empty = bar_full + 8 * STAGES;
+  const uint32_t bar_tfull = bar_empty + 8 * STAGES;
+  const uint32_t bar_tempty = bar_tfull + 8 * ACC;
+  const uint32_t bar_final = bar_tempty + 8 * ACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int tile0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tile_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  constexpr int TILE_M = PAIR ? 2 * BM : BM;
+  const KProb& pb = p.pr[0];  // one problem, never split
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int a = 0; a < ACC; ++a) {
+      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tempty + 8 * a, C::TEMPTY_COUNT);
+    }
+    mbar_init(bar_final, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+  }
+  if (warp == 1) {
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // the peer's barriers are initialised
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
+
+  if (warp < 4) {
+    if constexpr (C::FOLD_REGS > 0) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::CTRL_REGS));
+    if (warp == 0 && lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_phase = 0;
+      bool ok = true;
+      const uint32_t full_lead = PAIR ? mapa_shared(bar_full, 0) : bar_full;
+      for (int t = tile0; ok && t < pb.num_tiles; t += tile_step) {
+        int mb, nb;
+        tile_coords(t, pb.num_m, pb.num_n, mb, nb);
+        const int arow = mb * TILE_M + static_cast<int>(rank) * BM;
+        const int brow = nb * BN + static_cast<int>(rank) * C::B_ROWS;
+        for (int kb = 0; kb < pb.num_kb; ++kb) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.w, DEV_ERR_WAIT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full + 8 * stage;
+          const uint32_t sa = sbase + stage * C::STAGE_BYTES;
+          if constexpr (PAIR) {
+            if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
+            tma_load_2d_pair(sa, &tmA, full_lead + 8 * stage, kb * BK, arow);
+            tma_load_2d_pair(sa + A_BYTES, &tmB, full_lead + 8 * stage, kb * BK, brow);
+          } else {
+            mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+            tma_load_2d(sa, &tmA, fb, kb * BK, arow);
+            tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, brow);
+          }
+          issued_mask |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let every load already issued land before the CTA exits
+        if constexpr (PAIR) {
+          const unsigned long long t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 200000ull) {
+          }
+        } else {
+          for (int s = 0; s < STAGES; ++s)
+            if (issued_mask & (1u << s)) mbar_wait_drain(bar_full + 8 * s, (issued_phase >> s) & 1u, 1000000000ull);
+        }
+      }
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+      // ---------------- MMA issuer: one TMEM buffer per K block ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = tile0; ok && t < pb.num_tiles; t += tile_step) {
+        for (int kb = 0; kb < pb.num_kb; ++kb) {
+          if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.w, DEV_ERR_WAIT_MMA) ||
+              !mbar_wait(bar_full + 8 * stage, phase, p.w, DEV_ERR_WAIT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+          const uint32_t sa = sbase + stage * C::STAGE_BYTES;
+          const uint64_t adesc = smem_desc_sw128(sa);
+          const uint64_t bdesc = smem_desc_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k) {
+            if constexpr (PAIR)
+              mma_f8_pair(d, adesc + 2 * k, bdesc + 2 * k, pb.idesc, k != 0);
+            else
+              mma_f8(d, adesc + 2 * k, bdesc + 2 * k, pb.idesc, k != 0);
+          }
+          if constexpr (PAIR) {
+            mma_commit_pair(bar_empty + 8 * stage, 0x3);
+            mma_commit_pair(bar_tfull + 8 * acc, 0x3);
+          } else {
+            mma_commit(bar_empty + 8 * stage);
+            mma_commit(bar_tfull + 8 * acc);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          acc = (acc + 1 == ACC) ? 0 : acc + 1;
+          if (acc == 0) acc_phase ^= 1u;
+        }
+      }
+      if constexpr (PAIR)
+        mma_commit_pair(bar_final, 0x1);
+      else
+        mma_commit(bar_final);
+      if (!mbar_wait_drain(bar_final, 0, 1000000000ull)) atomicOr(p.w.err, DEV_ERR_WAIT_TEARDOWN);
+    }
+  } else {
+    // ---------------- fold (warpgroups 1-2) ----------------
+    if constexpr (C::FOLD_REGS > 0) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::FOLD_REGS));
+    constexpr int COLS = C::COLS, NCH = C::NCH;
+    const int fw = warp - 4;  // 0 .. 7
+    const int q = warp & 3;   // TMEM lane quarter
+    const int col0 = (fw >> 2) * COLS;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t tempty_lead = PAIR ? mapa_shared(bar_tempty, 0) : bar_tempty;
+    uint8_t* stg = smem + C::OFF_STG + fw * STG_BYTES;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = tile0; ok && t < pb.num_tiles; t += tile_step) {
+      int mb, nb;
+      tile_coords(t, pb.num_m, pb.num_n, mb, nb);
+      const int row0 = mb * TILE_M + static_cast<int>(rank) * BM + q * 32;  // this warp's 32 rows
+      const int row = row0 + lane;
+      const int nblk = (nb * BN + col0) / 128;
+      const bool row_ok = row < pb.M;
+      const bool col_ok = nblk * 128 < pb.N;
+      const float* sa_row = pb.sa + static_cast<int64_t>(row_ok ? row : 0) * pb.sa_ld;
+      const float* sb_col = pb.sb + (col_ok ? nblk : 0);
+      float accum[COLS];
+#pragma unroll
+      for (int j = 0; j < COLS; ++j) accum[j] = 0.0f;
+      float sa_n = row_ok ? __ldg(sa_row) : 0.0f;
+      float sb_n = col_ok ? __ldg(sb_col) : 0.0f;
+      uint32_t buf[2][32];
+      if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE)) break;
+      __syncwarp();
+      tc_fence_after();
+      tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), buf[0]);
+      for (int kb = 0; ok && kb < pb.num_kb; ++kb) {
+        const float sc = __fmul_rn(sa_n, sb_n);
+        const uint64_t ss = (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | __float_as_uint(sc);
+        const bool more = kb + 1 < pb.num_kb;
+        sa_n = (row_ok && more) ? __ldg(sa_row + kb + 1) : 0.0f;
+        sb_n = (col_ok && more) ? __ldg(sb_col + static_cast<int64_t>(kb + 1) * pb.sb_ld) : 0.0f;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+          uint32_t(&cur)[32] = buf[ch & 1];
+          uint32_t(&nxt)[32] = buf[(ch + 1) & 1];
+          tmem_ld_wait();
+          reg_fence(cur);
+          if (ch + 1 < NCH) {
+            tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0 + (ch + 1) * 32), nxt);
+          } else {
+            // the whole block is in registers: hand the buffer back, start on the next one
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (PAIR)
+                mbar_arrive_cluster(tempty_lead + 8 * acc);
+              else
+                mbar_arrive(bar_tempty + 8 * acc);
+            }
+            acc = (acc + 1 == ACC) ? 0 : acc + 1;
+            if (acc == 0) acc_phase ^= 1u;
+            if (more) {
+              ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE);
+              __syncwarp();
+              tc_fence_after();
+              if (ok) tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), nxt);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) fma2(accum[ch * 32 + j], accum[ch * 32 + j + 1], cur[j], cur[j + 1], ss);
+        }
+      }
+      if (!ok) break;
+      // bf16 out, 64 columns per staged TMA store
+#pragma unroll
+      for (int c = 0; c < COLS / 64; ++c) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(accum[c * 64 + 2 * j], accum[c * 64 + 2 * j + 1]);
+        if (lane == 0) bulk_wait_group_read<0>();  // the staging buffer's previous store has read it
+        __syncwarp();
+        const int cc = nb * BN + col0 + c * 64;
+        if (row0 < pb.M && cc < pb.N) stage_and_store(stg, pk, lane, &tmC, cc, row0);
+      }
+    }
+    if (lane == 0) bulk_wait_group<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1021,6 +1324,99 @@ cudaError_t launch_choice(const TileChoice& c, const Maps& m0, const Maps& m1, c
   return launch_kernel<false, 128, QF, false>(m0, m1, tq, p, stream);
 }
 
+// The block-scaled kernel's launch configuration on the current device: shared memory set,
+// the register split checked (setmaxnreg.inc waits until the CTA's pool holds the registers it
+// asks for, so a kernel compiled with fewer registers than the split assumes is never launched)
+// and, for CTA pairs, the pairs the device holds at once.
+template <int BN, bool PAIR>
+cudaError_t prepare_blk(int* slots, const char** why) {
+  using C = BlkCfg<BN, PAIR>;
+  static bool done[64] = {};
+  static int cached[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev < 64 && done[dev]) {
+    *slots = cached[dev];
+    return cudaSuccess;
+  }
+  cudaFuncAttributes fa{};
+  if ((e = cudaFuncGetAttributes(&fa, gemm_blk_kernel<BN, PAIR>)) != cudaSuccess) return e;
+  if (C::FOLD_REGS > 0 && fa.numRegs < C::LAUNCH_REGS) {
+    *why = "block-scaled GEMM: kernel compiled with fewer registers than its register split needs";
+    return cudaErrorInvalidConfiguration;
+  }
+  if ((e = cudaFuncSetAttribute(gemm_blk_kernel<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM)) !=
+      cudaSuccess)
+    return e;
+  int n = num_sms();
+  if (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(gemm_blk_kernel<BN, PAIR>), &cfg)) !=
+        cudaSuccess)
+      return e;
+  }
+  if (dev < 64) {
+    done[dev] = true;
+    cached[dev] = n;
+  }
+  *slots = n;
+  return cudaSuccess;
+}
+
+template <int BN, bool PAIR>
+cudaError_t launch_blk(const Maps& m, KParams& p, cudaStream_t stream, const char** why) {
+  using C = BlkCfg<BN, PAIR>;
+  int slots = 0;
+  cudaError_t e = prepare_blk<BN, PAIR>(&slots, why);
+  if (e != cudaSuccess) return e;
+  if (slots <= 0) return cudaErrorInvalidConfiguration;
+  if (slots > p.pr[0].num_tiles) slots = p.pr[0].num_tiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? 2 * slots : slots));
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (PAIR) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, gemm_blk_kernel<BN, PAIR>, m.a, m.b, m.c, p);
+}
+
+// Pairs of the block-scaled kernel the device holds at once (0: no clusters of two).
+int blk_pair_capacity() {
+  int n = 0;
+  const char* why = nullptr;
+  if (prepare_blk<256, true>(&n, &why) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 // Pairs the device holds at once (0 when it cannot launch clusters of two).
 int pair_capacity() {
   int n = 0;
@@ -1055,10 +1451,17 @@ int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why) {
-  // block scaling folds every 128-deep K block out of TMEM: 128-wide single-CTA tiles keep
-  // the fold's registers (64 fp32 per thread) and its four accumulator buffers within budget
-  TileChoice choice{128, false, 1};
-  if (!g.block_scaled) {
+  // block scaling folds every 128-deep K block out of TMEM into registers: 256-wide tiles
+  // (two TMEM buffers) unless N is one 128-column block, on CTA pairs when M has more than
+  // one row block
+  TileChoice choice{g.N > 128 ? 256 : 128, false, 1};
+  if (g.block_scaled) {
+#ifdef FP8GB_BLK_FORCE_PAIR  // compile-time override, for tuning builds
+    choice.pair = FP8GB_BLK_FORCE_PAIR != 0 && g.M > BM;
+#else
+    choice.pair = g.M > BM && blk_pair_capacity() > 0;
+#endif
+  } else {
 #ifdef FP8GB_FORCE_BN  // compile-time override of the tile choice, for tuning builds
 #ifndef FP8GB_FORCE_PAIR
 #define FP8GB_FORCE_PAIR 0
@@ -1093,7 +1496,11 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why
     }
     p.cst = g.cst;
   }
-  if (g.block_scaled) return launch_kernel<true, 128, -1, false>(m0, m0, tq, p, stream);
+  if (g.block_scaled) {
+    if (choice.bn == 256)
+      return choice.pair ? launch_blk<256, true>(m0, p, stream, why) : launch_blk<256, false>(m0, p, stream, why);
+    return choice.pair ? launch_blk<128, true>(m0, p, stream, why) : launch_blk<128, false>(m0, p, stream, why);
+  }
   if (g.qf == 0) return launch_choice<0>(choice, m0, m0, tq, p, stream);
   if (g.qf == 1) return launch_choice<1>(choice, m0, m0, tq, p, stream);
   return launch_choice<-1>(choice, m0, m0, tq, p, stream);
