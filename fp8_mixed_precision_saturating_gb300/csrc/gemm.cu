@@ -23,8 +23,9 @@
 // therefore runs on CTA pairs (clusters of two, tcgen05 cta_group::2): the pair computes a
 // 256 x BN tile, each CTA loads its own 128 rows of A and half of B's BN rows, the even
 // CTA issues the MMAs, and both CTAs drain their half of the accumulator.
-// Block scaled: every 128-deep K block gets a fresh accumulator buffer (four, rotating),
-// and 8 epilogue warps fold each block into fp32 registers with its scale product.
+// Block scaled (gemm_blk_kernel): every 128-deep K block gets a fresh accumulator buffer
+// (two of 256 columns, alternating), and 8 fold warps multiply it by its scale product and
+// add it into fp32 registers.
 // Every mbarrier wait is bounded (see ptx.cuh); on a timeout the CTA stops issuing work,
 // drains what it issued and frees its TMEM.
 #include <cuda.h>
@@ -65,17 +66,14 @@ constexpr int GROUP_M = 16;          // tile raster: 16 M-blocks share each B ti
 // PAIR: two CTAs of a cluster share one 256 x BN tile through the CTA-pair MMA; each holds
 // its 128 rows of A and half of B's BN rows, so a CTA loads 16 KB + BN * 64 bytes per
 // 128-deep K block instead of 16 KB + BN * 128 for the same tensor work.
-template <bool BLOCK, int BN, int QF, bool PAIR = false>
+template <int BN, int QF, bool PAIR = false>
 struct Cfg {
   static_assert(BN == 128 || BN == 192 || BN == 256, "tile width");
-  static_assert(QF < 0 || !BLOCK, "FP8 output with per-tensor scales only");
-  static_assert(!(PAIR && BLOCK), "CTA pairs with per-tensor scales only");
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;   // B rows this CTA loads per stage
   static constexpr int B_BYTES = B_ROWS * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // per tensor: two warps per TMEM lane quarter, each draining half of the tile's columns;
-  // block scaled: one warp per lane quarter and 64 columns
-  static constexpr int EPI_WARPS = BLOCK ? 4 * (BN / 64) : 8;
+  // two warps per TMEM lane quarter, each draining half of the tile's columns
+  static constexpr int EPI_WARPS = 8;
   static constexpr int QSTG_PER_WARP = QF >= 0 ? QSTG_BYTES : 0;
   static constexpr int STAGES_FIT = (230000 - EPI_WARPS * (STG_BYTES + QSTG_PER_WARP)) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT < (192 * 1024) / STAGE_BYTES ? STAGES_FIT : (192 * 1024) / STAGE_BYTES;
@@ -225,13 +223,13 @@ __device__ __forceinline__ void stage_and_store(uint8_t* stg, const uint32_t (&p
   }
 }
 
-template <bool BLOCK, int BN, int QF, bool PAIR>
-__global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
+template <int BN, int QF, bool PAIR>
+__global__ void __launch_bounds__(Cfg<BN, QF, PAIR>::THREADS, 1)
     gemm_f8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ KParams p) {
-  using C = Cfg<BLOCK, BN, QF, PAIR>;
+  using C = Cfg<BN, QF, PAIR>;
   constexpr int STAGES = C::STAGES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
   constexpr uint32_t TMEM_COLS = C::TMEM_COLS;
@@ -365,18 +363,9 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
         KProb q;
         const Unit un = unit_at(u, p, q);
         const int kb0 = un.kb0, kb1 = un.kb1;
-        if (!BLOCK) {
-          if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.w, DEV_ERR_WAIT_MMA)) break;
-          tc_fence_after();
-        }
+        if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.w, DEV_ERR_WAIT_MMA)) break;
+        tc_fence_after();
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (BLOCK) {
-            if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.w, DEV_ERR_WAIT_MMA)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
           if (!mbar_wait(bar_full + 8 * stage, phase, p.w, DEV_ERR_WAIT_MMA)) {
             ok = false;
             break;
@@ -391,7 +380,7 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
           const uint64_t bdesc = smem_desc_sw128(sa + A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k) {
-            const uint32_t accumulate = BLOCK ? (k != 0) : (kb != kb0 || k != 0);
+            const uint32_t accumulate = (kb != kb0 || k != 0);
             if constexpr (PAIR)
               mma_f8_pair(d, adesc + 2 * k, bdesc + 2 * k, q.idesc, accumulate);
             else
@@ -405,13 +394,8 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
             stage = 0;
             phase ^= 1u;
           }
-          if (BLOCK) {
-            mma_commit(bar_tfull + 8 * acc);
-            acc = (acc + 1 == ACC) ? 0 : acc + 1;
-            if (acc == 0) acc_phase ^= 1u;
-          }
         }
-        if (!BLOCK && ok) {
+        if (ok) {
           if constexpr (PAIR)
             mma_commit_pair(bar_tfull + 8 * acc, 0x3);  // both halves of the tile are ready
           else
@@ -438,7 +422,7 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    if constexpr (!BLOCK) {
+    {
       const float dd0 = __fmul_rn(__ldg(p.pr[0].sa), __ldg(p.pr[0].sb));
       const float dd1 = p.nprob > 1 ? __fmul_rn(__ldg(p.pr[1].sa), __ldg(p.pr[1].sb)) : dd0;
       // FP8 output: with a non-empty history the epilogue casts the bf16 result with the
@@ -611,71 +595,6 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
           castops::atomic_max_amax(p.cst.amax_cur, qam);
         }
       }
-    } else {
-      // each warp folds 64 columns (half of the 128-column scale block) of its TMEM lane
-      // quarter, as two 32-column chunks per K block. The load of the next chunk is in flight
-      // while the current one is folded (software pipeline over chunks), so a TMEM round trip
-      // overlaps 32 FMAs instead of stalling the warp.
-      const int col0 = (ew >> 2) * 64;
-      const KProb& pb = p.pr[0];  // block scaling: one problem, never split
-      for (int t = tile0; ok && t < pb.num_tiles; t += tile_step) {
-        int mb, nb;
-        tile_coords(t, pb.num_m, pb.num_n, mb, nb);
-        const int row = mb * BM + q * 32 + lane;
-        const int nblk = (nb * BN + col0) / 128;
-        const bool row_ok = row < pb.M;
-        const bool col_ok = nblk * 128 < pb.N;
-        const float* sa_row = pb.sa + (int64_t)row * pb.sa_ld;
-        const float* sb_col = pb.sb + nblk;
-        float accum[64];
-#pragma unroll
-        for (int j = 0; j < 64; ++j) accum[j] = 0.0f;
-        float sa_n = row_ok ? __ldg(sa_row) : 0.0f;
-        float sb_n = col_ok ? __ldg(sb_col) : 0.0f;
-        uint32_t ra[32], rb[32];
-        if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE)) break;
-        __syncwarp();
-        tc_fence_after();
-        tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), ra);
-        tmem_ld_wait();
-        reg_fence(ra);
-        for (int kb = 0; kb < pb.num_kb; ++kb) {
-          const float sc = __fmul_rn(sa_n, sb_n);
-          const bool more = kb + 1 < pb.num_kb;
-          sa_n = (row_ok && more) ? __ldg(sa_row + kb + 1) : 0.0f;
-          sb_n = (col_ok && more) ? __ldg(sb_col + (int64_t)(kb + 1) * pb.sb_ld) : 0.0f;
-          tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0 + 32), rb);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) accum[j] = fmaf(__uint_as_float(ra[j]), sc, accum[j]);
-          tmem_ld_wait();
-          reg_fence(rb);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);  // block kb is in registers
-          acc = (acc + 1 == ACC) ? 0 : acc + 1;
-          if (acc == 0) acc_phase ^= 1u;
-          if (more) {
-            ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE);
-            __syncwarp();
-            tc_fence_after();
-            if (ok) tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), ra);
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) accum[32 + j] = fmaf(__uint_as_float(rb[j]), sc, accum[32 + j]);
-          if (!ok) break;
-          if (more) {
-            tmem_ld_wait();
-            reg_fence(ra);
-          }
-        }
-        if (!ok) break;
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(accum[2 * j], accum[2 * j + 1]);
-        if (lane == 0) bulk_wait_group_read<0>();
-        __syncwarp();
-        stage_and_store(stg, pk, lane, &tmC, nb * BN + col0, mb * BM + q * 32);
-      }
     }
     if (lane == 0) bulk_wait_group<0>();
     if (warp == 2 && lane == 0) FP8GB_STAMP(5);
@@ -706,8 +625,13 @@ __global__ void __launch_bounds__(Cfg<BLOCK, BN, QF, PAIR>::THREADS, 1)
 // gives registers up (setmaxnreg) to the fold warpgroups 1-2, whose threads each hold BN/2
 // accumulators: the two warps of a TMEM lane quarter split the tile's columns in halves, and
 // each half lies in one 128-column scale block of B. A thread loads its columns from TMEM in
-// 32-column chunks, the next chunk in flight while the current one is folded with packed
-// fp32 FMAs, and releases the TMEM buffer as soon as the block's last chunk is in registers.
+// 64-column chunks through one register buffer, folds each with packed fp32 FMAs, and
+// releases the TMEM buffer as soon as the block's last chunk is in registers. With two
+// buffers the MMA runs one block ahead of the fold, so the release of a buffer (its wake-up,
+// loads and first chunk's FMAs) sits on the tensor pipe's critical path: measured at
+// 16384 x 14336 x 4096, the fold's FMAs cost 0.19 of the 0.80 ms and the per-block hand-over
+// without them ~0.08 against the per-tensor kernel's 0.54 ms. (32-column chunks with the next
+// one in flight measured the same; plain scalar FMAs 11 % slower.)
 // With PAIR, two CTAs of a cluster share a 256 x BN tile through the CTA-pair MMA (each holds
 // its 128 rows of A and half of B's rows) and each folds its own 128 rows.
 template <int BN, bool PAIR>
@@ -718,7 +642,6 @@ struct BlkCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int FOLD_WARPS = 8;
   static constexpr int COLS = BN / 2;  // accumulator columns per fold thread
-  static constexpr int NCH = COLS / 32;
   static constexpr int THREADS = 384;  // three warpgroups
   static constexpr int STG = FOLD_WARPS * STG_BYTES;
   static constexpr int STAGES_FIT = (230000 - STG) / STAGE_BYTES;
@@ -741,13 +664,19 @@ struct BlkCfg {
   static_assert(STAGES >= 3, "ring depth");
 };
 
-// acc[i], acc[i+1] += v[i], v[i+1] times s (two fp32 FMAs, round to nearest each).
-__device__ __forceinline__ void fma2(float& a0, float& a1, uint32_t v0, uint32_t v1, uint64_t ss) {
-  uint64_t acc = (static_cast<uint64_t>(__float_as_uint(a1)) << 32) | __float_as_uint(a0);
-  const uint64_t v = (static_cast<uint64_t>(v1) << 32) | v0;
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(v), "l"(ss));
-  a0 = __uint_as_float(static_cast<uint32_t>(acc));
-  a1 = __uint_as_float(static_cast<uint32_t>(acc >> 32));
+// a0, a1 += fp32(v0) * s, fp32(v1) * s: two fp32 FMAs (round to nearest each) in one packed
+// instruction. The pairs are formed with mov.b64 inside the asm so that ptxas can keep each
+// accumulator pair in an aligned register pair (measured 4 % faster for the whole GEMM than
+// building the 64-bit operands with shifts).
+__device__ __forceinline__ void fma2(float& a0, float& a1, uint32_t v0, uint32_t v1, float s) {
+  asm("{\n\t.reg .b64 a, v, s;\n\t"
+      "mov.b64 a, {%0, %1};\n\t"
+      "mov.b64 v, {%2, %3};\n\t"
+      "mov.b64 s, {%4, %4};\n\t"
+      "fma.rn.f32x2 a, v, s, a;\n\t"
+      "mov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(v0), "r"(v1), "f"(s));
 }
 
 template <int BN, bool PAIR>
@@ -903,7 +832,7 @@ __global__ void __launch_bounds__(BlkCfg<BN, PAIR>::THREADS, 1)
   } else {
     // ---------------- fold (warpgroups 1-2) ----------------
     if constexpr (C::FOLD_REGS > 0) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::FOLD_REGS));
-    constexpr int COLS = C::COLS, NCH = C::NCH;
+    constexpr int COLS = C::COLS;
     const int fw = warp - 4;  // 0 .. 7
     const int q = warp & 3;   // TMEM lane quarter
     const int col0 = (fw >> 2) * COLS;
@@ -926,29 +855,30 @@ __global__ void __launch_bounds__(BlkCfg<BN, PAIR>::THREADS, 1)
       float accum[COLS];
 #pragma unroll
       for (int j = 0; j < COLS; ++j) accum[j] = 0.0f;
-      float sa_n = row_ok ? __ldg(sa_row) : 0.0f;
-      float sb_n = col_ok ? __ldg(sb_col) : 0.0f;
-      uint32_t buf[2][32];
+      // scales two K blocks ahead: an L2 round trip is longer than one block's fold
+      float sa1 = row_ok ? __ldg(sa_row) : 0.0f, sb1 = col_ok ? __ldg(sb_col) : 0.0f;
+      float sa2 = (row_ok && pb.num_kb > 1) ? __ldg(sa_row + 1) : 0.0f;
+      float sb2 = (col_ok && pb.num_kb > 1) ? __ldg(sb_col + pb.sb_ld) : 0.0f;
       if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE)) break;
       __syncwarp();
       tc_fence_after();
-      tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), buf[0]);
+      uint32_t buf[64];
+      tmem_ld64(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), buf);
       for (int kb = 0; ok && kb < pb.num_kb; ++kb) {
-        const float sc = __fmul_rn(sa_n, sb_n);
-        const uint64_t ss = (static_cast<uint64_t>(__float_as_uint(sc)) << 32) | __float_as_uint(sc);
+        const float sc = __fmul_rn(sa1, sb1);
         const bool more = kb + 1 < pb.num_kb;
-        sa_n = (row_ok && more) ? __ldg(sa_row + kb + 1) : 0.0f;
-        sb_n = (col_ok && more) ? __ldg(sb_col + static_cast<int64_t>(kb + 1) * pb.sb_ld) : 0.0f;
+        sa1 = sa2;
+        sb1 = sb2;
+        sa2 = (row_ok && kb + 2 < pb.num_kb) ? __ldg(sa_row + kb + 2) : 0.0f;
+        sb2 = (col_ok && kb + 2 < pb.num_kb) ? __ldg(sb_col + static_cast<int64_t>(kb + 2) * pb.sb_ld) : 0.0f;
+        // 64-column chunks through one buffer: two TMEM round trips per block (four with
+        // 32-column chunks), the buffer handed back once the last chunk has landed
+        constexpr int NC64 = COLS / 64;
 #pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          uint32_t(&cur)[32] = buf[ch & 1];
-          uint32_t(&nxt)[32] = buf[(ch + 1) & 1];
+        for (int ch = 0; ch < NC64; ++ch) {
           tmem_ld_wait();
-          reg_fence(cur);
-          if (ch + 1 < NCH) {
-            tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0 + (ch + 1) * 32), nxt);
-          } else {
-            // the whole block is in registers: hand the buffer back, start on the next one
+          reg_fence(buf);
+          if (ch + 1 == NC64) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -959,15 +889,17 @@ __global__ void __launch_bounds__(BlkCfg<BN, PAIR>::THREADS, 1)
             }
             acc = (acc + 1 == ACC) ? 0 : acc + 1;
             if (acc == 0) acc_phase ^= 1u;
-            if (more) {
-              ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE);
-              __syncwarp();
-              tc_fence_after();
-              if (ok) tmem_ld32(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), nxt);
-            }
           }
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) fma2(accum[ch * 32 + j], accum[ch * 32 + j + 1], cur[j], cur[j + 1], ss);
+          for (int j = 0; j < 64; j += 2) fma2(accum[ch * 64 + j], accum[ch * 64 + j + 1], buf[j], buf[j + 1], sc);
+          if (ch + 1 < NC64) {
+            tmem_ld64(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0 + (ch + 1) * 64), buf);
+          } else if (more) {
+            ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE);
+            __syncwarp();
+            tc_fence_after();
+            if (ok) tmem_ld64(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), buf);
+          }
         }
       }
       if (!ok) break;
@@ -1024,14 +956,14 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t
   return encode_tmap_2d(m, base, dt, inner, outer, row_bytes, box_inner, box_outer, 128);
 }
 
-template <bool BLOCK, int BN, int QF, bool PAIR>
+template <int BN, int QF, bool PAIR>
 cudaError_t prepare_kernel(int* pair_clusters) {
   // the attribute is per device; remember which devices were configured and, for CTA-pair
   // kernels, how many pairs the device holds at once
   static bool done[64] = {};
   static int clusters[64] = {};
   static std::mutex mu;
-  using C = Cfg<BLOCK, BN, QF, PAIR>;
+  using C = Cfg<BN, QF, PAIR>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1040,7 +972,7 @@ cudaError_t prepare_kernel(int* pair_clusters) {
     *pair_clusters = clusters[dev];
     return cudaSuccess;
   }
-  e = cudaFuncSetAttribute(gemm_f8_kernel<BLOCK, BN, QF, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  e = cudaFuncSetAttribute(gemm_f8_kernel<BN, QF, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   int n = 0;
   if (PAIR) {
@@ -1055,7 +987,7 @@ cudaError_t prepare_kernel(int* pair_clusters) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(gemm_f8_kernel<BLOCK, BN, QF, PAIR>), &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(gemm_f8_kernel<BN, QF, PAIR>), &cfg);
     if (e != cudaSuccess) return e;
   }
   if (dev < 64) {
@@ -1278,11 +1210,11 @@ void make_schedule(KParams& p, int slots) {
   for (size_t i = 0; i < sc.unit.size(); ++i) p.sched_unit[i] = sc.unit[i];
 }
 
-template <bool BLOCK, int BN, int QF, bool PAIR>
+template <int BN, int QF, bool PAIR>
 cudaError_t launch_kernel(const Maps& m0, const Maps& m1, const CUtensorMap& tq, KParams& p, cudaStream_t stream) {
-  using C = Cfg<BLOCK, BN, QF, PAIR>;
+  using C = Cfg<BN, QF, PAIR>;
   int clusters = 0;
-  cudaError_t e = prepare_kernel<BLOCK, BN, QF, PAIR>(&clusters);
+  cudaError_t e = prepare_kernel<BN, QF, PAIR>(&clusters);
   if (e != cudaSuccess) return e;
   int slots = PAIR ? clusters : num_sms();
   if (slots <= 0) return cudaErrorInvalidConfiguration;
@@ -1308,20 +1240,20 @@ cudaError_t launch_kernel(const Maps& m0, const Maps& m1, const CUtensorMap& tq,
   ++na;
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_f8_kernel<BLOCK, BN, QF, PAIR>, m0.a, m0.b, m0.c, tq, m1.a, m1.b, m1.c, p);
+  return cudaLaunchKernelEx(&cfg, gemm_f8_kernel<BN, QF, PAIR>, m0.a, m0.b, m0.c, tq, m1.a, m1.b, m1.c, p);
 }
 
 template <int QF>
 cudaError_t launch_choice(const TileChoice& c, const Maps& m0, const Maps& m1, const CUtensorMap& tq, KParams& p,
                           cudaStream_t stream) {
   if (c.pair) {
-    if (c.bn == 256) return launch_kernel<false, 256, QF, true>(m0, m1, tq, p, stream);
-    if (c.bn == 192) return launch_kernel<false, 192, QF, true>(m0, m1, tq, p, stream);
-    return launch_kernel<false, 128, QF, true>(m0, m1, tq, p, stream);
+    if (c.bn == 256) return launch_kernel<256, QF, true>(m0, m1, tq, p, stream);
+    if (c.bn == 192) return launch_kernel<192, QF, true>(m0, m1, tq, p, stream);
+    return launch_kernel<128, QF, true>(m0, m1, tq, p, stream);
   }
-  if (c.bn == 256) return launch_kernel<false, 256, QF, false>(m0, m1, tq, p, stream);
-  if (c.bn == 192) return launch_kernel<false, 192, QF, false>(m0, m1, tq, p, stream);
-  return launch_kernel<false, 128, QF, false>(m0, m1, tq, p, stream);
+  if (c.bn == 256) return launch_kernel<256, QF, false>(m0, m1, tq, p, stream);
+  if (c.bn == 192) return launch_kernel<192, QF, false>(m0, m1, tq, p, stream);
+  return launch_kernel<128, QF, false>(m0, m1, tq, p, stream);
 }
 
 // The block-scaled kernel's launch configuration on the current device: shared memory set,
@@ -1420,7 +1352,7 @@ int blk_pair_capacity() {
 // Pairs the device holds at once (0 when it cannot launch clusters of two).
 int pair_capacity() {
   int n = 0;
-  if (prepare_kernel<false, 256, -1, true>(&n) != cudaSuccess) {
+  if (prepare_kernel<256, -1, true>(&n) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }

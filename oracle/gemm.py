@@ -9,6 +9,8 @@ Definitions (A [M,K] and B [N,K] are code arrays, both contracted over K):
 * per-tensor:   C_ij = bf16( fl32(d_a * d_b) * sum_k a_ik * b_jk )
 * block scaled: C_ij = bf16( sum_kb fl32(d_a[i,kb] * d_b[kb, j // 128]) * P_ij,kb ),
                 P_ij,kb = sum over k in K-block kb of a_ik * b_jk
+* MX scaled:    C_ij = bf16( sum_g 2^(e_a[i,g] + e_b[j,g]) * P_ij,g ), P_ij,g the sum over the
+                g-th group of 32 consecutive k (power-of-two scales, one per row and group)
 with a, b the decoded FP8 values, the sums taken over the reals and bf16 the
 round-to-nearest-even rounding of the real result.
 
@@ -203,6 +205,49 @@ def block_scaled_mm_sampled(a_codes, fa, d_a, b_codes, fb, d_b, rows, cols):
             if sums[i]:
                 tot[i] += Fraction(float(sc[i])) * sums[i]
         mag += sc.astype(np.float64) * np.einsum("ik,ik->i", Ad[:, ks], Bd[:, ks])
+    ref = np.array([bf16_round_exact(t * unit) for t in tot], dtype=np.float64)
+    return ref, mag
+
+
+MX = 32
+
+
+def mx_scaled_mm(a_codes, fa, e_a, b_codes, fb, e_b):
+    """MX-scaled A [M,K] (exponents e_a [M, K/32]) times B [N,K] (e_b [N, K/32]).  Every
+    term is a code product times a power of two, so each group's sum scaled by 2^(e_a + e_b)
+    and the sum over groups are exact in fp64 while the partial sums fit 53 bits (the
+    sampled form below is exact always).  Returns (C_ref, bound magnitude)."""
+    A = _dec(a_codes, fa)
+    B = _dec(b_codes, fb)
+    M, K = A.shape
+    acc = np.zeros((M, B.shape[0]))
+    mag = np.zeros((M, B.shape[0]))
+    for g in range(K // MX):
+        ks = slice(g * MX, (g + 1) * MX)
+        sc = np.ldexp(1.0, (np.asarray(e_a)[:, g][:, None] + np.asarray(e_b)[:, g][None, :]).astype(np.int64))
+        acc += sc * (A[:, ks] @ B[:, ks].T)
+        mag += sc * (np.abs(A[:, ks]) @ np.abs(B[:, ks]).T)
+    return bf16_round(acc), mag
+
+
+def mx_scaled_mm_sampled(a_codes, fa, e_a, b_codes, fb, e_b, rows, cols):
+    """The MX definition for selected outputs, exactly: integer group sums times exact powers
+    of two, rounded once."""
+    ai, bi, A, B = _sampled_ints(a_codes, fa, b_codes, fb, rows, cols)
+    K = ai.shape[1]
+    unit = Fraction(1, 1 << (_SHIFT[fa] + _SHIFT[fb]))
+    ea = np.asarray(e_a)[rows]
+    eb = np.asarray(e_b)[cols]
+    tot = [Fraction(0)] * len(rows)
+    mag = np.zeros(len(rows))
+    Ad, Bd = np.abs(_dec(A, fa)), np.abs(_dec(B, fb))
+    for g in range(K // MX):
+        ks = slice(g * MX, (g + 1) * MX)
+        sums = _exact_row_dots(ai[:, ks], bi[:, ks])
+        for i in range(len(rows)):
+            if sums[i]:
+                tot[i] += Fraction(2) ** int(ea[i, g] + eb[i, g]) * sums[i]
+        mag += np.ldexp(1.0, (ea[:, g] + eb[:, g]).astype(np.int64)) * np.einsum("ik,ik->i", Ad[:, ks], Bd[:, ks])
     ref = np.array([bf16_round_exact(t * unit) for t in tot], dtype=np.float64)
     return ref, mag
 

@@ -24,6 +24,12 @@ Definitions (readings where the pages leave a step open):
   amax_eff = max of the filled entries when n > 0, else (bootstrap) the current amax.
   Each cast records its own current amax; ``commit`` pushes it at index n % hist_len.
 
+* MX units (hardware block scaling): 32 consecutive elements along the contraction
+  dimension share a power-of-two scale 2^e, stored as one UE8M0 byte e + 127.  e is the
+  smallest integer with FP8_MAX * 2^e >= amax of the 32 elements, so no element saturates;
+  e = 0 when that amax is zero or not finite; e is clamped to [-127, 127] (the byte's
+  range without its NaN code).  The cast is the same q = cast(fl32(x * 2^-e)).
+
 Parity: amax, scales, codes and counters are pinned by brute-force tests on small
 arrays (tests/test_oracle_quant.py).  The delayed-scaling state machine is "parity
 unpinned" by the pages beyond those invariants (the pages name the technique only).
@@ -131,6 +137,48 @@ def quantize_block_128x128(w_bits: np.ndarray, fmt: str):
             ov += o
             un += u
     return dict(q=q, qT=np.ascontiguousarray(q.T), d=d, s=s, amax=am, overflow=ov, underflow=un)
+
+
+MX_BLOCK = 32
+
+
+def mx_exponent(a, fmt: str) -> int:
+    """The MX scale exponent of a group with amax a: the smallest integer e with
+    FP8_MAX * 2^e >= a, clamped to [-127, 127]; 0 for a zero or non-finite a."""
+    a = float(np.float32(a))
+    if not (np.isfinite(a) and a > 0):
+        return 0
+    mx = fp8.fp8_max(fmt)
+    e = int(np.ceil(np.log2(a / mx)))
+    while mx * 2.0 ** e < a:          # exact comparisons settle the logarithm's rounding
+        e += 1
+    while mx * 2.0 ** (e - 1) >= a:
+        e -= 1
+    return max(-127, min(127, e))
+
+
+def quantize_mx(x_bits: np.ndarray, fmt: str):
+    """MX scaling along the last axis of a [R, C] array (C % 32 == 0): one power-of-two
+    scale per 32 consecutive elements of a row.  Returns dict(q [R, C], e [R, C/32] int,
+    ue8m0 [R, C/32] uint8 = e + 127, amax [R, C/32], overflow, underflow)."""
+    R, C = x_bits.shape
+    assert C % MX_BLOCK == 0
+    G = C // MX_BLOCK
+    q = np.empty((R, C), dtype=np.uint8)
+    e = np.empty((R, G), dtype=np.int64)
+    am = np.empty((R, G), dtype=np.float32)
+    ov = un = 0
+    for i in range(R):
+        for g in range(G):
+            unit = x_bits[i, g * MX_BLOCK:(g + 1) * MX_BLOCK]
+            a = amax(unit)
+            ei = mx_exponent(a, fmt)
+            qi, o, u = cast_with_scale(unit, np.float32(2.0 ** -ei), fmt)
+            q[i, g * MX_BLOCK:(g + 1) * MX_BLOCK] = qi
+            e[i, g], am[i, g] = ei, a
+            ov += o
+            un += u
+    return dict(q=q, e=e, ue8m0=(e + 127).astype(np.uint8), amax=am, overflow=ov, underflow=un)
 
 
 class DelayedState:

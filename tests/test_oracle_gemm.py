@@ -205,3 +205,38 @@ def test_bf16_round_exact_against_torch_and_ties():
     assert gemm.bf16_round_exact(-(Fraction(1) + Fraction(1, 256) + Fraction(1, 2 ** 60))) == -(1.0 + 2 ** -7)
     assert gemm.bf16_round_exact(Fraction(2) ** 128) == float("inf")
     assert gemm.bf16_round_exact(Fraction(3, 2 ** 135)) == 2.0 ** -133      # 1.5 subnormal ulps -> even
+
+
+def test_mx_reduces_to_per_tensor_with_equal_exponents():
+    rng = np.random.default_rng(70)
+    A = rand_codes(rng, (5, 128), fp8.E4M3)
+    B = rand_codes(rng, (7, 128), fp8.E5M2)
+    ea = np.full((5, 4), -3)
+    eb = np.full((7, 4), 2)
+    mx_full, mx_mag = gemm.mx_scaled_mm(A, fp8.E4M3, ea, B, fp8.E5M2, eb)
+    ref, mag, _ = gemm.scaled_mm(A, fp8.E4M3, B, fp8.E5M2, 2.0 ** -3, 2.0 ** 2)
+    assert np.array_equal(mx_full, ref)
+    assert np.allclose(mx_mag, mag, rtol=1e-15)
+
+
+@pytest.mark.parametrize("fa,fb", [(fp8.E4M3, fp8.E4M3), (fp8.E5M2, fp8.E4M3)])
+def test_mx_rational_with_distinct_exponents(fa, fb):
+    rng = np.random.default_rng(71)
+    M, N, K = 3, 4, 96
+    A = rand_codes(rng, (M, K), fa)
+    B = rand_codes(rng, (N, K), fb)
+    ea = rng.integers(-30, 30, size=(M, K // 32))
+    eb = rng.integers(-30, 30, size=(N, K // 32))
+    full, _ = gemm.mx_scaled_mm(A, fa, ea, B, fb, eb)
+    rows = np.repeat(np.arange(M), N)
+    cols = np.tile(np.arange(N), M)
+    samp, _ = gemm.mx_scaled_mm_sampled(A, fa, ea, B, fb, eb, rows, cols)
+    for t, (i, j) in enumerate(zip(rows, cols)):
+        tot = Fraction(0)
+        for g in range(K // 32):
+            sc = Fraction(2) ** int(ea[i, g] + eb[j, g])
+            tot += sc * sum(Fraction(fp8.decode(int(A[i, k]), fa)) * Fraction(fp8.decode(int(B[j, k]), fb))
+                            for k in range(32 * g, 32 * g + 32))
+        want = gemm.bf16_round_exact(tot)
+        assert samp[t] == want
+        assert full[i, j] == want

@@ -144,3 +144,77 @@ def test_current_mode_ignores_history():
     st.commit()
     r = st.quantize(bits([1.0]), fp8.E4M3, delayed=False)
     assert r["s"] == 448.0
+
+
+# ---------------------------------------------------------------------------------------
+# MX units: power-of-two scales per 32 elements along the contraction dimension
+# ---------------------------------------------------------------------------------------
+def _mx_exponent_by_search(a, fmt):
+    """The definition read directly: the smallest integer e in [-127, 127] with
+    FP8_MAX * 2^e >= a (searched upward; the clamps at both ends), 0 for zero or non-finite."""
+    if not (np.isfinite(a) and a > 0):
+        return 0
+    mx = fp8.fp8_max(fmt)
+    for e in range(-127, 128):
+        if mx * 2.0 ** e >= a:
+            return e
+    return 127
+
+
+@pytest.mark.parametrize("fmt", [fp8.E4M3, fp8.E5M2])
+def test_mx_exponent_against_search(fmt):
+    rng = np.random.default_rng(60)
+    v = np.abs(rng.standard_normal(3000) * 10.0 ** rng.uniform(-45, 38, 3000)).astype(np.float32)
+    mx = np.float32(fp8.fp8_max(fmt))
+    edges = [mx * np.float32(2.0) ** k for k in range(-60, 60, 7)]
+    edges += [np.nextafter(x, np.float32(np.inf)) for x in edges] + [np.nextafter(x, np.float32(0)) for x in edges]
+    for a in list(v) + edges + [np.float32(1e-45), np.float32(3.3e38)]:
+        a = np.float32(a)
+        assert quant.mx_exponent(a, fmt) == _mx_exponent_by_search(float(a), fmt), a
+
+
+def test_mx_exponent_hand_values():
+    E4, E5 = fp8.E4M3, fp8.E5M2
+    assert quant.mx_exponent(448.0, E4) == 0 and quant.mx_exponent(449.0, E4) == 1
+    assert quant.mx_exponent(448.0 * 8, E4) == 3 and quant.mx_exponent(448.0 * 8 + 1, E4) == 4
+    assert quant.mx_exponent(1.0, E4) == -8          # 448 * 2^-8 = 1.75 >= 1 > 0.875
+    assert quant.mx_exponent(57344.0, E5) == 0 and quant.mx_exponent(57345.0, E5) == 1
+    assert quant.mx_exponent(0.0, E4) == 0 and quant.mx_exponent(np.inf, E4) == 0 and quant.mx_exponent(np.nan, E5) == 0
+    assert quant.mx_exponent(1e-40, E4) == -127      # clamped to the byte's range
+
+
+@pytest.mark.parametrize("fmt", [fp8.E4M3, fp8.E5M2])
+def test_mx_groups_use_the_top_binade_and_never_saturate(fmt):
+    rng = np.random.default_rng(61)
+    x = bits(rng.standard_normal((6, 256)) * 10.0 ** rng.uniform(-6, 6, (6, 8)).repeat(32, axis=1))
+    o = quant.quantize_mx(x, fmt)
+    assert o["overflow"] == 0
+    mx = fp8.fp8_max(fmt)
+    vals = np.abs(fp8.decode_array(o["q"], fmt)).reshape(6, 8, 32)
+    top = vals.max(axis=2)
+    assert np.all(top <= mx) and np.all(top >= mx / 2)   # the group's amax lands in (max/2, max]
+    assert np.array_equal(o["ue8m0"].astype(np.int64), o["e"] + 127)
+    # groups are independent: scaling one group by 2^5 moves only its exponent, by 5
+    x2 = x.copy()
+    x2[:, 64:96] = bits(quant.widen_bf16(x[:, 64:96]) * np.float32(32.0))
+    o2 = quant.quantize_mx(x2, fmt)
+    assert np.array_equal(o2["q"], o["q"])
+    want = o["e"].copy()
+    want[:, 2] += 5
+    assert np.array_equal(o2["e"], want)
+
+
+def test_mx_reproduces_representable_groups_exactly():
+    """A group whose elements are E4M3 values times 2^e (the largest one 448 * 2^e) casts to
+    exactly those codes with exponent e."""
+    rng = np.random.default_rng(62)
+    codes = rng.integers(0, 0x7F, size=(3, 64)).astype(np.uint8) | (rng.integers(0, 2, size=(3, 64)) << 7).astype(np.uint8)
+    codes[:, 0] = 0x7E
+    codes[:, 32] = 0xFE
+    e = np.array([[-20, 5], [0, 17], [-3, -9]])
+    vals = fp8.decode_array(codes, fp8.E4M3) * np.ldexp(1.0, np.repeat(e, 32, axis=1))
+    x = bits(vals)
+    assert np.array_equal(quant.widen_bf16(x).astype(np.float64), vals)
+    o = quant.quantize_mx(x, fp8.E4M3)
+    assert np.array_equal(o["e"], e)
+    assert np.array_equal(o["q"], codes)
