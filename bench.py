@@ -655,6 +655,7 @@ SWEEP_GEMMS = [
     ("bwd_dgrad", 16384, 1024, 4096, 1, 0, False),
     ("bwd_wgrad", 1024, 4096, 16384, 0, 1, False),
     ("fine_fwd_block", 16384, 14336, 4096, 0, 0, True),
+    ("fine_fwd_mx", 16384, 14336, 4096, 0, 0, "mx"),
     ("fine_fwd_tensor", 16384, 14336, 4096, 0, 0, False),
     ("loop_fwd", 32768, 6144, 1536, 0, 0, False),
     ("loop_dgrad", 32768, 1536, 6144, 1, 0, False),
@@ -717,7 +718,13 @@ def run_sweep(args):
             continue
         A, B = codes(m, k, fa), codes(n, k, fb)
         C = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
-        if blk:
+        if blk == "mx":  # UE8M0 scale atoms, exponents in [-7, 7]
+            sa = torch.randint(120, 135, (-(-m // 128) * (k // 128) * 512,), generator=gen, device="cuda",
+                               dtype=torch.int32).to(torch.uint8)
+            sb = torch.randint(120, 135, (-(-n // 128) * (k // 128) * 512,), generator=gen, device="cuda",
+                               dtype=torch.int32).to(torch.uint8)
+            gran = g.FP8_GRAN_MX_1x32
+        elif blk:
             sa = torch.rand(m, k // 128, generator=gen, device="cuda") * 1e-2
             sb = torch.rand(k // 128, n // 128, generator=gen, device="cuda") * 1e-2
             gran = g.FP8_GRAN_BLOCK_128x128

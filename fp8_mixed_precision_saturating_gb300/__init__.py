@@ -25,7 +25,7 @@ lib = ctypes.CDLL(LIB_PATH)
 # enums (include/fp8gb.h)
 FP8_OK, FP8_ERR_INVALID_ARG, FP8_ERR_UNSUPPORTED, FP8_ERR_ALIGNMENT, FP8_ERR_CUDA, FP8_ERR_TIMEOUT = range(6)
 FP8_E4M3, FP8_E5M2 = 0, 1
-FP8_GRAN_TENSOR, FP8_GRAN_TILE_1x128, FP8_GRAN_BLOCK_128x128 = 0, 1, 2
+FP8_GRAN_TENSOR, FP8_GRAN_TILE_1x128, FP8_GRAN_BLOCK_128x128, FP8_GRAN_MX_1x32 = 0, 1, 2, 3
 FP8_SCALE_CURRENT, FP8_SCALE_DELAYED = 0, 1
 
 

@@ -114,14 +114,47 @@ fp8_status_t validate_common(const void* x, int64_t rows, int64_t cols, int64_t 
   return FP8_OK;
 }
 
+// MX scales: groups of 32 along the contraction dimension, which runs along x's rows (q given:
+// activations [M, K]) or down its columns (qT given: a weight [K, N], written transposed).
+fp8_status_t quantize_mx_impl(const void* x, int64_t rows, int64_t cols, int64_t ld, fp8_format_t fmt,
+                              fp8_scaling_t mode, const fp8_tensor_state_t* st, void* q, void* qT, float* sf,
+                              cudaStream_t stream) {
+  const char* who = "fp8_quantize (MX)";
+  if (mode != FP8_SCALE_CURRENT) return fail(FP8_ERR_UNSUPPORTED, "%s: MX scales use current scaling", who);
+  if ((q == nullptr) == (qT == nullptr))
+    return fail(FP8_ERR_INVALID_ARG, "%s: exactly one of q_out (groups along rows) and qT_out (groups down columns)", who);
+  if (sf == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: the scale buffer is required", who);
+  if (!aligned16(x) || !aligned16(q) || !aligned16(qT) || !aligned16(sf))
+    return fail(FP8_ERR_ALIGNMENT, "%s: x, the codes and the scale buffer must be 16-byte aligned", who);
+  if (ld % 8 != 0) return fail(FP8_ERR_ALIGNMENT, "%s: ld %% 8 == 0", who);
+  const bool down = qT != nullptr;
+  const int64_t kdim = down ? rows : cols;
+  if (kdim % 128 != 0)
+    return fail(FP8_ERR_UNSUPPORTED, "%s: the contraction dimension (%s) must be a multiple of 128", who,
+                down ? "rows" : "cols");
+  if (down && cols % 8 != 0) return fail(FP8_ERR_UNSUPPORTED, "%s: with qT_out, cols %% 8 == 0", who);
+  if (down && rows / 128 > 65535) return fail(FP8_ERR_UNSUPPORTED, "%s: more than 65535 row blocks", who);
+  if (!down && ((rows + 127) / 128) * 128 * (cols / 128) > INT32_MAX)
+    return fail(FP8_ERR_UNSUPPORTED, "%s: more than 2^31 tiles", who);
+  if (rows * cols == 0) return FP8_OK;
+  cudaError_t e;
+  if (st != nullptr && st->amax_cur != nullptr) {
+    if ((e = cudaMemsetAsync(st->amax_cur, 0, sizeof(float), stream)) != cudaSuccess) return cuda_fail(e, who);
+  }
+  e = launch_cast_mx(fmt, down, x, rows, cols, ld, down ? qT : q, sf, to_qs(st), stream);
+  return e == cudaSuccess ? FP8_OK : cuda_fail(e, "MX cast kernel");
+}
+
 fp8_status_t quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld, fp8_format_t fmt, fp8_gran_t gran,
                            fp8_scaling_t mode, const fp8_tensor_state_t* st, void* q, void* qT, float* unit_si,
                            cudaStream_t stream) {
   const char* who = "fp8_quantize";
   fp8_status_t s = validate_common(x, rows, cols, ld, fmt, who);
   if (s != FP8_OK) return s;
-  if (gran != FP8_GRAN_TENSOR && gran != FP8_GRAN_TILE_1x128 && gran != FP8_GRAN_BLOCK_128x128)
+  if (gran != FP8_GRAN_TENSOR && gran != FP8_GRAN_TILE_1x128 && gran != FP8_GRAN_BLOCK_128x128 &&
+      gran != FP8_GRAN_MX_1x32)
     return fail(FP8_ERR_INVALID_ARG, "%s: unknown granularity %d", who, (int)gran);
+  if (gran == FP8_GRAN_MX_1x32) return quantize_mx_impl(x, rows, cols, ld, fmt, mode, st, q, qT, unit_si, stream);
   if (mode != FP8_SCALE_CURRENT && mode != FP8_SCALE_DELAYED)
     return fail(FP8_ERR_INVALID_ARG, "%s: unknown scaling mode %d", who, (int)mode);
   const int64_t n = rows * cols;
@@ -181,8 +214,8 @@ fp8_status_t scaled_mm_impl(const void* A, fp8_format_t fa, const void* B, fp8_f
   if (M < 0 || N < 0 || K < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
   if ((fa != FP8_E4M3 && fa != FP8_E5M2) || (fb != FP8_E4M3 && fb != FP8_E5M2))
     return fail(FP8_ERR_INVALID_ARG, "%s: unknown format", who);
-  if (gran != FP8_GRAN_TENSOR && gran != FP8_GRAN_BLOCK_128x128)
-    return fail(FP8_ERR_INVALID_ARG, "%s: granularity must be TENSOR or BLOCK_128x128", who);
+  if (gran != FP8_GRAN_TENSOR && gran != FP8_GRAN_BLOCK_128x128 && gran != FP8_GRAN_MX_1x32)
+    return fail(FP8_ERR_INVALID_ARG, "%s: granularity must be TENSOR, BLOCK_128x128 or MX_1x32", who);
   if (M == 0 || N == 0) return FP8_OK;
   if (C == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: null C", who);
   if (ldc < N) return fail(FP8_ERR_INVALID_ARG, "%s: ldc < N", who);
@@ -199,7 +232,16 @@ fp8_status_t scaled_mm_impl(const void* A, fp8_format_t fa, const void* B, fp8_f
     return fail(FP8_ERR_ALIGNMENT, "%s: A and B must be 16-byte aligned with lda, ldb multiples of 16", who);
   if (gran == FP8_GRAN_BLOCK_128x128 && (K % 128 != 0 || N % 128 != 0))
     return fail(FP8_ERR_UNSUPPORTED, "%s: block scaling needs K and N multiples of 128", who);
+  if (gran == FP8_GRAN_MX_1x32) {
+    if (K % 128 != 0) return fail(FP8_ERR_UNSUPPORTED, "%s: MX scaling needs K %% 128 == 0", who);
+    if (!aligned16(sa) || !aligned16(sb)) return fail(FP8_ERR_ALIGNMENT, "%s: MX scale buffers 16-byte aligned", who);
+  }
   GemmArgs g{A, B, C, M, N, K, lda, ldb, ldc, (int)fa, (int)fb, sa, sb, gran == FP8_GRAN_BLOCK_128x128};
+  if (gran == FP8_GRAN_MX_1x32) {
+    g.mx = true;
+    g.sfa8 = reinterpret_cast<const uint8_t*>(sa);
+    g.sfb8 = reinterpret_cast<const uint8_t*>(sb);
+  }
   if (ws != nullptr && gran == FP8_GRAN_TENSOR) {
     g.ws = ws;
     g.ws_bytes = ws_bytes;
@@ -345,7 +387,9 @@ fp8_status_t fp8_requantize_weights(const void* w_master_bf16, int64_t K, int64_
                                     fp8_scaling_t mode, const fp8_tensor_state_t* st, void* wq_kn, void* wqT_nk,
                                     float* block_scale_inv, void* stream) {
   if (gran == FP8_GRAN_TILE_1x128)
-    return fail(FP8_ERR_INVALID_ARG, "fp8_requantize_weights: weights take TENSOR or BLOCK_128x128 scales");
+    return fail(FP8_ERR_INVALID_ARG, "fp8_requantize_weights: weights take TENSOR, BLOCK_128x128 or MX_1x32 scales");
+  if (gran == FP8_GRAN_MX_1x32 && wq_kn != nullptr)
+    return fail(FP8_ERR_UNSUPPORTED, "fp8_requantize_weights: MX weights are written transposed only (wqT_nk)");
   if (wq_kn == nullptr && wqT_nk == nullptr && K * N > 0)
     return fail(FP8_ERR_INVALID_ARG, "fp8_requantize_weights: no output");
   return quantize_impl(w_master_bf16, K, N, N, FP8_E4M3, gran, mode, st, wq_kn, wqT_nk, block_scale_inv,
@@ -406,7 +450,18 @@ fp8_status_t fp8_linear_fwd(const void* x_bf16, int64_t M, int64_t K, int64_t N,
     return scaled_mm_impl(xq_save, FP8_E4M3, wqT_nk, FP8_E4M3, M, N, K, K, K, FP8_GRAN_BLOCK_128x128,
                           x_tile_scale_inv, w_block_scale_inv, y_bf16, N, s);
   }
-  return fail(FP8_ERR_INVALID_ARG, "%s: granularity must be TENSOR or BLOCK_128x128", who);
+  if (gran == FP8_GRAN_MX_1x32) {
+    if (mode != FP8_SCALE_CURRENT) return fail(FP8_ERR_UNSUPPORTED, "%s: MX scaling uses current scaling", who);
+    if (xqT_save != nullptr) return fail(FP8_ERR_UNSUPPORTED, "%s: no transposed copy with MX scales", who);
+    if (w_block_scale_inv == nullptr || x_tile_scale_inv == nullptr)
+      return fail(FP8_ERR_INVALID_ARG, "%s: MX scaling needs the scale buffers of W and x", who);
+    st = quantize_impl(x_bf16, M, K, K, FP8_E4M3, FP8_GRAN_MX_1x32, FP8_SCALE_CURRENT, x_st, xq_save, nullptr,
+                       x_tile_scale_inv, s);
+    if (st != FP8_OK) return st;
+    return scaled_mm_impl(xq_save, FP8_E4M3, wqT_nk, FP8_E4M3, M, N, K, K, K, FP8_GRAN_MX_1x32, x_tile_scale_inv,
+                          w_block_scale_inv, y_bf16, N, s);
+  }
+  return fail(FP8_ERR_INVALID_ARG, "%s: granularity must be TENSOR, BLOCK_128x128 or MX_1x32", who);
 }
 
 }  // extern "C"

@@ -94,12 +94,18 @@ cudaError_t launch_cast_blocks(int fmt, const void* x, int64_t rows, int64_t col
                                float* unit_scale_inv, const QuantState& st, cudaStream_t stream);
 cudaError_t launch_cast_1x128(int fmt, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
                               float* unit_scale_inv, const QuantState& st, cudaStream_t stream);
+// MX scales (power of two per 32 elements along the contraction, UE8M0 bytes in 512-byte
+// atoms [ceil(MN / 128)][K / 128]): along_rows = false quantises x [rows, cols] with groups
+// along its rows (contraction = cols) into q [rows, cols]; along_rows = true quantises W
+// [rows, cols] with groups along its columns (contraction = rows) into q = W_q^T [cols, rows].
+cudaError_t launch_cast_mx(int fmt, bool along_rows, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
+                           void* sf, const QuantState& st, cudaStream_t stream);
 cudaError_t launch_history_commit(const QuantStates& sts, cudaStream_t stream);
 cudaError_t launch_selftest_wait(const WaitCtl& w, cudaStream_t stream);
 
 // GEMM: C [M,N] bf16 = A [M,K] * B [N,K]^T with per-tensor (block_scaled = false: sa, sb
-// point to one fp32 each) or fine-grained scales (block_scaled = true: sa [M, K/128],
-// sb [K/128, N/128]).
+// point to one fp32 each), fine-grained scales (block_scaled = true: sa [M, K/128],
+// sb [K/128, N/128]) or MX scales (mx = true: sfa8, sfb8 UE8M0 scale atoms, K % 128 == 0).
 struct GemmArgs {
   const void* A;
   const void* B;
@@ -117,6 +123,10 @@ struct GemmArgs {
   // optional workspace for split K (per-tensor scales, bf16 output only)
   void* ws = nullptr;
   int64_t ws_bytes = 0;
+  // MX scaling (block_scaled false): UE8M0 scale atoms of A and B; sa, sb unused
+  bool mx = false;
+  const uint8_t* sfa8 = nullptr;
+  const uint8_t* sfb8 = nullptr;
 };
 // Returns cudaSuccess, or an error; `why` receives a static message for host-side failures.
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why);

@@ -242,6 +242,58 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// ---------------------------------------------------------------------------------------
+// block scaling (kind::mxf8f6f4): UE8M0 scale factors in TMEM
+// ---------------------------------------------------------------------------------------
+// 1-D bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from global to
+// shared memory, completion signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Shared-memory descriptor of a tile without swizzle whose 8-row core matrices (8 rows of 16
+// bytes, 128 contiguous bytes) follow each other every 128 bytes (stride byte offset 128).
+__device__ __forceinline__ uint64_t smem_desc_plain128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= static_cast<uint64_t>(128u >> 4) << 32;          // stride byte offset
+  d |= static_cast<uint64_t>(1u) << 46;                 // version; layout type 0 (no swizzle)
+  return d;
+}
+
+// Copy 32 rows of 16 bytes from shared memory (descriptor `sdesc`) into TMEM columns taddr ..
+// taddr + 3 of lanes 0-31, replicated into all four lane quarters: row r lands in lane r (and
+// r + 32, r + 64, r + 96), its bytes 4c .. 4c + 3 in column taddr + c.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D[tmem] (+)= (A * 2^sfa) (B * 2^sfb)^T for 8-bit operands, fp32 accumulation, with one UE8M0
+// scale per row of A and of B for the instruction's 32 K (scale_vec::1X). sfa / sfb are the
+// TMEM addresses of the scale columns; the instruction descriptor's scale-factor ids pick
+// the byte within each 32-bit TMEM word.
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                         uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with UE8M0 scales, fp32 accumulator, both operands
+// K-major (format codes 0 = E4M3, 1 = E5M2); the scale-factor ids (bits 4-5 for B, 29-30 for
+// A) are or-ed in per instruction.
+__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t afmt, uint32_t bfmt, uint32_t M, uint32_t N) {
+  return (afmt << 7) | (bfmt << 10) | ((N >> 3) << 17) | (1u << 23)  // scale type UE8M0
+         | ((M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id) { return (b_id << 4) | (a_id << 29); }
+
 // Each thread of the warp reads 32 consecutive fp32 columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

@@ -118,10 +118,37 @@ __device__ __forceinline__ bool load_patch(const uint16_t* __restrict__ x, int64
   return in;
 }
 
+// Write a patch already transposed (ct[cc] = the codes of the tile's column cg * 8 + cc, rows
+// rg * 8 .. + 8) into qT [cols, rows] through the CTA's shared buffer tT; every thread of the
+// CTA must call this. Callers alternate between two buffers from tile to tile: the barrier of
+// the next call orders this call's reads of one buffer before the call after next writes it.
+__device__ __forceinline__ void store_patchT(const uint2 (&ct)[8], int64_t rows, int64_t cols, int64_t ty, int64_t tx,
+                                             uint8_t* __restrict__ qT, uint8_t* tT) {
+  const int t = threadIdx.x;
+  const int cg = t & 15, rg = t >> 4;
+  // tT row R = column index within the tile, 16-byte chunks XOR-swizzled by (R / 8) % 8
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) {
+    const int R = cg * 8 + cc;
+    const int chunk = (rg >> 1) ^ ((R >> 3) & 7);
+    *reinterpret_cast<uint2*>(tT + R * 128 + chunk * 16 + (rg & 1) * 8) = ct[cc];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const int R = p * 32 + (t >> 3);
+    const int j = t & 7;
+    const int64_t gr = tx * 128 + R;      // row of qT
+    const int64_t gc = ty * 128 + j * 16; // column of qT
+    if (gr < cols && gc < rows) {
+      const uint4 val = *reinterpret_cast<const uint4*>(tT + R * 128 + ((j ^ ((R >> 3) & 7)) * 16));
+      *reinterpret_cast<uint4*>(qT + gr * rows + gc) = val;
+    }
+  }
+}
+
 // Write the patch's codes row-major into q [rows, cols] and transposed into qT [cols, rows]
-// (through the CTA's shared buffer tT; every thread of the CTA must call this). Callers
-// alternate between two buffers from tile to tile: the barrier of the next call orders this
-// call's reads of one buffer before the call after next writes it again.
+// (through the CTA's shared buffer tT; every thread of the CTA must call this).
 __device__ __forceinline__ void store_patch(const uint2 (&c)[8], bool in, int64_t rows, int64_t cols, int64_t ty,
                                             int64_t tx, uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
                                             uint8_t* tT) {
@@ -136,25 +163,7 @@ __device__ __forceinline__ void store_patch(const uint2 (&c)[8], bool in, int64_
   if (qT != nullptr) {
     uint2 ct[8];
     transpose8x8(c, ct);
-    // tT row R = column index within the tile, 16-byte chunks XOR-swizzled by (R / 8) % 8
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-      const int R = cg * 8 + cc;
-      const int chunk = (rg >> 1) ^ ((R >> 3) & 7);
-      *reinterpret_cast<uint2*>(tT + R * 128 + chunk * 16 + (rg & 1) * 8) = ct[cc];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const int R = p * 32 + (t >> 3);
-      const int j = t & 7;
-      const int64_t gr = tx * 128 + R;      // row of qT
-      const int64_t gc = ty * 128 + j * 16; // column of qT
-      if (gr < cols && gc < rows) {
-        const uint4 val = *reinterpret_cast<const uint4*>(tT + R * 128 + ((j ^ ((R >> 3) & 7)) * 16));
-        *reinterpret_cast<uint4*>(qT + gr * rows + gc) = val;
-      }
-    }
+    store_patchT(ct, rows, cols, ty, tx, qT, tT);
   }
 }
 
@@ -587,6 +596,165 @@ __global__ void __launch_bounds__(kThreads) cast_1x128_kernel(const uint16_t* __
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// MX units: 32 consecutive elements along the contraction dimension share a power-of-two
+// scale 2^e, stored as the UE8M0 byte e + 127 in the tensor cores' scale-factor layout
+// ---------------------------------------------------------------------------------------
+// e is the smallest integer with FP8_MAX * 2^e >= amax (nothing saturates), 0 for a zero or
+// non-finite amax, at least -127. With amax = (1 + f / 128) 2^(E - 1) (bf16 exponent field
+// E + 126, 7-bit fraction f) and FP8_MAX = 0.875 * 2^EMX (EMX = 9 for E4M3, 16 for E5M2):
+// amax <= FP8_MAX * 2^(E - EMX) exactly when 1 + f / 128 <= 1.75, i.e. f <= 96; otherwise
+// one more. A subnormal amax (below 2^-126) needs e below -127: clamped.
+template <int FMT>
+__device__ __forceinline__ int mx_exponent(uint32_t b) {
+  constexpr int EMX = FMT == 0 ? 9 : 16;
+  if (b == 0u || b >= 0x7F80u) return 0;
+  const int eb = static_cast<int>(b >> 7);
+  if (eb == 0) return -127;
+  const int e = (eb - 126) - EMX + ((b & 0x7Fu) > 96u ? 1 : 0);
+  return e < -127 ? -127 : e;
+}
+
+// 2^e for e in [-127, 127] (2^-127 is subnormal).
+__device__ __forceinline__ float pow2f(int e) {
+  return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// Byte offset of the scale of MN index mn and contraction block kb (128 elements = 4 groups,
+// one byte each) in atoms of 512 bytes, [ceil(MN / 128)][nkb]; inside an atom the four bytes
+// of mn sit at 16 (mn % 32) + 4 ((mn / 32) % 4).
+__device__ __forceinline__ int64_t mx_sf_offset(int64_t mn, int64_t kb, int64_t nkb) {
+  return ((mn >> 7) * nkb + kb) * 512 + 16 * (mn & 31) + 4 * ((mn >> 5) & 3);
+}
+
+// Rows of x [rows, cols] in groups of 32 along the row (activations, contraction = cols;
+// cols % 128 == 0). Four lanes per 128-element tile as in the 1 x 128 cast: lane l holds the
+// 16-byte chunks l, l + 4, l + 8, l + 12, i.e. chunk l of each of the tile's four groups, so a
+// group's amax is the maximum over the four lanes. The tiles of rows past the last (up to a
+// multiple of 128) only write their scale bytes (e = 0).
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) cast_mx_rows_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                int64_t cols, int64_t ld, uint8_t* __restrict__ q,
+                                                                uint8_t* __restrict__ sf, QuantState st) {
+  __shared__ uint32_t red[2 * kThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  const uint32_t kbs = static_cast<uint32_t>(cols / 128);
+  const uint32_t prow = static_cast<uint32_t>((rows + 127) & ~int64_t(127));
+  const uint32_t ntiles = prow * kbs;
+  const int gl = threadIdx.x & 3;
+  const uint32_t group = (blockIdx.x * kThreads + threadIdx.x) >> 2;
+  const uint32_t ngroups = (gridDim.x * kThreads) >> 2;
+  uint32_t ov = 0, un = 0, mall = 0;
+  // every lane of a warp runs the same number of iterations (the shuffles need it)
+  const uint32_t warp_first = group & ~7u;
+  for (uint32_t base = warp_first; base < ntiles; base += ngroups) {
+    const uint32_t tile = base + (group & 7);
+    const bool live = tile < ntiles;
+    const uint32_t r = live ? tile / kbs : 0, kb = live ? tile - r * kbs : 0;
+    const bool ok = live && r < rows;
+    const uint16_t* src = x + static_cast<int64_t>(r) * ld + kb * 128;
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      v[j] = ok ? __ldcs(reinterpret_cast<const uint4*>(src + (j * 4 + gl) * 8)) : make_uint4(0, 0, 0, 0);
+    uint32_t word = 0, o1 = 0, u1 = 0, dummy = 0;
+    uint2 cq[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t m = fold2(absmax_v(0u, v[j]));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      mall = max(mall, m);
+      const int e = mx_exponent<FMT>(m);
+      cq[j] = cast8<FMT, false>(v[j], make_scaler<FMT>(pow2f(-e), pow2f(e)), o1, u1, dummy);
+      word |= static_cast<uint32_t>(e + 127) << (8 * j);
+    }
+    if (ok) {
+      uint8_t* dst = q + static_cast<int64_t>(r) * cols + kb * 128;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) *reinterpret_cast<uint2*>(dst + (j * 4 + gl) * 8) = cq[j];
+      ov += o1;
+      un += u1;
+    }
+    if (live && gl == 0) *reinterpret_cast<uint32_t*>(sf + mx_sf_offset(r, kb, kbs)) = word;
+  }
+  if (st.counters != nullptr) block_add_counters(ov, un, st.counters, red);
+  if (st.amax_cur != nullptr) {
+    const uint32_t b = block_max_u32(mall, red);
+    if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
+  }
+}
+
+// 8 x 8 transpose of bf16 elements: in[i] holds row i (8 halves), out[j] column j.
+__device__ __forceinline__ void transpose8x8_h16(const uint4 (&in)[8], uint4 (&out)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t* a = reinterpret_cast<const uint32_t*>(&in[2 * k]);
+      const uint32_t* b = reinterpret_cast<const uint32_t*>(&in[2 * k + 1]);
+      w[k] = __byte_perm(a[j >> 1], b[j >> 1], (j & 1) ? 0x7632 : 0x5410);
+    }
+    out[j] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Columns of W [rows, cols] in groups of 32 along the column (weights, contraction = rows;
+// rows % 128 == 0, cols % 8 == 0), codes written transposed into qT [cols, rows]. One CTA per
+// 128 x 128 tile: each thread transposes its 8 x 8 patch in registers (a column of W becomes a
+// row of 8), the CTA reduces each column's maximum over each group of 32 rows through shared
+// memory, computes the 512 scales of the tile once, and casts and stores the transposed codes;
+// the tile's scales are one 512-byte atom. Tiles past the last column write e = 0.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) cast_mx_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                int64_t cols, int64_t ld, uint8_t* __restrict__ qT,
+                                                                uint8_t* __restrict__ sf, QuantState st) {
+  __shared__ __align__(128) uint8_t tT[128 * 128];
+  __shared__ uint16_t cmax[16][128];  // per slab of 8 rows, each column's max |x| (bf16 bits)
+  __shared__ Scaler scl[4][128];      // per group of 32 rows, each column's scaler
+  __shared__ __align__(16) uint8_t atom[512];
+  __shared__ uint32_t red[2 * kThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  const int64_t ty = blockIdx.y, tx = blockIdx.x;
+  const int t = threadIdx.x;
+  const int cg = t & 15, rg = t >> 4;
+  uint4 v[8];
+  const bool in = load_patch(x, rows, cols, ld, ty, tx, v);
+  uint4 vt[8];
+  transpose8x8_h16(v, vt);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) cmax[rg][cg * 8 + j] = static_cast<uint16_t>(fold2(absmax_v(0u, vt[j])));
+  __syncthreads();
+  uint32_t mall = 0;
+  for (int p = t; p < 512; p += kThreads) {
+    const int c = p & 127, g = p >> 7;
+    const uint32_t m = max(max(static_cast<uint32_t>(cmax[4 * g][c]), static_cast<uint32_t>(cmax[4 * g + 1][c])),
+                           max(static_cast<uint32_t>(cmax[4 * g + 2][c]), static_cast<uint32_t>(cmax[4 * g + 3][c])));
+    mall = max(mall, m);
+    const int e = mx_exponent<FMT>(m);
+    scl[g][c] = make_scaler<FMT>(pow2f(-e), pow2f(e));
+    atom[16 * (c & 31) + 4 * (c >> 5) + g] = static_cast<uint8_t>(e + 127);
+  }
+  __syncthreads();
+  const int g = rg >> 2;
+  uint32_t ov = 0, un = 0, dummy = 0;
+  uint2 ct[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) ct[j] = cast8<FMT, false>(vt[j], scl[g][cg * 8 + j], ov, un, dummy);
+  if (!in) ov = un = 0;
+  store_patchT(ct, rows, cols, ty, tx, qT, tT);  // (its barrier also orders the atom's writes)
+  if (t < 32)
+    *reinterpret_cast<uint4*>(sf + (tx * (rows / 128) + ty) * 512 + t * 16) = *reinterpret_cast<const uint4*>(atom + t * 16);
+  if (st.counters != nullptr) block_add_counters(ov, un, st.counters, red);
+  if (st.amax_cur != nullptr) {
+    const uint32_t b = block_max_u32(mall, red);
+    if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
+  }
+}
+
 __global__ void history_commit_kernel(QuantStates sts) {
   pdl_wait();
   pdl_trigger();
@@ -723,6 +891,22 @@ cudaError_t launch_cast_1x128(int fmt, const void* x, int64_t rows, int64_t cols
   auto* qp = static_cast<uint8_t*>(q);
   return launch_pdl(fmt == 0 ? cast_1x128_kernel<0> : cast_1x128_kernel<1>, dim3(g), dim3(kThreads), 0, stream, xp,
                     rows, cols, ld, qp, unit_scale_inv, st);
+}
+
+cudaError_t launch_cast_mx(int fmt, bool along_rows, const void* x, int64_t rows, int64_t cols, int64_t ld, void* q,
+                           void* sf, const QuantState& st, cudaStream_t stream) {
+  auto* xp = static_cast<const uint16_t*>(x);
+  auto* qp = static_cast<uint8_t*>(q);
+  auto* sp = static_cast<uint8_t*>(sf);
+  if (along_rows) {
+    const dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>(rows / 128));
+    return launch_pdl(fmt == 0 ? cast_mx_cols_kernel<0> : cast_mx_cols_kernel<1>, grid, dim3(kThreads), 0, stream, xp,
+                      rows, cols, ld, qp, sp, st);
+  }
+  const int64_t ntiles = ((rows + 127) / 128) * 128 * (cols / 128);
+  const int g = grid_for(ntiles, kThreads / 4, num_sms(), 8);
+  return launch_pdl(fmt == 0 ? cast_mx_rows_kernel<0> : cast_mx_rows_kernel<1>, dim3(g), dim3(kThreads), 0, stream, xp,
+                    rows, cols, ld, qp, sp, st);
 }
 
 cudaError_t launch_history_commit(const QuantStates& sts, cudaStream_t stream) {

@@ -68,8 +68,26 @@ typedef enum {
 typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format_t;
 
 /* [GUARD] "Real products...": per-tensor, fine-grained 1x128 tiles (one scale per row
- * and 128 consecutive columns) and 128x128 blocks. */
-typedef enum { FP8_GRAN_TENSOR = 0, FP8_GRAN_TILE_1x128 = 1, FP8_GRAN_BLOCK_128x128 = 2 } fp8_gran_t;
+ * and 128 consecutive columns) and 128x128 blocks, with fp32 scales; and MX units, the same
+ * fine-grained idea on the tensor cores' own block scaling: one power-of-two scale per 32
+ * consecutive elements along the contraction dimension, stored as a UE8M0 byte.
+ *
+ * MX scale layout (FP8_GRAN_MX_1x32). For an operand with MN rows (M for the GEMM's A, N
+ * for its B) and contraction K (K % 128 == 0), the scale of MN index m and contraction
+ * group g (elements 32 g .. 32 g + 31) is 2^e with e the smallest integer such that
+ * FP8_MAX * 2^e >= the group's amax (so no element saturates; e = 0 for a zero or non-finite
+ * amax; e >= -127), stored as the byte e + 127. The bytes form ceil(MN / 128) x (K / 128)
+ * atoms of 512 bytes, atom (m / 128, g / 4) at byte offset ((m / 128) * (K / 128) + g / 4) * 512;
+ * inside it the byte of (m, g) sits at 16 (m % 32) + 4 ((m / 32) % 4) + g % 4. Rows past the
+ * last MN index up to a multiple of 128 hold e = 0. The buffer (ceil(MN/128) * K/128 * 512
+ * bytes) is caller-owned and 16-byte aligned; it is passed through the `float*` scale
+ * arguments of the entry points below, which then point to these bytes. */
+typedef enum {
+  FP8_GRAN_TENSOR = 0,
+  FP8_GRAN_TILE_1x128 = 1,
+  FP8_GRAN_BLOCK_128x128 = 2,
+  FP8_GRAN_MX_1x32 = 3
+} fp8_gran_t;
 
 /* Current scaling takes the scale from this tensor's own amax; delayed scaling takes it
  * from the maximum of an amax history ([GUARD] "Real products...": delayed scaling with
@@ -112,6 +130,12 @@ typedef struct {
  *  gran = FP8_GRAN_BLOCK_128x128: rows % 128 == 0 and cols % 128 == 0; one scale per
  *    128x128 block, inverse scales in unit_scale_inv [rows/128, cols/128]. Mode CURRENT;
  *    `st` as for tiles.
+ *  gran = FP8_GRAN_MX_1x32: mode CURRENT; unit_scale_inv receives the MX scale bytes (layout
+ *    above). Exactly one of q_out and qT_out: with q_out the groups run along x's rows
+ *    (activations: contraction = cols, cols % 128 == 0; codes [rows, cols], scales with
+ *    MN = rows); with qT_out they run down its columns (a weight [K, N]: contraction = rows,
+ *    rows % 128 == 0, cols % 8 == 0; codes written transposed [cols, rows], scales with
+ *    MN = cols). `st` as for tiles. ld % 8 == 0.
  *  q_out [rows, cols] (leading dimension cols) receives the codes; may be NULL when
  *    qT_out is given. qT_out [cols, rows] (leading dimension rows) receives the transposed
  *    codes, or is NULL. With qT_out, rows % 16 == 0. With q_out and a GEMM consumer,
@@ -156,6 +180,9 @@ fp8_status_t fp8_quantize_many(const fp8_quant_job_t* jobs, int32_t n, void* str
  *    scale_inv_b [K/128, N/128] (indexed [k/128][n/128]); each 128-deep K block is
  *    accumulated separately and added as C_ij += d_a[i,kb] * d_b[kb, j/128] * P_ij,kb.
  *    Requires K % 128 == 0 and N % 128 == 0.
+ *  gran = FP8_GRAN_MX_1x32: MX scales on the tensor cores' block scaling: scale_inv_a and
+ *    scale_inv_b point to the MX scale bytes of A (MN = M) and of B (MN = N), and
+ *    C_ij = bf16( sum_g 2^(e_a[i,g] + e_b[j,g]) * sum_{k in group g} a_ik b_jk ). K % 128 == 0.
  *  Any M, N >= 0 and K >= 0 (K == 0 writes zeros). A, B, C 16-byte aligned; lda and ldb
  *  multiples of 16, ldc a multiple of 8. */
 fp8_status_t fp8_scaled_mm(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb,
@@ -242,8 +269,10 @@ fp8_status_t fp8_scaled_mm_quant(const void* A, fp8_format_t fa, const void* B, 
  *  re-quantised to E4M3 and cached for the next forward. One pass over W writes
  *  wq_kn [K,N] (for dgrad) and/or wqT_nk [N,K] (for the forward); either may be NULL but
  *  not both. gran TENSOR (st required; CURRENT or DELAYED: delayed scaling uses the
- *  history before this call's amax is pushed) or BLOCK_128x128 (block_scale_inv
- *  [K/128, N/128]). Same rules as fp8_quantize. */
+ *  history before this call's amax is pushed), BLOCK_128x128 (block_scale_inv
+ *  [K/128, N/128]) or MX_1x32 (groups of 32 down each column of W, i.e. along K; wq_kn must
+ *  be NULL, wqT_nk [N,K] receives the codes and block_scale_inv the MX scale bytes with
+ *  MN = N). Same rules as fp8_quantize. */
 fp8_status_t fp8_requantize_weights(const void* w_master_bf16, int64_t K, int64_t N,
                                     fp8_gran_t gran, fp8_scaling_t mode,
                                     const fp8_tensor_state_t* st, void* wq_kn, void* wqT_nk,
@@ -269,6 +298,8 @@ fp8_status_t fp8_update_requantize_weights(void* w_master_bf16, const float* del
  *  xq_save with x_tile_scale_inv [M, K/128]) and runs the scaled GEMM against the cached
  *  wqT_nk [N,K]. gran TENSOR uses w_st->scale_inv; gran BLOCK_128x128 (1x128 x tiles,
  *  128x128 W blocks) uses w_block_scale_inv [K/128, N/128] and requires mode CURRENT.
+ *  gran MX_1x32 (mode CURRENT): x cast with MX scales (x_tile_scale_inv receives its scale
+ *  bytes, MN = M), the GEMM with W's MX scale bytes in w_block_scale_inv (MN = N).
  *  xqT_save [K,M] (nullable, gran TENSOR only) keeps the transposed codes for wgrad.
  *  x contiguous; K % 16 == 0 (K % 128 == 0 for gran BLOCK); M % 16 == 0 with xqT_save.
  *  x_st is required for gran TENSOR and optional otherwise. An empty token batch (M == 0)
