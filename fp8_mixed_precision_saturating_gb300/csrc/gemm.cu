@@ -81,7 +81,10 @@ struct Cfg {
   // two warps per TMEM lane quarter, each draining half of the tile's columns
   static constexpr int EPI_WARPS = 8;
   static constexpr int QSTG_PER_WARP = QF >= 0 ? QSTG_BYTES : 0;
-  static constexpr int STAGES_FIT = (230000 - EPI_WARPS * (STG_BYTES + QSTG_PER_WARP)) / (STAGE_BYTES + SF_BYTES);
+  // bf16 staging per epilogue warp: 32 rows x 64 columns (128-byte swizzle), or with MX
+  // 32 x 32 (64-byte swizzle), which leaves shared memory for a fourth 256-wide stage
+  static constexpr int STG = MX ? STG_BYTES / 2 : STG_BYTES;
+  static constexpr int STAGES_FIT = (230000 - EPI_WARPS * (STG + QSTG_PER_WARP)) / (STAGE_BYTES + SF_BYTES);
   static constexpr int STAGES = STAGES_FIT < (192 * 1024) / STAGE_BYTES ? STAGES_FIT : (192 * 1024) / STAGE_BYTES;
   // TMEM: ACC accumulator buffers, then (MX) 4 columns of A's scales and 4 per atom of B's
   static constexpr int SF_COLS = MX ? 4 * (1 + SFB_ATOMS) : 0;
@@ -93,8 +96,11 @@ struct Cfg {
   static constexpr int STG_PER_WARP = 1;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int OFF_SF = STAGES * STAGE_BYTES;
-  static constexpr int OFF_STG = OFF_SF + STAGES * SF_BYTES;
-  static constexpr int OFF_QSTG = OFF_STG + EPI_WARPS * STG_PER_WARP * STG_BYTES;
+  // the staging buffers start on a 1024-byte boundary: the TMA store applies the swizzle from
+  // the shared-memory address bits, so a buffer 512 bytes off would have its 16-byte chunks
+  // read from the wrong positions (columns 0-31 and 32-63 of a 64-column store exchanged)
+  static constexpr int OFF_STG = (OFF_SF + STAGES * SF_BYTES + 1023) & ~1023;
+  static constexpr int OFF_QSTG = OFF_STG + EPI_WARPS * STG_PER_WARP * STG;
   static constexpr int OFF_BAR = OFF_QSTG + EPI_WARPS * QSTG_PER_WARP;
   // full[S], empty[S], tfull[ACC], tempty[ACC], final
   static constexpr int NBAR = 2 * STAGES + 2 * ACC + 1;
@@ -104,6 +110,7 @@ struct Cfg {
   static constexpr int TEMPTY_COUNT = (PAIR ? 2 : 1) * EPI_WARPS;
   static_assert(SMEM <= 232448, "shared memory");
   static_assert((A_BYTES % 1024) == 0 && (B_BYTES % 1024) == 0, "stage halves on 1024-byte swizzle atoms");
+  static_assert(OFF_STG % 1024 == 0 && STG % 1024 == 0 && OFF_QSTG % 512 == 0, "staging on swizzle atoms");
 };
 
 // One GEMM problem of a launch. A launch runs one problem, or two independent ones (the
@@ -466,7 +473,7 @@ __global__ void __launch_bounds__(Cfg<BN, QF, PAIR, MX>::THREADS, 1)
     const int ew = warp - 2;             // 0 .. EPI_WARPS-1
     const int q = warp & 3;              // TMEM lane quarter this warp may read
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    uint8_t* stg = smem + C::OFF_STG + ew * C::STG_PER_WARP * STG_BYTES;
+    uint8_t* stg = smem + C::OFF_STG + ew * C::STG_PER_WARP * C::STG;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -541,6 +548,26 @@ __global__ void __launch_bounds__(Cfg<BN, QF, PAIR, MX>::THREADS, 1)
             pk[j] = pack_bf16x2(__fmul_rn(__uint_as_float(ra[2 * j]), dd), __fmul_rn(__uint_as_float(ra[2 * j + 1]), dd));
             pk[16 + j] =
                 pack_bf16x2(__fmul_rn(__uint_as_float(rb[2 * j]), dd), __fmul_rn(__uint_as_float(rb[2 * j + 1]), dd));
+          }
+          if constexpr (MX) {
+            // two stores of 32 columns through the half-size buffer: 16-byte chunk j of row r
+            // sits at chunk j ^ ((r / 2) % 4) (64-byte swizzle)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
+              __syncwarp();
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) =
+                    make_uint4(pk[16 * h + 4 * j], pk[16 * h + 4 * j + 1], pk[16 * h + 4 * j + 2], pk[16 * h + 4 * j + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0 && rows_live) {
+                tma_store_2d(tC, smem_u32(stg), nb * BN + col + 32 * h, row0);
+                bulk_commit_group();
+              }
+            }
+            return;
           }
           if (lane == 0) bulk_wait_group_read<0>();  // the previous stores have read the staging buffers
           __syncwarp();
@@ -628,17 +655,8 @@ __global__ void __launch_bounds__(Cfg<BN, QF, PAIR, MX>::THREADS, 1)
           }
         }
         if (last) {
-          if constexpr (MX && BN == 256) {
-            // block-scaled MMAs 256 wide leave the accumulator's 32-column blocks swapped in
-            // pairs (TMEM column 32 b + r holds output column 32 (b ^ 1) + r, the B rows and
-            // their scales alike; measured on GB300), so each 64-column chunk is stored with its
-            // halves exchanged
-            emit(r1, r0, hc * 64);
-            if (two) emit(r3, r2, (hc + 2) * 64);
-          } else {
-            emit(r0, r1, hc * 64);
-            if (two) emit(r2, r3, (hc + 2) * 64);
-          }
+          emit(r0, r1, hc * 64);
+          if (two) emit(r2, r3, (hc + 2) * 64);
         }
         acc = (acc + 1 == ACC) ? 0 : acc + 1;
         if (acc == 0) acc_phase ^= 1u;
@@ -720,6 +738,7 @@ struct BlkCfg {
   static_assert(FOLD_REGS == 0 || 128 * CTRL_REGS + 256 * FOLD_REGS <= THREADS * LAUNCH_REGS, "register split");
   static_assert(SMEM <= 232448, "shared memory");
   static_assert(STAGES >= 3, "ring depth");
+  static_assert(OFF_STG % 1024 == 0, "staging buffers on 1024-byte swizzle atoms");
 };
 
 // a0, a1 += fp32(v0) * s, fp32(v1) * s: two fp32 FMAs (round to nearest each) in one packed
@@ -1169,9 +1188,10 @@ bool make_problem(const GemmArgs& g, const TileChoice& c, KProb& q, Maps& m, con
     q.ws = reinterpret_cast<float4*>(static_cast<uint8_t*>(g.ws) + l.counter_bytes);
   }
   const uint32_t b_rows = c.pair ? static_cast<uint32_t>(c.bn / 2) : static_cast<uint32_t>(c.bn);
+  const bool cmap = g.mx ? encode_tmap_2d(&m.c, g.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.N, g.M, g.ldc * 2, 32, 32, 64)
+                         : make_map(&m.c, g.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.N, g.M, g.ldc * 2, 64, 32);
   if (!make_map(&m.a, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.M, g.lda, BK, BM) ||
-      !make_map(&m.b, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.N, g.ldb, BK, b_rows) ||
-      !make_map(&m.c, g.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.N, g.M, g.ldc * 2, 64, 32)) {
+      !make_map(&m.b, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.N, g.ldb, BK, b_rows) || !cmap) {
     *why = "cuTensorMapEncodeTiled failed (driver entry point missing or tensor map rejected)";
     return false;
   }
