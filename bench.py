@@ -14,6 +14,10 @@ writing a 256 MiB buffer (the L2 flush, not timed). Per-kernel times come from t
 launched eagerly in the same loop, each behind a flush.
 
 Sub-records in the same line, each with its own roofline, kernel times and oracle CPU baseline:
+  finegrained_upproj_fwd_mx  the headline's shapes and inputs with MX scales (a power-of-two
+                    UE8M0 scale per 32 contraction elements, applied by the tensor cores):
+                    W's cast down its columns (written as W_q^T) || x's cast along its rows,
+                    the block-scaled (kind::mxf8f6f4) GEMM
   backward_upproj   M=16384, K=1024, N=4096: dy's E5M2 cast (current scaling, dy_q and dy_q^T),
                     dgrad and wgrad in one grouped launch
   delayed_loop      32768 tokens, d 1536 -> 6144, history 16: one layer-step (optimizer step
@@ -129,8 +133,9 @@ STAGE_SOURCES = {
     # GPT-2-small training step
     "requant_w": _CAST_SOURCES, "quant_x": _CAST_SOURCES, "quant_dy": _CAST_SOURCES,
     "gemm_fwd": _GEMM_SOURCES, "gemm_bwd": _GEMM_SOURCES,
-    # fine-grained forward (headline)
+    # fine-grained forward (headline), and the same shapes with MX scales
     "fine_cast_w": _CAST_SOURCES, "fine_cast_x": _CAST_SOURCES, "fine_gemm": _GEMM_SOURCES,
+    "mx_cast_w": _CAST_SOURCES, "mx_cast_x": _CAST_SOURCES, "mx_gemm": _GEMM_SOURCES,
     # backward
     "bwd_cast_dy": _CAST_SOURCES, "bwd_gemm": _GEMM_SOURCES,
     # delayed loop, one layer-step
@@ -320,6 +325,7 @@ def run_gpu(args):
     # ---- sub-records (rank 0 reports them; every rank runs the same work)
     subs = {}
     if not args.headline_only:
+        subs["finegrained_upproj_fwd_mx"] = bench_finegrained_mx(ctx, args.steps, args.warmup)
         subs["backward_upproj"] = bench_backward(ctx, max(5, args.steps // 2), args.warmup)
         subs["delayed_loop"] = bench_delayed_loop(ctx, max(3, args.steps // 4), args.warmup)
         subs["gpt2s_train_step"] = bench_gpt2(ctx, args.steps, args.warmup)
@@ -462,6 +468,50 @@ def e2e_finegrained(ctx, x_h, w_h, steps, step_flops):
     return {"value": round(step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(2 * (M * K + K * N)), "d2h_bytes_per_step": int(2 * M * N),
             "api": "fp8_requantize_weights + fp8_linear_fwd (block scaling), pinned host buffers"}
+
+
+def bench_finegrained_mx(ctx, steps, warmup):
+    """The headline's shapes and inputs with MX scales: W's cast in groups of 32 down its
+    columns (W_q^T and its scale bytes) beside x's cast in groups of 32 along its rows, then
+    the GEMM on the tensor cores' block scaling."""
+    from datagen import workload_inputs
+    torch, g, stream, flush = ctx["torch"], ctx["g"], ctx["stream"], ctx["flush"]
+    M, K, N = FINE["M"], FINE["K"], FINE["N"]
+    w_in = workload_inputs("finegrained_fwd")
+    x, wm = dev_bf16(torch, w_in["x"]), dev_bf16(torch, w_in["w"])
+    u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device="cuda")
+    xq, wqT = u8(M, K), u8(N, K)
+    xsf, wsf = u8(-(-M // 128) * (K // 128) * 512), u8(-(-N // 128) * (K // 128) * 512)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    X, CUR = g.FP8_GRAN_MX_1x32, g.FP8_SCALE_CURRENT
+    flops = 2.0 * M * N * K
+    stages = [
+        Stage("mx_cast_w", lambda: g.fp8_requantize_weights(wm, K, N, X, CUR, None, None, wqT, wsf), 1,
+              nbytes=K * N * 3.0 + wsf.numel()),
+        Stage("mx_cast_x", lambda: g.fp8_quantize(x, M, K, K, g.FP8_E4M3, X, CUR, None, xq, None, xsf), 1,
+              nbytes=M * K * 3.0 + xsf.numel()),
+        Stage("mx_gemm", lambda: g.fp8_scaled_mm(xq, 0, wqT, 0, M, N, K, K, K, X, xsf, wsf, y, N), 1, flops=flops),
+    ]
+    side = torch.cuda.Stream()
+
+    def enqueue():
+        side.wait_stream(stream)
+        stages[0].fn()
+        with torch.cuda.stream(side):
+            stages[1].fn()
+        stream.wait_stream(side)
+        stages[2].fn()
+
+    step_ms, stage_ms, _ = time_step(torch, stream, flush, enqueue, stages, steps, warmup)
+    ms = sum(step_ms) / steps
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
+            "steps": steps,
+            "config": {"workload": "finegrained_upproj_fwd_mx", "M_tokens": M, "d_model": K, "d_ff": N,
+                       "scaling": "E4M3 with a UE8M0 power-of-two scale per 32 contraction elements (x along its "
+                                  "rows, W down its columns), applied by block-scaled MMAs",
+                       "step": "(W cast || x cast on two streams), MX GEMM; one CUDA graph"},
+            "roofline": roofline(stages, stage_ms, ctx["hbm"], ctx["bf16_tf"], ctx["peak_src"], name="mx_gemm"),
+            "kernels": kernel_records(stages, stage_ms, ctx["hbm"], ctx["fp8_peak"])}
 
 
 def bench_backward(ctx, steps, warmup):
@@ -908,13 +958,13 @@ def _t(fn):
 FINE_SLAB_COLS = 1792  # 14 of the 112 column blocks of W (and of y)
 
 
-def finegrained_slab(rows: int):
-    """The first `rows` rows of the headline's x and the first FINE_SLAB_COLS columns of its W
-    (the workload's own draws)."""
+def finegrained_slab(rows: int, cols: int = FINE_SLAB_COLS):
+    """The first `rows` rows of the headline's x and the first `cols` columns of its W (the
+    workload's own draws)."""
     import numpy as np
     from datagen import workload_inputs
     w_in = workload_inputs("finegrained_fwd", M=rows)  # the first rows of the full x
-    return w_in["x"], np.ascontiguousarray(w_in["w"][:, :FINE_SLAB_COLS])
+    return w_in["x"], np.ascontiguousarray(w_in["w"][:, :cols])
 
 
 def leg_finegrained(rows: int):
@@ -930,6 +980,22 @@ def leg_finegrained(rows: int):
     parts = {"cast_x_1x128": t_x * M / rows, "cast_w_128x128": t_w * N / c, "gemm_block_scaled": t_g * (M / rows) * (N / c)}
     return 2.0 * M * N * K, parts, (f"x 1x128 cast of {rows} of {M} rows, W 128x128 cast of {c} of {N} columns, "
                                      f"block-scaled GEMM on the {rows} x {c} output slab; extrapolated linearly")
+
+
+def leg_finegrained_mx(rows: int):
+    """The MX casts of `rows` rows of x and 32 columns of W, the MX GEMM on the rows x 32
+    output slab they give (the oracle's MX cast visits every group of 32 in Python)."""
+    import numpy as np
+    from oracle import fp8, gemm, quant
+    M, K, N = FINE["M"], FINE["K"], FINE["N"]
+    c = 32
+    x, w = finegrained_slab(rows, c)
+    t_x, ox = _t(lambda: quant.quantize_mx(x, fp8.E4M3))
+    t_w, ow = _t(lambda: quant.quantize_mx(np.ascontiguousarray(w.T), fp8.E4M3))
+    t_g, _ = _t(lambda: gemm.mx_scaled_mm(ox["q"], fp8.E4M3, ox["e"], ow["q"], fp8.E4M3, ow["e"]))
+    parts = {"cast_x_mx": t_x * M / rows, "cast_w_mx": t_w * N / c, "gemm_mx": t_g * (M / rows) * (N / c)}
+    return 2.0 * M * N * K, parts, (f"x MX cast of {rows} of {M} rows, W MX cast of {c} of {N} columns, MX GEMM "
+                                     f"on the {rows} x {c} output slab; extrapolated linearly")
 
 
 def leg_backward(rows: int):
@@ -1006,7 +1072,7 @@ def leg_gpt2(rows: int):
 
 
 # leg name -> (function, slab rows with all cores, slab rows on one core)
-CPU_LEGS = {"finegrained": (leg_finegrained, 128, 64), "backward_upproj": (leg_backward, 1024, 256),
+CPU_LEGS = {"finegrained": (leg_finegrained, 128, 64), "finegrained_upproj_fwd_mx": (leg_finegrained_mx, 16, 8), "backward_upproj": (leg_backward, 1024, 256),
             "delayed_loop": (leg_delayed_loop, 1024, 256), "gpt2s_train_step": (leg_gpt2, 2048, 512)}
 
 
