@@ -59,7 +59,8 @@ constexpr int BM = 128, BK = 128;
 constexpr int A_BYTES = BM * BK;
 constexpr int STG_BYTES = 32 * 128;  // one staging buffer: 32 rows x 64 bf16
 constexpr int QSTG_BYTES = 32 * 64;  // one staging buffer of FP8 output: 32 rows x 64 codes
-constexpr int GROUP_M = 16;          // tile raster: 16 M-blocks share each B tile
+// Tile raster: groups of `group_m` row blocks sweep the column blocks together, so a B tile
+// is read by the group's CTAs from L2 and B is read from DRAM once per group.
 
 // Tile 128 x BN per CTA (BN = 256, 192 or 128); the ring depth fills ~192 KB of shared
 // memory, less when the epilogue also stages FP8 output (QF >= 0: 0 = E4M3, 1 = E5M2).
@@ -141,6 +142,7 @@ constexpr int kMaxSchedUnits = 1024;   // units of an explicit schedule
 struct KParams {
   KProb pr[2];
   int nprob;  // 1 or 2
+  int group_m;  // row blocks per raster group
   int units;  // work units of all problems
   WaitCtl w;
   QuantState cst;  // scaling state of the FP8 output (QF >= 0, one problem)
@@ -189,11 +191,11 @@ __device__ __forceinline__ KProb prob_of(const KParams& p, int pi) {
   return q;
 }
 
-__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb, int& nb) {
-  const int per_group = GROUP_M * num_n;
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m, int& mb, int& nb) {
+  const int per_group = group_m * num_n;
   const int g = t / per_group;
-  const int first_m = g * GROUP_M;
-  const int gsize = min(GROUP_M, num_m - first_m);
+  const int first_m = g * group_m;
+  const int gsize = min(group_m, num_m - first_m);
   const int local = t - g * per_group;
   mb = first_m + local % gsize;
   nb = local / gsize;
@@ -214,7 +216,7 @@ __device__ __forceinline__ Unit unit_at(int u, const KParams& p, KProb& q) {
   r.split = v - r.t * q.splits;
   r.kb0 = r.split * q.num_kb / q.splits;
   r.kb1 = (r.split + 1) * q.num_kb / q.splits;
-  tile_coords(r.t, q.num_m, q.num_n, r.mb, r.nb);
+  tile_coords(r.t, q.num_m, q.num_n, p.group_m, r.mb, r.nb);
   return r;
 }
 
@@ -822,7 +824,7 @@ __global__ void __launch_bounds__(BlkCfg<BN, PAIR>::THREADS, 1)
       const uint32_t full_lead = PAIR ? mapa_shared(bar_full, 0) : bar_full;
       for (int t = tile0; ok && t < pb.num_tiles; t += tile_step) {
         int mb, nb;
-        tile_coords(t, pb.num_m, pb.num_n, mb, nb);
+        tile_coords(t, pb.num_m, pb.num_n, p.group_m, mb, nb);
         const int arow = mb * TILE_M + static_cast<int>(rank) * BM;
         const int brow = nb * BN + static_cast<int>(rank) * C::B_ROWS;
         for (int kb = 0; kb < pb.num_kb; ++kb) {
@@ -921,7 +923,7 @@ __global__ void __launch_bounds__(BlkCfg<BN, PAIR>::THREADS, 1)
     bool ok = true;
     for (int t = tile0; ok && t < pb.num_tiles; t += tile_step) {
       int mb, nb;
-      tile_coords(t, pb.num_m, pb.num_n, mb, nb);
+      tile_coords(t, pb.num_m, pb.num_n, p.group_m, mb, nb);
       const int row0 = mb * TILE_M + static_cast<int>(rank) * BM + q * 32;  // this warp's 32 rows
       const int row = row0 + lane;
       const int nblk = (nb * BN + col0) / 128;
@@ -1500,6 +1502,11 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why
 #endif
   }
   KParams p{};
+  // the long fine-grained GEMMs sweep B with 8192-row groups: measured at 16384 x 14336 x 4096,
+  // B is then read from DRAM twice (fold kernel on pairs: 244 MB against 306 with 16 tiles per
+  // group; MX on single CTAs: 204 MB against 550, 1.5 % faster); whole-M groups (16384 rows)
+  // thrash L2 on pairs (937 MB)
+  p.group_m = (g.block_scaled || g.mx) ? (choice.pair ? 32 : 64) : 16;
   Maps m0;
   if (!make_problem(g, choice, p.pr[0], m0, why)) return cudaErrorInvalidValue;
   p.pr[1] = p.pr[0];
@@ -1609,6 +1616,7 @@ cudaError_t launch_gemm_group(const GemmArgs& g0in, const GemmArgs& g1in, void* 
   if (pl.b0 > 0) g0.ws = ws;
   if (pl.b1 > 0) g1.ws = static_cast<uint8_t*>(ws) + pl.b0;
   KParams p{};
+  p.group_m = 16;
   Maps m0, m1;
   if (!make_problem(g0, pl.c0, p.pr[0], m0, why) || !make_problem(g1, pl.c1, p.pr[1], m1, why))
     return cudaErrorInvalidValue;
