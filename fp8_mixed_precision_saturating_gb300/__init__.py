@@ -92,6 +92,8 @@ _SIGS = {
     "fp8_linear_bwd": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _SP, _I, _P, _P, _P, _P, _P],
     "fp8_linear_bwd_noalloc": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _SP, _I, _P, _P, _P],
     "fp8_linear_bwd_ws": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _SP, _I, _P, _P, _P, _P, _P, _I64, _P],
+    "fp8_linear_bwd_mn": [_P, _I64, _I64, _I64, _P, _SP, _P, _SP, _SP, _I, _P, _P, _P, _P, _I64, _P],
+    "fp8_scaled_mm_t": [_P, _I, _P, _I, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _I64, _P],
     "fp8_history_commit": [_SP, _P],
     "fp8_history_commit_many": [_SP, ctypes.c_int32, _P],
     "fp8_poll_device_error": [],
@@ -294,6 +296,20 @@ def fp8_linear_bwd_ws(dy, M, K, N, xqT_save, x_st, wq_kn, w_st, dy_st, mode, dyq
     return _check(lib.fp8_linear_bwd_ws(_ptr(dy), M, K, N, _ptr(xqT_save), _state(x_st), _ptr(wq_kn), _state(w_st),
                                         _state(dy_st), mode, _ptr(dyq_ws), _ptr(dyqT_ws), _ptr(dx), _ptr(dw),
                                         _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def fp8_linear_bwd_mn(dy, M, K, N, xq_save, x_st, wq_kn, w_st, dy_st, mode, dyq_ws, dx, dw, workspace=None,
+                      workspace_bytes=0, stream=None):
+    return _check(lib.fp8_linear_bwd_mn(_ptr(dy), M, K, N, _ptr(xq_save), _state(x_st), _ptr(wq_kn), _state(w_st),
+                                        _state(dy_st), mode, _ptr(dyq_ws), _ptr(dx), _ptr(dw), _ptr(workspace),
+                                        workspace_bytes, _stream(stream)))
+
+
+def fp8_scaled_mm_t(A, fa, B, fb, M, N, K, lda, ldb, scale_inv_a, scale_inv_b, C, ldc, workspace=None,
+                    workspace_bytes=0, stream=None):
+    return _check(lib.fp8_scaled_mm_t(_ptr(A), fa, _ptr(B), fb, M, N, K, lda, ldb, _ptr(scale_inv_a),
+                                      _ptr(scale_inv_b), _ptr(C), ldc, _ptr(workspace), workspace_bytes,
+                                      _stream(stream)))
 
 
 def fp8_linear_bwd_workspace_bytes(M, K, N) -> int:

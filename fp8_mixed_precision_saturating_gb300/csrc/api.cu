@@ -507,24 +507,85 @@ fp8_status_t grouped_impl(const fp8_mm_problem_t* pr, int32_t n, void* ws, int64
   return e == cudaSuccess ? FP8_OK : cuda_fail(e, why);
 }
 
+// C [M,N] = A^T B with A [K, M] and B [K, N] row-major, read MN-major (per-tensor scales).
+fp8_status_t scaled_mm_t_impl(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb, int64_t M, int64_t N,
+                              int64_t K, int64_t lda, int64_t ldb, const float* sa, const float* sb, void* C,
+                              int64_t ldc, void* ws, int64_t ws_bytes, cudaStream_t stream, const char* who) {
+  if (M < 0 || N < 0 || K < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
+  if ((fa != FP8_E4M3 && fa != FP8_E5M2) || (fb != FP8_E4M3 && fb != FP8_E5M2))
+    return fail(FP8_ERR_INVALID_ARG, "%s: unknown format", who);
+  if (ws_bytes < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative workspace size", who);
+  if (ws != nullptr && !aligned16(ws)) return fail(FP8_ERR_ALIGNMENT, "%s: workspace must be 16-byte aligned", who);
+  if (M == 0 || N == 0) return FP8_OK;
+  if (C == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: null C", who);
+  if (ldc < N) return fail(FP8_ERR_INVALID_ARG, "%s: ldc < N", who);
+  if (!aligned16(C) || ldc % 8 != 0) return fail(FP8_ERR_ALIGNMENT, "%s: C must be 16-byte aligned, ldc %% 8 == 0", who);
+  if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31)) return fail(FP8_ERR_UNSUPPORTED, "%s: size >= 2^31", who);
+  if (K == 0) {
+    cudaError_t e = cudaMemset2DAsync(C, ldc * 2, 0, N * 2, M, stream);
+    return e == cudaSuccess ? FP8_OK : cuda_fail(e, who);
+  }
+  if (A == nullptr || B == nullptr || sa == nullptr || sb == nullptr)
+    return fail(FP8_ERR_INVALID_ARG, "%s: null A, B or scale", who);
+  if (lda < M || ldb < N) return fail(FP8_ERR_INVALID_ARG, "%s: lda < M or ldb < N", who);
+  if (!aligned16(A) || !aligned16(B) || lda % 16 != 0 || ldb % 16 != 0)
+    return fail(FP8_ERR_ALIGNMENT, "%s: A and B must be 16-byte aligned with lda, ldb multiples of 16", who);
+  GemmArgs g{A, B, C, M, N, K, lda, ldb, ldc, (int)fa, (int)fb, sa, sb, false};
+  g.mn = true;
+  g.ws = ws;
+  g.ws_bytes = ws != nullptr ? ws_bytes : 0;
+  const char* why = "launch";
+  cudaError_t e = launch_gemm(g, stream, &why);
+  return e == cudaSuccess ? FP8_OK : cuda_fail(e, why);
+}
+
+// The backward pass. mn: wgrad reads x's codes xq [M, K] and dy's codes dyq [M, N] as they are
+// (MN-major; xqT_save then holds xq and dyqT_ws is unused); otherwise xqT_save [K, M] and
+// dyqT_ws [N, M] are the transposed copies.
 fp8_status_t linear_bwd_impl(const void* dy_bf16, int64_t M, int64_t K, int64_t N, const void* xqT_save,
                              const fp8_tensor_state_t* x_st, const void* wq_kn, const fp8_tensor_state_t* w_st,
                              fp8_tensor_state_t* dy_st, fp8_scaling_t mode, void* dyq_ws, void* dyqT_ws, void* dx_bf16,
-                             void* dw_bf16, void* ws, int64_t ws_bytes, cudaStream_t s, const char* who) {
+                             void* dw_bf16, void* ws, int64_t ws_bytes, cudaStream_t s, const char* who,
+                             bool mn = false) {
   if (M < 0 || K < 0 || N < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative size", who);
   if (M % 16 || K % 16 || N % 16) return fail(FP8_ERR_UNSUPPORTED, "%s: M, K and N must be multiples of 16", who);
   // a buffer may be null only when it holds no elements (an empty token batch)
   if (dyq_ws == nullptr && M * N > 0) return fail(FP8_ERR_INVALID_ARG, "%s: dyq_ws is required", who);
-  if (dw_bf16 != nullptr && ((dyqT_ws == nullptr && M * N > 0) || (xqT_save == nullptr && M * K > 0) ||
+  if (dw_bf16 != nullptr && ((!mn && dyqT_ws == nullptr && M * N > 0) || (xqT_save == nullptr && M * K > 0) ||
                              x_st == nullptr || !x_st->scale_inv))
-    return fail(FP8_ERR_INVALID_ARG, "%s: wgrad needs dyqT_ws, xqT_save and x_st", who);
+    return fail(FP8_ERR_INVALID_ARG, "%s: wgrad needs %s and x_st", who, mn ? "xq_save" : "dyqT_ws, xqT_save");
   if (dx_bf16 != nullptr && (wq_kn == nullptr || w_st == nullptr || !w_st->scale_inv))
     return fail(FP8_ERR_INVALID_ARG, "%s: dgrad needs wq_kn and w_st", who);
   if (ws_bytes < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative workspace size", who);
   if (ws != nullptr && !aligned16(ws)) return fail(FP8_ERR_ALIGNMENT, "%s: workspace must be 16-byte aligned", who);
   fp8_status_t st = quantize_impl(dy_bf16, M, N, N, FP8_E5M2, FP8_GRAN_TENSOR, mode, dy_st, dyq_ws,
-                                  dw_bf16 != nullptr ? dyqT_ws : nullptr, nullptr, s);
+                                  (dw_bf16 != nullptr && !mn) ? dyqT_ws : nullptr, nullptr, s);
   if (st != FP8_OK) return st;
+  if (mn && M > 0 && K > 0 && N > 0) {
+    if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31)) return fail(FP8_ERR_UNSUPPORTED, "%s: size >= 2^31", who);
+    if ((dw_bf16 != nullptr && (!aligned16(xqT_save) || !aligned16(dw_bf16))) ||
+        (dx_bf16 != nullptr && (!aligned16(wq_kn) || !aligned16(dx_bf16))) || !aligned16(dyq_ws))
+      return fail(FP8_ERR_ALIGNMENT, "%s: codes and outputs must be 16-byte aligned", who);
+    // wgrad dW [K,N] = xq^T dyq: A = xq as [M, K] (contraction M, K contiguous), B = dyq as [M, N]
+    GemmArgs gw{xqT_save, dyq_ws, dw_bf16, K, N, M, K, N, N, (int)FP8_E4M3, (int)FP8_E5M2,
+                dw_bf16 != nullptr ? x_st->scale_inv : nullptr, dy_st->scale_inv, false};
+    gw.mn = true;
+    GemmArgs gd{dyq_ws, wq_kn, dx_bf16, M, K, N, N, N, K, (int)FP8_E5M2, (int)FP8_E4M3, dy_st->scale_inv,
+                dx_bf16 != nullptr ? w_st->scale_inv : nullptr, false};
+    const char* why = "launch";
+    cudaError_t e = cudaSuccess;
+    if (dx_bf16 != nullptr && dw_bf16 != nullptr) {
+      e = launch_gemm_group(gw, gd, ws, ws != nullptr ? ws_bytes : 0, s, &why);
+    } else if (dw_bf16 != nullptr) {
+      gw.ws = ws;
+      gw.ws_bytes = ws != nullptr ? ws_bytes : 0;
+      e = launch_gemm(gw, s, &why);
+    } else if (dx_bf16 != nullptr) {
+      return scaled_mm_impl(dyq_ws, FP8_E5M2, wq_kn, FP8_E4M3, M, K, N, N, N, FP8_GRAN_TENSOR, dy_st->scale_inv,
+                            w_st->scale_inv, dx_bf16, K, s, ws, ws_bytes, who);
+    }
+    return e == cudaSuccess ? FP8_OK : cuda_fail(e, why);
+  }
   if (M == 0 || K == 0 || N == 0) {
     // an empty contraction writes zeros; empty outputs write nothing
     if (dx_bf16 != nullptr && (st = scaled_mm_impl(dyq_ws, FP8_E5M2, wq_kn, FP8_E4M3, M, K, N, N, N, FP8_GRAN_TENSOR,
@@ -575,6 +636,25 @@ fp8_status_t fp8_linear_bwd_ws(const void* dy_bf16, int64_t M, int64_t K, int64_
                                void* dx_bf16, void* dw_bf16, void* workspace, int64_t workspace_bytes, void* stream) {
   return linear_bwd_impl(dy_bf16, M, K, N, xqT_save, x_st, wq_kn, w_st, dy_st, mode, dyq_ws, dyqT_ws, dx_bf16, dw_bf16,
                          workspace, workspace_bytes, static_cast<cudaStream_t>(stream), "fp8_linear_bwd_ws");
+}
+
+fp8_status_t fp8_linear_bwd_mn(const void* dy_bf16, int64_t M, int64_t K, int64_t N, const void* xq_save,
+                               const fp8_tensor_state_t* x_st, const void* wq_kn, const fp8_tensor_state_t* w_st,
+                               fp8_tensor_state_t* dy_st, fp8_scaling_t mode, void* dyq_ws, void* dx_bf16, void* dw_bf16,
+                               void* workspace, int64_t workspace_bytes, void* stream) {
+  const char* who = "fp8_linear_bwd_mn";
+  if (workspace_bytes < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative workspace size", who);
+  if (workspace != nullptr && !aligned16(workspace))
+    return fail(FP8_ERR_ALIGNMENT, "%s: workspace must be 16-byte aligned", who);
+  return linear_bwd_impl(dy_bf16, M, K, N, xq_save, x_st, wq_kn, w_st, dy_st, mode, dyq_ws, nullptr, dx_bf16, dw_bf16,
+                         workspace, workspace_bytes, static_cast<cudaStream_t>(stream), who, true);
+}
+
+fp8_status_t fp8_scaled_mm_t(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb, int64_t M, int64_t N,
+                             int64_t K, int64_t lda, int64_t ldb, const float* scale_inv_a, const float* scale_inv_b,
+                             void* C_bf16, int64_t ldc, void* workspace, int64_t workspace_bytes, void* stream) {
+  return scaled_mm_t_impl(A, fa, B, fb, M, N, K, lda, ldb, scale_inv_a, scale_inv_b, C_bf16, ldc, workspace,
+                          workspace_bytes, static_cast<cudaStream_t>(stream), "fp8_scaled_mm_t");
 }
 
 int64_t fp8_linear_bwd_workspace_bytes(int64_t M, int64_t K, int64_t N) {

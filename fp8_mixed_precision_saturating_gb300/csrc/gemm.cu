@@ -134,6 +134,9 @@ struct KProb {
   const uint8_t* sfa;
   const uint8_t* sfb;
   int sf_nkb, sfb_atoms;  // K / 128, atoms along N (ceil(N / 128))
+  // operands stored contraction-major (A as [K, M], B as [K, N], row-major) and read MN-major
+  // by the tensor cores: tiles arrive as boxes of 128 MN x 128 K
+  int mn;
 };
 
 constexpr int kMaxSlots = 160;         // CTAs (or CTA pairs) of a persistent grid
@@ -188,6 +191,7 @@ __device__ __forceinline__ KProb prob_of(const KParams& p, int pi) {
   q.sfb = pi ? b.sfb : a.sfb;
   q.sf_nkb = pi ? b.sf_nkb : a.sf_nkb;
   q.sfb_atoms = pi ? b.sfb_atoms : a.sfb_atoms;
+  q.mn = pi ? b.mn : a.mn;
   return q;
 }
 
@@ -350,8 +354,13 @@ __global__ void __launch_bounds__(Cfg<BN, QF, PAIR, MX>::THREADS, 1)
           if constexpr (PAIR) {
             // both CTAs' bytes land on rank 0's barrier, which alone expects them
             if (rank == 0) mbar_arrive_expect_tx(fb, 2 * STAGE_BYTES);
-            tma_load_2d_pair(sa, tA, full_lead + 8 * stage, kb * BK, arow);
-            tma_load_2d_pair(sa + A_BYTES, tB, full_lead + 8 * stage, kb * BK, brow);
+            if (q.mn) {  // (a CTA's half of B is one 128-column box)
+              tma_load_2d_pair(sa, tA, full_lead + 8 * stage, arow, kb * BK);
+              tma_load_2d_pair(sa + A_BYTES, tB, full_lead + 8 * stage, brow, kb * BK);
+            } else {
+              tma_load_2d_pair(sa, tA, full_lead + 8 * stage, kb * BK, arow);
+              tma_load_2d_pair(sa + A_BYTES, tB, full_lead + 8 * stage, kb * BK, brow);
+            }
           } else if constexpr (MX) {
             // the K block's scale atoms: A's for this tile's 128 rows, B's for its BN columns
             // (atoms past the last column of B are not loaded; their columns are not stored)
@@ -366,8 +375,15 @@ __global__ void __launch_bounds__(Cfg<BN, QF, PAIR, MX>::THREADS, 1)
               bulk_load(sfs + 512 * (1 + a), q.sfb + (static_cast<int64_t>(a0 + a) * q.sf_nkb + kb) * 512, 512, fb);
           } else {
             mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            tma_load_2d(sa, tA, fb, kb * BK, arow);
-            tma_load_2d(sa + A_BYTES, tB, fb, kb * BK, brow);
+            if (q.mn) {
+              tma_load_2d(sa, tA, fb, arow, kb * BK);
+#pragma unroll
+              for (int h = 0; h < C::B_ROWS / 128; ++h)
+                tma_load_2d(sa + A_BYTES + h * (128 * BK), tB, fb, brow + 128 * h, kb * BK);
+            } else {
+              tma_load_2d(sa, tA, fb, kb * BK, arow);
+              tma_load_2d(sa + A_BYTES, tB, fb, kb * BK, brow);
+            }
           }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -418,8 +434,10 @@ __global__ void __launch_bounds__(Cfg<BN, QF, PAIR, MX>::THREADS, 1)
 #endif
           const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
           const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint64_t adesc = smem_desc_sw128(sa);
-          const uint64_t bdesc = smem_desc_sw128(sa + A_BYTES);
+          // K-major: a 32-deep step is 32 bytes along each row; MN-major: 32 rows of 128 bytes
+          const uint64_t adesc = q.mn ? smem_desc_sw128_mn(sa) : smem_desc_sw128(sa);
+          const uint64_t bdesc = q.mn ? smem_desc_sw128_mn(sa + A_BYTES) : smem_desc_sw128(sa + A_BYTES);
+          const uint64_t kstep = q.mn ? (32 * 128) >> 4 : 32 >> 4;
           if constexpr (MX) {
             // this K block's scales into TMEM (the copies and the MMAs below execute in issue
             // order), then four MMAs of 32 K, each taking byte k of every row's scale word
@@ -438,9 +456,9 @@ __global__ void __launch_bounds__(Cfg<BN, QF, PAIR, MX>::THREADS, 1)
             for (int k = 0; k < BK / 32; ++k) {
               const uint32_t accumulate = (kb != kb0 || k != 0);
               if constexpr (PAIR)
-                mma_f8_pair(d, adesc + 2 * k, bdesc + 2 * k, q.idesc, accumulate);
+                mma_f8_pair(d, adesc + kstep * k, bdesc + kstep * k, q.idesc, accumulate);
               else
-                mma_f8(d, adesc + 2 * k, bdesc + 2 * k, q.idesc, accumulate);
+                mma_f8(d, adesc + kstep * k, bdesc + kstep * k, q.idesc, accumulate);
             }
             if constexpr (PAIR)
               mma_commit_pair(bar_empty + 8 * stage, 0x3);  // frees the stage in both CTAs
@@ -1102,7 +1120,7 @@ constexpr int64_t kSplitMaxBytes = int64_t(64) << 20;
 // shape never overlap the counters of another and a reused workspace needs no clearing.
 constexpr int64_t kSplitCounterBytes = 4096 * 4;
 
-TileChoice choose_tile(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters, int max_splits) {
+TileChoice choose_tile(int64_t M, int64_t N, int64_t K, int sms, int pair_clusters, int max_splits, bool mn = false) {
   const int widths[3] = {256, 192, 128};
   const int w_single[3] = {362, 322, 275};
   const int w_pair[3] = {300, 285, 278};
@@ -1110,9 +1128,11 @@ TileChoice choose_tile(int64_t M, int64_t N, int64_t K, int sms, int pair_cluste
   TileChoice best{256, false, 1};
   int64_t best_cost = -1;
   for (int i = 0; i < 3; ++i) {
+    if (mn && widths[i] == 192) continue;  // MN-major B tiles are whole 128-column boxes
     const int64_t tn = (N + widths[i] - 1) / widths[i];
     for (int pair = 0; pair < 2; ++pair) {
       if (pair && (M <= BM || pair_clusters <= 0)) continue;  // a pair computes 256 rows
+      if (pair && mn && widths[i] != 256) continue;
       const int64_t tiles = pair ? (M + 2 * BM - 1) / (2 * BM) * tn : (M + BM - 1) / BM * tn;
       const int64_t slots = pair ? pair_clusters : sms;
       for (int sp = 1; sp <= (widths[i] == 192 ? 1 : max_splits) && sp <= kb; ++sp) {
@@ -1167,10 +1187,16 @@ bool make_problem(const GemmArgs& g, const TileChoice& c, KProb& q, Maps& m, con
   q.num_n = static_cast<int>((g.N + c.bn - 1) / c.bn);
   q.num_kb = static_cast<int>((g.K + BK - 1) / BK);
   q.num_tiles = q.num_m * q.num_n;
+  if (g.mn && (g.mx || g.block_scaled || g.qf >= 0 || c.bn == 192 || (c.pair && c.bn != 256))) {
+    *why = "MN-major operands: per-tensor scales, bf16 output, tiles of whole 128-column boxes";
+    return false;
+  }
+  q.mn = g.mn ? 1 : 0;
   q.idesc = g.mx ? idesc_mxf8(static_cast<uint32_t>(g.fa), static_cast<uint32_t>(g.fb), static_cast<uint32_t>(rows),
                               static_cast<uint32_t>(c.bn))
                  : idesc_f8(static_cast<uint32_t>(g.fa), static_cast<uint32_t>(g.fb), static_cast<uint32_t>(rows),
                             static_cast<uint32_t>(c.bn));
+  if (g.mn) q.idesc |= idesc_mn_major();
   q.sfa = g.mx ? g.sfa8 : nullptr;
   q.sfb = g.mx ? g.sfb8 : nullptr;
   q.sf_nkb = static_cast<int>(g.K / 128);
@@ -1192,8 +1218,11 @@ bool make_problem(const GemmArgs& g, const TileChoice& c, KProb& q, Maps& m, con
   const uint32_t b_rows = c.pair ? static_cast<uint32_t>(c.bn / 2) : static_cast<uint32_t>(c.bn);
   const bool cmap = g.mx ? encode_tmap_2d(&m.c, g.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.N, g.M, g.ldc * 2, 32, 32, 64)
                          : make_map(&m.c, g.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.N, g.M, g.ldc * 2, 64, 32);
-  if (!make_map(&m.a, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.M, g.lda, BK, BM) ||
-      !make_map(&m.b, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.N, g.ldb, BK, b_rows) || !cmap) {
+  const bool amap = g.mn ? make_map(&m.a, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.M, g.K, g.lda, 128, BK)
+                        : make_map(&m.a, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.M, g.lda, BK, BM);
+  const bool bmap = g.mn ? make_map(&m.b, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.N, g.K, g.ldb, 128, BK)
+                        : make_map(&m.b, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.K, g.N, g.ldb, BK, b_rows);
+  if (!amap || !bmap || !cmap) {
     *why = "cuTensorMapEncodeTiled failed (driver entry point missing or tensor map rejected)";
     return false;
   }
@@ -1492,12 +1521,12 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why
 #endif
     choice = {FP8GB_FORCE_BN, FP8GB_FORCE_PAIR != 0, 1};
 #else
-    choice = choose_tile(g.M, g.N, g.K, num_sms(), pair_capacity(), g.qf < 0 && g.ws != nullptr ? 2 : 1);
+    choice = choose_tile(g.M, g.N, g.K, num_sms(), pair_capacity(), g.qf < 0 && g.ws != nullptr ? 2 : 1, g.mn);
     // a workspace too small for the best split falls back to the best unsplit shape
     if (choice.splits > 1) {
       const SplitLayout l = split_layout(g.M, g.N, choice);
       if (l.total_bytes > g.ws_bytes || l.slices * 4 > kSplitCounterBytes)
-        choice = choose_tile(g.M, g.N, g.K, num_sms(), pair_capacity(), 1);
+        choice = choose_tile(g.M, g.N, g.K, num_sms(), pair_capacity(), 1, g.mn);
     }
 #endif
   }

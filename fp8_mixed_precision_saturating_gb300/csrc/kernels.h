@@ -127,6 +127,9 @@ struct GemmArgs {
   bool mx = false;
   const uint8_t* sfa8 = nullptr;
   const uint8_t* sfb8 = nullptr;
+  // operands stored contraction-major: A as [K, M] (lda >= M) and B as [K, N] (ldb >= N),
+  // row-major, read MN-major (per-tensor scales, bf16 output only)
+  bool mn = false;
 };
 // Returns cudaSuccess, or an error; `why` receives a static message for host-side failures.
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why);

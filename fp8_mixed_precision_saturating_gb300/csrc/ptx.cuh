@@ -351,6 +351,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for an MN-major tile written by TMA as boxes of 128 MN bytes x K rows with the
+// 128-byte swizzle: 8-row K groups 1024 bytes apart (stride byte offset), consecutive 128-byte
+// MN chunks 16 KB apart (leading byte offset: one box of 128 K rows each).
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);          // start address
+  d |= static_cast<uint64_t>(16384u >> 4) << 16;                // leading byte offset
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;                 // stride byte offset
+  d |= static_cast<uint64_t>(1u) << 46;                         // version
+  d |= static_cast<uint64_t>(2u) << 61;                         // 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor for kind::f8f6f4, fp32 accumulator, both operands K-major.
 // Format codes: 0 = E4M3, 1 = E5M2.
 __host__ __device__ constexpr uint32_t idesc_f8(uint32_t afmt, uint32_t bfmt, uint32_t M, uint32_t N) {
@@ -359,5 +372,8 @@ __host__ __device__ constexpr uint32_t idesc_f8(uint32_t afmt, uint32_t bfmt, ui
          | ((N >> 3) << 17)
          | ((M >> 4) << 24);
 }
+
+// Bits that mark A and B MN-major in an instruction descriptor.
+__host__ __device__ constexpr uint32_t idesc_mn_major() { return (1u << 15) | (1u << 16); }
 
 }  // namespace fp8gb

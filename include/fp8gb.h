@@ -338,6 +338,34 @@ fp8_status_t fp8_linear_bwd_ws(const void* dy_bf16, int64_t M, int64_t K, int64_
                                fp8_tensor_state_t* dy_st, fp8_scaling_t mode, void* dyq_ws, void* dyqT_ws,
                                void* dx_bf16, void* dw_bf16, void* workspace, int64_t workspace_bytes, void* stream);
 
+/* fp8_linear_bwd_ws whose weight gradient reads x's saved codes xq_save [M,K] (as the forward
+ * writes them, with no transposed copy) and dy's codes dyq_ws [M,N] as they are: the tensor
+ * cores read both MN-major (the contraction runs over the tokens, the rows of both), so the dy
+ * cast writes one copy of the codes (3 bytes per element moved instead of 4) and the forward
+ * needs no xqT_save. [GUARD] "What an interviewer would ask next": E5M2 gradients; the result
+ * definition is fp8_linear_bwd's (the same per-tensor scales, products and fp32 accumulation;
+ * only the operands' layout in shared memory differs):
+ *   dgrad  dx [M,K] = d_dy d_w  dyq wq_kn^T
+ *   wgrad  dW [K,N] = d_x  d_dy xq_save^T dyq
+ * dyq_ws [M,N] caller scratch (16-byte aligned); workspace as fp8_linear_bwd_ws (size from
+ * fp8_linear_bwd_workspace_bytes). M, K, N multiples of 16; dx or dw may be NULL. */
+fp8_status_t fp8_linear_bwd_mn(const void* dy_bf16, int64_t M, int64_t K, int64_t N, const void* xq_save,
+                               const fp8_tensor_state_t* x_st, const void* wq_kn, const fp8_tensor_state_t* w_st,
+                               fp8_tensor_state_t* dy_st, fp8_scaling_t mode, void* dyq_ws, void* dx_bf16,
+                               void* dw_bf16, void* workspace, int64_t workspace_bytes, void* stream);
+
+/* C [M,N] (bf16, ldc) = A^T B for operands stored contraction-major: A [K,M] row-major (lda >= M)
+ * and B [K,N] row-major (ldb >= N); C_ij = bf16( d_a d_b sum_k a_ki b_kj ), fp32 accumulation,
+ * per-tensor scales. The tensor cores read both operands MN-major, so a weight gradient
+ * x_q^T dy_q takes the codes as the casts wrote them. [SPEED] "Explanation": the scaled FP8
+ * matmul; the page lays operands out contiguous along the contraction for the library it
+ * calls, which this layout does without. A, B 16-byte aligned, lda and ldb multiples of 16, ldc
+ * of 8; workspace as fp8_scaled_mm_ws (split K for few-tile outputs; size from
+ * fp8_scaled_mm_workspace_bytes(M, N, K)). */
+fp8_status_t fp8_scaled_mm_t(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb, int64_t M, int64_t N,
+                             int64_t K, int64_t lda, int64_t ldb, const float* scale_inv_a, const float* scale_inv_b,
+                             void* C_bf16, int64_t ldc, void* workspace, int64_t workspace_bytes, void* stream);
+
 /* Workspace bytes fp8_linear_bwd_ws uses for these sizes with dx and dW both requested on the
  * current device (0: it would not split). Negative on a CUDA error. */
 int64_t fp8_linear_bwd_workspace_bytes(int64_t M, int64_t K, int64_t N);
