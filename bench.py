@@ -18,8 +18,9 @@ Sub-records in the same line, each with its own roofline, kernel times and oracl
                     UE8M0 scale per 32 contraction elements, applied by the tensor cores):
                     W's cast down its columns (written as W_q^T) || x's cast along its rows,
                     the block-scaled (kind::mxf8f6f4) GEMM
-  backward_upproj   M=16384, K=1024, N=4096: dy's E5M2 cast (current scaling, dy_q and dy_q^T),
-                    dgrad and wgrad in one grouped launch
+  backward_upproj   M=16384, K=1024, N=4096: dy's E5M2 cast (current scaling, dy_q only),
+                    dgrad and wgrad in one grouped launch, the wgrad reading x_q and dy_q
+                    MN-major (no transposed copies)
   delayed_loop      32768 tokens, d 1536 -> 6144, history 16: one layer-step (optimizer step
                     fused with W's refresh, x cast, forward, dy cast, dgrad + wgrad, commit)
                     and the 12-layer step
@@ -515,8 +516,9 @@ def bench_finegrained_mx(ctx, steps, warmup):
 
 
 def bench_backward(ctx, steps, warmup):
-    """dy's per-tensor E5M2 cast (current scaling: amax pass, then dy_q and dy_q^T in one pass)
-    and the grouped dgrad + wgrad launch, with x's and W's saved codes cast once beforehand."""
+    """dy's per-tensor E5M2 cast (current scaling: amax pass, then dy_q in one pass) and the
+    grouped dgrad + wgrad launch, with x's and W's saved codes cast once beforehand. The wgrad
+    problem reads x_q [M, K] and dy_q [M, N] MN-major, so no cast writes a transposed copy."""
     from datagen import workload_inputs
     torch, g, stream, flush = ctx["torch"], ctx["g"], ctx["stream"], ctx["flush"]
     M, K, N = BWD["M"], BWD["K"], BWD["N"]
@@ -526,19 +528,19 @@ def bench_backward(ctx, steps, warmup):
     bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
     T, CUR = g.FP8_GRAN_TENSOR, g.FP8_SCALE_CURRENT
     xst, wst, gst = g.TensorState(), g.TensorState(), g.TensorState()
-    wq, wqT, xq, xqT, dyq, dyqT = u8(K, N), u8(N, K), u8(M, K), u8(K, M), u8(M, N), u8(N, M)
+    wq, wqT, xq, dyq = u8(K, N), u8(N, K), u8(M, K), u8(M, N)
     dx, dw = bf(M, K), bf(K, N)
     with torch.cuda.stream(stream):
         g.fp8_requantize_weights(wm, K, N, T, CUR, wst, wq, wqT)
-        g.fp8_quantize(x, M, K, K, g.FP8_E4M3, T, CUR, xst, xq, xqT)
-    bwd = [g.mm_problem(xqT, 0, dyqT, 1, K, N, M, M, M, xst.scale_inv, gst.scale_inv, dw, N),
+        g.fp8_quantize(x, M, K, K, g.FP8_E4M3, T, CUR, xst, xq, None)
+    bwd = [g.mm_problem(xq, 0, dyq, 1, K, N, M, K, N, xst.scale_inv, gst.scale_inv, dw, N, mn_major=1),
            g.mm_problem(dyq, 1, wq, 0, M, K, N, N, N, gst.scale_inv, wst.scale_inv, dx, K)]
     wsb = g.fp8_scaled_mm_grouped_workspace_bytes(bwd)
     ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
     flops = 2 * 2.0 * M * N * K
     stages = [
-        Stage("bwd_cast_dy", lambda: g.fp8_quantize(dy, M, N, N, g.FP8_E5M2, T, CUR, gst, dyq, dyqT), 1,
-              nbytes=M * N * 4.0),
+        Stage("bwd_cast_dy", lambda: g.fp8_quantize(dy, M, N, N, g.FP8_E5M2, T, CUR, gst, dyq, None), 1,
+              nbytes=M * N * 3.0),
         Stage("bwd_gemm", lambda: g.fp8_scaled_mm_grouped(bwd, ws, wsb), 1, flops=flops),
     ]
 
@@ -551,7 +553,8 @@ def bench_backward(ctx, steps, warmup):
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
             "steps": steps, "config": {"workload": "upproj_bwd", "M_tokens": M, "d_model": K, "d_ff": N,
                                        "dy": "bf16 sign * 1e-4 * exp(2 z); E5M2 per tensor, current scaling",
-                                       "step": "dy cast (dy_q, dy_q^T), dgrad + wgrad in one grouped launch"},
+                                       "step": "dy cast (dy_q), dgrad + wgrad in one grouped launch, "
+                                               "wgrad reading x_q and dy_q MN-major"},
             "roofline": roofline(stages, stage_ms, ctx["hbm"], ctx["bf16_tf"], ctx["peak_src"], name="bwd_gemm"),
             "kernels": kernel_records(stages, stage_ms, ctx["hbm"], ctx["fp8_peak"])}
 
@@ -574,7 +577,7 @@ def bench_delayed_loop(ctx, steps, warmup):
     D, T = g.FP8_SCALE_DELAYED, g.FP8_GRAN_TENSOR
     st = [[g.TensorState(H) for _ in range(3)] for _ in range(L)]
     wq, wqT = [u8(K, N) for _ in range(L)], [u8(N, K) for _ in range(L)]
-    xq, xqT, dyq, dyqT = u8(M, K), u8(K, M), u8(M, N), u8(N, M)
+    xq, dyq = u8(M, K), u8(M, N)
     y, dx, dw = bf(M, N), bf(M, K), bf(K, N)
     wsb = g.fp8_linear_bwd_workspace_bytes(M, K, N)
     ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
@@ -582,8 +585,8 @@ def bench_delayed_loop(ctx, steps, warmup):
     def layer_step(l):  # 6 launches: update + requantise, x cast, forward GEMM, dy cast, grouped bwd, commit
         ws_, xs, gs = st[l]
         g.fp8_update_requantize_weights(W[l], delta[l], K, N, D, ws_, wq[l], wqT[l])
-        g.fp8_linear_fwd(x, M, K, N, wqT[l], ws_, None, xs, T, D, xq, xqT, None, y)
-        g.fp8_linear_bwd_ws(dy, M, K, N, xqT, xs, wq[l], ws_, gs, D, dyq, dyqT, dx, dw, ws, wsb)
+        g.fp8_linear_fwd(x, M, K, N, wqT[l], ws_, None, xs, T, D, xq, None, None, y)
+        g.fp8_linear_bwd_mn(dy, M, K, N, xq, xs, wq[l], ws_, gs, D, dyq, dx, dw, ws, wsb)
         g.fp8_history_commit_many([ws_, xs, gs])
 
     with torch.cuda.stream(stream):
@@ -591,17 +594,17 @@ def bench_delayed_loop(ctx, steps, warmup):
             layer_step(l)
         torch.cuda.synchronize()
     ws0, xs0, gs0 = st[0]
-    bwd = [g.mm_problem(xqT, 0, dyqT, 1, K, N, M, M, M, xs0.scale_inv, gs0.scale_inv, dw, N),
+    bwd = [g.mm_problem(xq, 0, dyq, 1, K, N, M, K, N, xs0.scale_inv, gs0.scale_inv, dw, N, mn_major=1),
            g.mm_problem(dyq, 1, wq[0], 0, M, K, N, N, N, gs0.scale_inv, ws0.scale_inv, dx, K)]
     fl = 2.0 * M * N * K
     stages = [
         Stage("loop_update_w", lambda: g.fp8_update_requantize_weights(W[0], delta[0], K, N, D, ws0, wq[0], wqT[0]), 1,
               nbytes=K * N * 10.0),
-        Stage("loop_cast_x", lambda: g.fp8_quantize(x, M, K, K, g.FP8_E4M3, T, D, xs0, xq, xqT), 1, nbytes=M * K * 4.0),
+        Stage("loop_cast_x", lambda: g.fp8_quantize(x, M, K, K, g.FP8_E4M3, T, D, xs0, xq, None), 1, nbytes=M * K * 3.0),
         Stage("loop_gemm_fwd", lambda: g.fp8_scaled_mm_ws(xq, 0, wqT[0], 0, M, N, K, K, K, T, xs0.scale_inv,
                                                             ws0.scale_inv, y, N, ws, wsb), 1, flops=fl),
-        Stage("loop_cast_dy", lambda: g.fp8_quantize(dy, M, N, N, g.FP8_E5M2, T, D, gs0, dyq, dyqT), 1,
-              nbytes=M * N * 4.0),
+        Stage("loop_cast_dy", lambda: g.fp8_quantize(dy, M, N, N, g.FP8_E5M2, T, D, gs0, dyq, None), 1,
+              nbytes=M * N * 3.0),
         Stage("loop_gemm_bwd", lambda: g.fp8_scaled_mm_grouped(bwd, ws, wsb), 1, flops=2 * fl),
         Stage("loop_commit", lambda: g.fp8_history_commit_many([ws0, xs0, gs0]), 1),
     ]
@@ -649,20 +652,20 @@ def bench_gpt2(ctx, steps, warmup):
     u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device="cuda")
     bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
     wst, xst, gst = g.TensorState(H), g.TensorState(H), g.TensorState(H)
-    wq, wqT, xq, xqT, dyq, dyqT = u8(K, N), u8(N, K), u8(M, K), u8(K, M), u8(M, N), u8(N, M)
+    wq, wqT, xq, dyq = u8(K, N), u8(N, K), u8(M, K), u8(M, N)
     y, dx, dw = bf(M, N), bf(M, K), bf(K, N)
     D, T = g.FP8_SCALE_DELAYED, g.FP8_GRAN_TENSOR
     fl = 2.0 * M * N * K
-    bwd = [g.mm_problem(xqT, 0, dyqT, 1, K, N, M, M, M, xst.scale_inv, gst.scale_inv, dw, N),
+    bwd = [g.mm_problem(xq, 0, dyq, 1, K, N, M, K, N, xst.scale_inv, gst.scale_inv, dw, N, mn_major=1),
            g.mm_problem(dyq, 1, wq, 0, M, K, N, N, N, gst.scale_inv, wst.scale_inv, dx, K)]
     wsb = max(g.fp8_scaled_mm_grouped_workspace_bytes(bwd), g.fp8_scaled_mm_workspace_bytes(M, N, K))
     ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
     stages = [
         Stage("requant_w", lambda: g.fp8_requantize_weights(wm, K, N, T, D, wst, wq, wqT), 1, nbytes=K * N * 4.0),
-        Stage("quant_x", lambda: g.fp8_quantize(x, M, K, K, g.FP8_E4M3, T, D, xst, xq, xqT), 1, nbytes=M * K * 4.0),
+        Stage("quant_x", lambda: g.fp8_quantize(x, M, K, K, g.FP8_E4M3, T, D, xst, xq, None), 1, nbytes=M * K * 3.0),
         Stage("gemm_fwd", lambda: g.fp8_scaled_mm_ws(xq, 0, wqT, 0, M, N, K, K, K, T, xst.scale_inv, wst.scale_inv,
                                                      y, N, ws, wsb), 1, flops=fl),
-        Stage("quant_dy", lambda: g.fp8_quantize(dy, M, N, N, g.FP8_E5M2, T, D, gst, dyq, dyqT), 1, nbytes=M * N * 4.0),
+        Stage("quant_dy", lambda: g.fp8_quantize(dy, M, N, N, g.FP8_E5M2, T, D, gst, dyq, None), 1, nbytes=M * N * 3.0),
         Stage("gemm_bwd", lambda: g.fp8_scaled_mm_grouped(bwd, ws, wsb), 1, flops=2 * fl),
         Stage("commit", lambda: g.fp8_history_commit_many([wst, xst, gst]), 1),
     ]
@@ -908,7 +911,7 @@ def run_delayed_loop(g, torch, fp8_peak, layers=12, steps=50, tokens=32768, d=15
     delta = [torch.randn(d, n, generator=gen, device="cuda") * 1e-3 for _ in range(layers)]
     st = [[g.TensorState(hist) for _ in range(3)] for _ in range(layers)]
     wq, wqT = [u8(d, n) for _ in range(layers)], [u8(n, d) for _ in range(layers)]
-    xq, xqT, dyq, dyqT = u8(tokens, d), u8(d, tokens), u8(tokens, n), u8(n, tokens)
+    xq, dyq = u8(tokens, d), u8(tokens, n)
     y, dx, dw = bf(tokens, n), bf(tokens, d), bf(d, n)
     wsb = g.fp8_linear_bwd_workspace_bytes(tokens, d, n)
     ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
@@ -917,8 +920,8 @@ def run_delayed_loop(g, torch, fp8_peak, layers=12, steps=50, tokens=32768, d=15
     def layer_step(l):  # the layer API: 6 launches (update + requantise, x cast, forward GEMM,
         ws_, xs, gs = st[l]  # dy cast, grouped dgrad + wgrad, history commit)
         g.fp8_update_requantize_weights(W[l], delta[l], d, n, D, ws_, wq[l], wqT[l])
-        g.fp8_linear_fwd(x, tokens, d, n, wqT[l], ws_, None, xs, T, D, xq, xqT, None, y)
-        g.fp8_linear_bwd_ws(dy, tokens, d, n, xqT, xs, wq[l], ws_, gs, D, dyq, dyqT, dx, dw, ws, wsb)
+        g.fp8_linear_fwd(x, tokens, d, n, wqT[l], ws_, None, xs, T, D, xq, None, None, y)
+        g.fp8_linear_bwd_mn(dy, tokens, d, n, xq, xs, wq[l], ws_, gs, D, dyq, dx, dw, ws, wsb)
         g.fp8_history_commit_many([ws_, xs, gs])
 
     for l in range(layers):  # untimed first step (bootstrap casts)

@@ -56,6 +56,7 @@ class fp8_mm_problem_t(ctypes.Structure):
         ("scale_inv_b", ctypes.c_void_p),
         ("C_bf16", ctypes.c_void_p),
         ("ldc", ctypes.c_int64),
+        ("mn_major", ctypes.c_int32),
     ]
 
 
@@ -236,10 +237,10 @@ def fp8_quantize_many(jobs, stream=None):
     return _check(lib.fp8_quantize_many(arr, len(jobs), _stream(stream)))
 
 
-def mm_problem(A, fa, B, fb, M, N, K, lda, ldb, scale_inv_a, scale_inv_b, C, ldc):
+def mm_problem(A, fa, B, fb, M, N, K, lda, ldb, scale_inv_a, scale_inv_b, C, ldc, mn_major=0):
     """One fp8_mm_problem_t (per-tensor scales) for fp8_scaled_mm_grouped."""
     return fp8_mm_problem_t(_ptr(A), fa, _ptr(B), fb, M, N, K, lda, ldb, _ptr(scale_inv_a), _ptr(scale_inv_b),
-                            _ptr(C), ldc)
+                            _ptr(C), ldc, mn_major)
 
 
 def fp8_scaled_mm_grouped(problems, workspace=None, workspace_bytes=0, stream=None):

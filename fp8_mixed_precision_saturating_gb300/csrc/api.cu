@@ -468,45 +468,6 @@ fp8_status_t fp8_linear_fwd(const void* x_bf16, int64_t M, int64_t K, int64_t N,
 
 namespace {
 
-// Checks of fp8_scaled_mm for one problem of a grouped call (per-tensor scales, M, N, K > 0).
-fp8_status_t check_group_problem(const fp8_mm_problem_t& q, int i, const char* who) {
-  if ((q.fa != FP8_E4M3 && q.fa != FP8_E5M2) || (q.fb != FP8_E4M3 && q.fb != FP8_E5M2))
-    return fail(FP8_ERR_INVALID_ARG, "%s: problem %d: unknown format", who, i);
-  if (q.M <= 0 || q.N <= 0 || q.K <= 0) return fail(FP8_ERR_INVALID_ARG, "%s: problem %d: M, N, K must be positive", who, i);
-  if (q.M >= (1ll << 31) || q.N >= (1ll << 31) || q.K >= (1ll << 31))
-    return fail(FP8_ERR_UNSUPPORTED, "%s: problem %d: size >= 2^31", who, i);
-  if (q.A == nullptr || q.B == nullptr || q.C_bf16 == nullptr || q.scale_inv_a == nullptr || q.scale_inv_b == nullptr)
-    return fail(FP8_ERR_INVALID_ARG, "%s: problem %d: null A, B, C or scale", who, i);
-  if (q.lda < q.K || q.ldb < q.K || q.ldc < q.N) return fail(FP8_ERR_INVALID_ARG, "%s: problem %d: lda, ldb < K or ldc < N", who, i);
-  if (!aligned16(q.A) || !aligned16(q.B) || !aligned16(q.C_bf16) || q.lda % 16 || q.ldb % 16 || q.ldc % 8)
-    return fail(FP8_ERR_ALIGNMENT, "%s: problem %d: A, B, C 16-byte aligned, lda and ldb multiples of 16, ldc of 8",
-                who, i);
-  return FP8_OK;
-}
-
-GemmArgs group_args(const fp8_mm_problem_t& q) {
-  return GemmArgs{q.A, q.B, q.C_bf16, q.M, q.N, q.K, q.lda, q.ldb, q.ldc, (int)q.fa, (int)q.fb,
-                  q.scale_inv_a, q.scale_inv_b, false};
-}
-
-fp8_status_t grouped_impl(const fp8_mm_problem_t* pr, int32_t n, void* ws, int64_t ws_bytes, cudaStream_t s,
-                          const char* who) {
-  if (n < 1 || n > 2 || pr == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: 1 or 2 problems", who);
-  if (ws_bytes < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative workspace size", who);
-  if (ws != nullptr && !aligned16(ws)) return fail(FP8_ERR_ALIGNMENT, "%s: workspace must be 16-byte aligned", who);
-  for (int i = 0; i < n; ++i) {
-    const fp8_status_t st = check_group_problem(pr[i], i, who);
-    if (st != FP8_OK) return st;
-  }
-  if (n == 1)
-    return scaled_mm_impl(pr[0].A, pr[0].fa, pr[0].B, pr[0].fb, pr[0].M, pr[0].N, pr[0].K, pr[0].lda, pr[0].ldb,
-                          FP8_GRAN_TENSOR, pr[0].scale_inv_a, pr[0].scale_inv_b, pr[0].C_bf16, pr[0].ldc, s, ws,
-                          ws_bytes, who);
-  const char* why = "launch";
-  const cudaError_t e = launch_gemm_group(group_args(pr[0]), group_args(pr[1]), ws, ws_bytes, s, &why);
-  return e == cudaSuccess ? FP8_OK : cuda_fail(e, why);
-}
-
 // C [M,N] = A^T B with A [K, M] and B [K, N] row-major, read MN-major (per-tensor scales).
 fp8_status_t scaled_mm_t_impl(const void* A, fp8_format_t fa, const void* B, fp8_format_t fb, int64_t M, int64_t N,
                               int64_t K, int64_t lda, int64_t ldb, const float* sa, const float* sb, void* C,
@@ -536,6 +497,52 @@ fp8_status_t scaled_mm_t_impl(const void* A, fp8_format_t fa, const void* B, fp8
   g.ws_bytes = ws != nullptr ? ws_bytes : 0;
   const char* why = "launch";
   cudaError_t e = launch_gemm(g, stream, &why);
+  return e == cudaSuccess ? FP8_OK : cuda_fail(e, why);
+}
+
+// Checks of fp8_scaled_mm for one problem of a grouped call (per-tensor scales, M, N, K > 0).
+fp8_status_t check_group_problem(const fp8_mm_problem_t& q, int i, const char* who) {
+  if ((q.fa != FP8_E4M3 && q.fa != FP8_E5M2) || (q.fb != FP8_E4M3 && q.fb != FP8_E5M2))
+    return fail(FP8_ERR_INVALID_ARG, "%s: problem %d: unknown format", who, i);
+  if (q.M <= 0 || q.N <= 0 || q.K <= 0) return fail(FP8_ERR_INVALID_ARG, "%s: problem %d: M, N, K must be positive", who, i);
+  if (q.M >= (1ll << 31) || q.N >= (1ll << 31) || q.K >= (1ll << 31))
+    return fail(FP8_ERR_UNSUPPORTED, "%s: problem %d: size >= 2^31", who, i);
+  if (q.A == nullptr || q.B == nullptr || q.C_bf16 == nullptr || q.scale_inv_a == nullptr || q.scale_inv_b == nullptr)
+    return fail(FP8_ERR_INVALID_ARG, "%s: problem %d: null A, B, C or scale", who, i);
+  if (q.mn_major != 0 && q.mn_major != 1) return fail(FP8_ERR_INVALID_ARG, "%s: problem %d: mn_major is 0 or 1", who, i);
+  if (q.mn_major ? (q.lda < q.M || q.ldb < q.N || q.ldc < q.N) : (q.lda < q.K || q.ldb < q.K || q.ldc < q.N))
+    return fail(FP8_ERR_INVALID_ARG, "%s: problem %d: leading dimension too small", who, i);
+  if (!aligned16(q.A) || !aligned16(q.B) || !aligned16(q.C_bf16) || q.lda % 16 || q.ldb % 16 || q.ldc % 8)
+    return fail(FP8_ERR_ALIGNMENT, "%s: problem %d: A, B, C 16-byte aligned, lda and ldb multiples of 16, ldc of 8",
+                who, i);
+  return FP8_OK;
+}
+
+GemmArgs group_args(const fp8_mm_problem_t& q) {
+  GemmArgs g{q.A, q.B, q.C_bf16, q.M, q.N, q.K, q.lda, q.ldb, q.ldc, (int)q.fa, (int)q.fb,
+             q.scale_inv_a, q.scale_inv_b, false};
+  g.mn = q.mn_major == 1;
+  return g;
+}
+
+fp8_status_t grouped_impl(const fp8_mm_problem_t* pr, int32_t n, void* ws, int64_t ws_bytes, cudaStream_t s,
+                          const char* who) {
+  if (n < 1 || n > 2 || pr == nullptr) return fail(FP8_ERR_INVALID_ARG, "%s: 1 or 2 problems", who);
+  if (ws_bytes < 0) return fail(FP8_ERR_INVALID_ARG, "%s: negative workspace size", who);
+  if (ws != nullptr && !aligned16(ws)) return fail(FP8_ERR_ALIGNMENT, "%s: workspace must be 16-byte aligned", who);
+  for (int i = 0; i < n; ++i) {
+    const fp8_status_t st = check_group_problem(pr[i], i, who);
+    if (st != FP8_OK) return st;
+  }
+  if (n == 1 && pr[0].mn_major)
+    return scaled_mm_t_impl(pr[0].A, pr[0].fa, pr[0].B, pr[0].fb, pr[0].M, pr[0].N, pr[0].K, pr[0].lda, pr[0].ldb,
+                            pr[0].scale_inv_a, pr[0].scale_inv_b, pr[0].C_bf16, pr[0].ldc, ws, ws_bytes, s, who);
+  if (n == 1)
+    return scaled_mm_impl(pr[0].A, pr[0].fa, pr[0].B, pr[0].fb, pr[0].M, pr[0].N, pr[0].K, pr[0].lda, pr[0].ldb,
+                          FP8_GRAN_TENSOR, pr[0].scale_inv_a, pr[0].scale_inv_b, pr[0].C_bf16, pr[0].ldc, s, ws,
+                          ws_bytes, who);
+  const char* why = "launch";
+  const cudaError_t e = launch_gemm_group(group_args(pr[0]), group_args(pr[1]), ws, ws_bytes, s, &why);
   return e == cudaSuccess ? FP8_OK : cuda_fail(e, why);
 }
 

@@ -219,7 +219,9 @@ fp8_status_t fp8_scaled_mm_ws(const void* A, fp8_format_t fa, const void* B, fp8
 int64_t fp8_scaled_mm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* One per-tensor-scaled GEMM of a grouped call: the arguments of fp8_scaled_mm with
- * gran = FP8_GRAN_TENSOR (C_bf16 [M,N] = bf16(d_a d_b sum_k a_ik b_jk)). */
+ * gran = FP8_GRAN_TENSOR (C_bf16 [M,N] = bf16(d_a d_b sum_k a_ik b_jk)) when mn_major is 0
+ * (A [M,K], B [N,K], contiguous along K); with mn_major 1 the arguments of fp8_scaled_mm_t
+ * (A [K,M] with lda >= M, B [K,N] with ldb >= N, C = A^T B). */
 typedef struct {
   const void* A;
   fp8_format_t fa;
@@ -230,6 +232,7 @@ typedef struct {
   const float* scale_inv_b;
   void* C_bf16;
   int64_t ldc;
+  int32_t mn_major;
 } fp8_mm_problem_t;
 
 /* n (1 or 2) independent GEMMs in one persistent launch: their tiles share the GPU (longest

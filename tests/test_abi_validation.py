@@ -83,6 +83,10 @@ def test_grouped_and_many_checks(g):
     refused(g, g.FP8_ERR_INVALID_ARG, "1 or 2 problems", g.fp8_scaled_mm_grouped, [p, p, p])
     refused(g, g.FP8_ERR_INVALID_ARG, "negative workspace", g.fp8_scaled_mm_grouped, [p, p], C16, -1)
     refused(g, g.FP8_ERR_ALIGNMENT, "workspace", g.fp8_scaled_mm_grouped, [p, p], ODD, 64)
+    bad_mn = g.mm_problem(A16, 0, B16, 0, 16, 16, 16, 16, 16, S16, S16, C16, 16, mn_major=2)
+    refused(g, g.FP8_ERR_INVALID_ARG, "mn_major is 0 or 1", g.fp8_scaled_mm_grouped, [p, bad_mn])
+    short_mn = g.mm_problem(A16, 0, B16, 0, 32, 16, 16, 16, 16, S16, S16, C16, 16, mn_major=1)  # lda < M
+    refused(g, g.FP8_ERR_INVALID_ARG, "leading dimension", g.fp8_scaled_mm_grouped, [p, short_mn])
     sa, sb = state(g, base=0x50000), state(g, base=0x60000)
     j = g.quant_job(A16, 16, 16, 16, 0, 0, sa, B16, C16)
     refused(g, g.FP8_ERR_INVALID_ARG, "jobs", g.fp8_quantize_many, [])

@@ -53,6 +53,36 @@ def test_scaled_mm_t_against_oracle(g, M, N, K, fa, fb):
     within(host_bf16_f64(C), ref, mag)
 
 
+@pytest.mark.parametrize("pa,pb", [((640, 384, 256, 0, 1), (256, 640, 384, 1, 0)),
+                                   ((1024, 1536, 4096, 0, 1), (4096, 1024, 512, 1, 0))])
+def test_grouped_mn_major_beside_k_major(g, pa, pb):
+    """One grouped launch of an MN-major problem (A [K, M], B [K, N]) beside a K-major one, split
+    K through the workspace; each against the oracle."""
+    rng = np.random.default_rng(pa[0] + pb[2])
+    probs, keep = [], []
+    for (M, N, K, fa, fb), mn in ((pa, 1), (pb, 0)):
+        sa, sb = np.float32(rng.uniform(0.05, 2)), np.float32(rng.uniform(0.05, 2))
+        if mn:
+            A, B = finite_codes(rng, (K, M), FMTS[fa]), finite_codes(rng, (K, N), FMTS[fb])
+            Ar, Br, lda, ldb = A.T, B.T, M, N
+        else:
+            A, B = finite_codes(rng, (M, K), FMTS[fa]), finite_codes(rng, (N, K), FMTS[fb])
+            Ar, Br, lda, ldb = A, B, K, K
+        C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        Ad, Bd, da, db = dev_u8(A), dev_u8(B), f32_scalar(sa), f32_scalar(sb)
+        keep += [Ad, Bd, da, db]
+        probs.append(g.mm_problem(Ad, fa, Bd, fb, M, N, K, lda, ldb, da, db, C, N, mn_major=mn))
+        keep.append((C, np.ascontiguousarray(Ar), FMTS[fa], np.ascontiguousarray(Br), FMTS[fb], sa, sb))
+    nbytes = g.fp8_scaled_mm_grouped_workspace_bytes(probs)
+    ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    g.fp8_scaled_mm_grouped(probs, ws, nbytes)
+    torch.cuda.synchronize()
+    g.fp8_poll_device_error()
+    for C, A, fa, B, fb, sa, sb in (k for k in keep if isinstance(k, tuple)):
+        ref, mag, _ = gemm.scaled_mm(A, fa, B, fb, sa, sb)
+        within(host_bf16_f64(C), ref, mag)
+
+
 def test_scaled_mm_t_padded_leading_dimensions(g):
     rng = np.random.default_rng(5)
     M, N, K, lda, ldb, ldc = 200, 300, 256, 224, 320, 304
