@@ -720,14 +720,17 @@ __global__ void __launch_bounds__(Cfg<BN, QF, PAIR, MX>::THREADS, 1)
 // Warpgroup 0 holds the TMA producer (warp 0) and the MMA issuer (warp 1; warps 2-3 idle) and
 // gives registers up (setmaxnreg) to the fold warpgroups 1-2, whose threads each hold BN/2
 // accumulators: the two warps of a TMEM lane quarter split the tile's columns in halves, and
-// each half lies in one 128-column scale block of B. A thread loads its columns from TMEM in
-// 64-column chunks through one register buffer, folds each with packed fp32 FMAs, and
-// releases the TMEM buffer as soon as the block's last chunk is in registers. With two
-// buffers the MMA runs one block ahead of the fold, so the release of a buffer (its wake-up,
-// loads and first chunk's FMAs) sits on the tensor pipe's critical path: measured at
-// 16384 x 14336 x 4096, the fold's FMAs cost 0.19 of the 0.80 ms and the per-block hand-over
-// without them ~0.08 against the per-tensor kernel's 0.54 ms. (32-column chunks with the next
-// one in flight measured the same; plain scalar FMAs 11 % slower.)
+// each half lies in one 128-column scale block of B. With two buffers the MMA runs one block
+// ahead of the fold, so the time from a block's completion to the release of its buffer sits
+// on the tensor pipe's path. Per-block clock traces (16384 x 14336 x 4096, CTA pairs) put
+// that time at ~700 cycles when a thread loaded 64 columns, folded them and loaded the other
+// 64 (~150 without the FMAs), and the round trip from a release to the completion of the
+// block two ahead at ~1200 cycles, against ~700 per block of tensor work. A warp issues in
+// order, so a load into registers that the preceding FMAs read waits for them: the fold
+// therefore loads through 80 registers in three groups, each load placed ahead of FMAs on
+// other registers (see the loop). 224-wide tiles with a whole block in registers (32
+// accumulators per thread parked in the TMEM the narrower buffers leave free) measured slower:
+// the tensor pipe takes about as long per K block at N = 224 as at 256.
 // With PAIR, two CTAs of a cluster share a 256 x BN tile through the CTA-pair MMA (each holds
 // its 128 rows of A and half of B's rows) and each folds its own 128 rows.
 template <int BN, bool PAIR>
@@ -753,8 +756,8 @@ struct BlkCfg {
   // register split: a CTA is launched with THREADS x LAUNCH_REGS registers; warpgroup 0 keeps
   // CTRL_REGS per thread and the two fold warpgroups take FOLD_REGS (0: no split)
   static constexpr int LAUNCH_REGS = 168;
-  static constexpr int CTRL_REGS = 56;
-  static constexpr int FOLD_REGS = BN == 256 ? 224 : 0;
+  static constexpr int CTRL_REGS = BN == 256 ? 40 : 56;
+  static constexpr int FOLD_REGS = BN == 256 ? 232 : 0;
   static_assert(FOLD_REGS == 0 || 128 * CTRL_REGS + 256 * FOLD_REGS <= THREADS * LAUNCH_REGS, "register split");
   static_assert(SMEM <= 232448, "shared memory");
   static_assert(STAGES >= 3, "ring depth");
@@ -959,44 +962,115 @@ __global__ void __launch_bounds__(BlkCfg<BN, PAIR>::THREADS, 1)
       if (!mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE)) break;
       __syncwarp();
       tc_fence_after();
-      uint32_t buf[64];
-      tmem_ld64(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), buf);
-      for (int kb = 0; ok && kb < pb.num_kb; ++kb) {
-        const float sc = __fmul_rn(sa1, sb1);
-        const bool more = kb + 1 < pb.num_kb;
-        sa1 = sa2;
-        sb1 = sb2;
-        sa2 = (row_ok && kb + 2 < pb.num_kb) ? __ldg(sa_row + kb + 2) : 0.0f;
-        sb2 = (col_ok && kb + 2 < pb.num_kb) ? __ldg(sb_col + static_cast<int64_t>(kb + 2) * pb.sb_ld) : 0.0f;
-        // 64-column chunks through one buffer: two TMEM round trips per block (four with
-        // 32-column chunks), the buffer handed back once the last chunk has landed
-        constexpr int NC64 = COLS / 64;
+      auto release = [&]() {  // this warp's reads of the buffer are done: hand it back to the MMA
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR)
+            mbar_arrive_cluster(tempty_lead + 8 * acc);
+          else
+            mbar_arrive(bar_tempty + 8 * acc);
+        }
+        acc = (acc + 1 == ACC) ? 0 : acc + 1;
+        if (acc == 0) acc_phase ^= 1u;
+      };
+      auto next_block = [&]() {  // wait for the next K block's buffer (the whole warp agrees)
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE));
+        tc_fence_after();
+        return ok;
+      };
+      if constexpr (COLS == 128) {
+        // 128 columns per thread through 80 buffer registers in three groups: lo = columns 0-47
+        // (bA, bB), mid = 48-79 (bC, bD), hi = 80-127 (bA, bB again). Per block: lo and mid
+        // land; lo is folded; hi is loaded into lo's registers while mid is folded; the TMEM
+        // buffer goes back once hi has landed; the next block's mid is loaded while hi is
+        // folded, then its lo. A warp issues in order, so every load is placed ahead of FMAs on
+        // other registers: the loads overlap the FMAs, and only 80 columns of FMAs lie between
+        // a block's completion and the release of its buffer.
+        uint32_t bA[32], bB[16], bC[16], bD[16];
+        auto addr = [&]() { return tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0); };
+        auto load_lo = [&](uint32_t a) {
+          tmem_ld32(a, bA);
+          tmem_ld16(a + 32, bB);
+        };
+        auto load_mid = [&](uint32_t a) {
+          tmem_ld16(a + 48, bC);
+          tmem_ld16(a + 64, bD);
+        };
+        auto fold_ab = [&](int c, float sc) {  // columns c .. c+47 from bA, bB
 #pragma unroll
-        for (int ch = 0; ch < NC64; ++ch) {
+          for (int j = 0; j < 32; j += 2) fma2(accum[c + j], accum[c + j + 1], bA[j], bA[j + 1], sc);
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) fma2(accum[c + 32 + j], accum[c + 33 + j], bB[j], bB[j + 1], sc);
+        };
+        {
+          const uint32_t a = addr();
+          load_mid(a);
+          load_lo(a);
+        }
+        for (int kb = 0; ok && kb < pb.num_kb; ++kb) {
+          const float sc = __fmul_rn(sa1, sb1);
+          const bool more = kb + 1 < pb.num_kb;
+          sa1 = sa2;
+          sb1 = sb2;
+          sa2 = (row_ok && kb + 2 < pb.num_kb) ? __ldg(sa_row + kb + 2) : 0.0f;
+          sb2 = (col_ok && kb + 2 < pb.num_kb) ? __ldg(sb_col + static_cast<int64_t>(kb + 2) * pb.sb_ld) : 0.0f;
           tmem_ld_wait();
-          reg_fence(buf);
-          if (ch + 1 == NC64) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              if constexpr (PAIR)
-                mbar_arrive_cluster(tempty_lead + 8 * acc);
-              else
-                mbar_arrive(bar_tempty + 8 * acc);
-            }
-            acc = (acc + 1 == ACC) ? 0 : acc + 1;
-            if (acc == 0) acc_phase ^= 1u;
+          reg_fence(bA);
+          reg_fence(bB);
+          reg_fence(bC);
+          reg_fence(bD);
+          fold_ab(0, sc);
+          {
+            const uint32_t a = addr();
+            tmem_ld32(a + 80, bA);
+            tmem_ld16(a + 112, bB);
           }
 #pragma unroll
-          for (int j = 0; j < 64; j += 2) fma2(accum[ch * 64 + j], accum[ch * 64 + j + 1], buf[j], buf[j + 1], sc);
-          if (ch + 1 < NC64) {
-            tmem_ld64(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0 + (ch + 1) * 64), buf);
-          } else if (more) {
-            ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, p.w, DEV_ERR_WAIT_EPILOGUE);
+          for (int j = 0; j < 16; j += 2) fma2(accum[48 + j], accum[49 + j], bC[j], bC[j + 1], sc);
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) fma2(accum[64 + j], accum[65 + j], bD[j], bD[j + 1], sc);
+          tmem_ld_wait();
+          reg_fence(bA);
+          reg_fence(bB);
+          release();
+          if (!more) {
+            fold_ab(80, sc);
+          } else if (__all_sync(0xFFFFFFFFu, mbar_test_wait(bar_tfull + 8 * acc, acc_phase))) {
+            // the next block is already waiting: its mid goes ahead of this block's hi FMAs;
+            // otherwise the hi FMAs fill the wait
             __syncwarp();
             tc_fence_after();
-            if (ok) tmem_ld64(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), buf);
+            const uint32_t a = addr();
+            load_mid(a);
+            fold_ab(80, sc);
+            load_lo(a);
+          } else {
+            fold_ab(80, sc);
+            if (next_block()) {
+              const uint32_t a = addr();
+              load_mid(a);
+              load_lo(a);
+            }
           }
+        }
+      } else {
+        // 64 columns per thread: one load, the buffer handed back before the FMAs
+        uint32_t buf[64];
+        tmem_ld64(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), buf);
+        for (int kb = 0; ok && kb < pb.num_kb; ++kb) {
+          const float sc = __fmul_rn(sa1, sb1);
+          const bool more = kb + 1 < pb.num_kb;
+          sa1 = sa2;
+          sb1 = sb2;
+          sa2 = (row_ok && kb + 2 < pb.num_kb) ? __ldg(sa_row + kb + 2) : 0.0f;
+          sb2 = (col_ok && kb + 2 < pb.num_kb) ? __ldg(sb_col + static_cast<int64_t>(kb + 2) * pb.sb_ld) : 0.0f;
+          tmem_ld_wait();
+          reg_fence(buf);
+          release();
+#pragma unroll
+          for (int j = 0; j < 64; j += 2) fma2(accum[j], accum[j + 1], buf[j], buf[j + 1], sc);
+          if (more && next_block()) tmem_ld64(tmem_base + lane_addr + static_cast<uint32_t>(acc * BN + col0), buf);
         }
       }
       if (!ok) break;

@@ -127,7 +127,9 @@ def test_k_zero_writes_zeros(g):
     assert (C.float() == 0).all()
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (256, 384, 512), (300, 512, 1024), (1024, 1280, 640)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (256, 384, 512), (300, 512, 1024), (1024, 1280, 640),
+                                   # single CTAs at M = 128, CTA pairs above; ragged M; several tiles
+                                   (128, 896, 512), (300, 896, 1024), (1024, 1792, 640), (512, 2688, 256)])
 def test_block_scaled_against_exact(g, M, N, K):
     rng = np.random.default_rng(M + N + K)
     A = rand_codes(rng, (M, K), fp8.E4M3, 100.0)
@@ -141,6 +143,24 @@ def test_block_scaled_against_exact(g, M, N, K):
     torch.cuda.synchronize()
     ref, mag = gemm.block_scaled_mm(A, fp8.E4M3, da, B, fp8.E4M3, db)
     assert_close(host_bf16_f64(C), ref, mag)
+
+
+def test_block_scaled_padded_ldc(g):
+    """A padded ldc: the stores leave the padding columns alone."""
+    M, N, K, ldc = 384, 896, 384, 960
+    rng = np.random.default_rng(17)
+    A = rand_codes(rng, (M, K), fp8.E4M3, 100.0)
+    B = rand_codes(rng, (N, K), fp8.E4M3, 100.0)
+    da = (10.0 ** rng.uniform(-4, -1, size=(M, K // 128))).astype(np.float32)
+    db = (10.0 ** rng.uniform(-4, -1, size=(K // 128, N // 128))).astype(np.float32)
+    C = torch.full((M, ldc), 7.0, dtype=torch.bfloat16, device="cuda")
+    g.fp8_scaled_mm(dev_u8(A), 0, dev_u8(B), 0, M, N, K, K, K, g.FP8_GRAN_BLOCK_128x128, torch.from_numpy(da).cuda(),
+                    torch.from_numpy(db).cuda(), C, ldc)
+    torch.cuda.synchronize()
+    ref, mag = gemm.block_scaled_mm(A, fp8.E4M3, da, B, fp8.E4M3, db)
+    got = host_bf16_f64(C)
+    assert_close(got[:, :N], ref, mag)
+    assert np.all(got[:, N:] == 7.0)
 
 
 def test_gemm_rejections(g):
