@@ -106,6 +106,8 @@ __device__ __forceinline__ void transpose8x8(const uint2 (&in)[8], uint2 (&out)[
 
 // This thread's 8x8 patch of tile (ty, tx); zeros outside the tensor (rows, cols % 8 == 0,
 // so a patch is either wholly inside or wholly outside).
+// KEEP: read with normal L2 priority (an amax pass whose cast pass follows), else evict-first.
+template <bool KEEP = false>
 __device__ __forceinline__ bool load_patch(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld,
                                            int64_t ty, int64_t tx, uint4 (&v)[8]) {
   const int t = threadIdx.x;
@@ -113,8 +115,10 @@ __device__ __forceinline__ bool load_patch(const uint16_t* __restrict__ x, int64
   const int64_t c0 = tx * 128 + (t & 15) * 8;
   const bool in = (r0 < rows) && (c0 < cols);
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    v[i] = in ? __ldcs(reinterpret_cast<const uint4*>(x + (r0 + i) * ld + c0)) : make_uint4(0, 0, 0, 0);
+  for (int i = 0; i < 8; ++i) {
+    const uint4* a = reinterpret_cast<const uint4*>(x + (r0 + i) * ld + c0);
+    v[i] = in ? (KEEP ? __ldcg(a) : __ldcs(a)) : make_uint4(0, 0, 0, 0);
+  }
   return in;
 }
 
@@ -271,7 +275,7 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(uint16_t* 
     for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const uint32_t ty = t / tiles_x, tx = t - ty * tiles_x;
       uint4 v[8];
-      const bool in = load_patch(x, rows, cols, ld, ty, tx, v);
+      const bool in = load_patch<true>(x, rows, cols, ld, ty, tx, v);
       if constexpr (UPD) update_patch(x, delta, cols, ld, ty, tx, in, v);
 #pragma unroll
       for (int i = 0; i < 8; ++i) m = absmax_v(m, v[i]);
@@ -289,7 +293,9 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(uint16_t* 
   }
   const Scaler sc = make_scaler<FMT>(s, d);
   uint32_t ov = 0, un = 0, m = 0;
-  for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  // after an amax pass the tiles are walked backwards: the first ones read are still in L2
+  for (uint32_t tr = blockIdx.x; tr < ntiles; tr += gridDim.x) {
+    const uint32_t t = pass ? ntiles - 1 - tr : tr;
     const uint32_t ty = t / tiles_x, tx = t - ty * tiles_x;
     uint4 v[8];
     const bool in = load_patch(x, rows, cols, ld, ty, tx, v);
@@ -451,7 +457,9 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_flat_kernel(const uint1
   if (blockIdx.x == 0 && threadIdx.x == 0) *st.amax_cur = 0.0f;
   if (pass) {
     uint32_t m = 0;
-    for (int64_t i = tid; i < nv; i += nth) m = absmax_v(absmax_v(m, __ldcs(xv + 2 * i)), __ldcs(xv + 2 * i + 1));
+    // read with normal L2 priority: the cast pass below walks the tensor backwards, so its
+    // first reads find the lines this pass read last still in L2
+    for (int64_t i = tid; i < nv; i += nth) m = absmax_v(absmax_v(m, __ldcg(xv + 2 * i)), __ldcg(xv + 2 * i + 1));
     for (int64_t j = nv * 16 + tid; j < n; j += nth) m = absmax_h2(m, x[flat ? j : (j / cols) * ld + j % cols]);
     const uint32_t b = block_max_u32(fold2(m), red);
     grid.sync();  // amax_cur is zero
@@ -467,25 +475,31 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_flat_kernel(const uint1
   const Scaler sc = make_scaler<FMT>(s, d);
   uint32_t ov = 0, un = 0, m = 0;
   uint4* qv = reinterpret_cast<uint4*>(q);
+  // after an amax pass the tensor is walked backwards (vector nv - 1 - i), so that the first
+  // reads find the lines that pass read last still in L2; a single pass walks it forwards
+  // (measured faster for a lone streaming pass)
+  const int64_t rv = pass ? nv - 1 : 0, sv = pass ? -1 : 1;
   int64_t i = tid;
   for (; i + nth < nv; i += 2 * nth) {
     uint4 a[2][2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      a[u][0] = __ldcs(xv + 2 * (i + u * nth));
-      a[u][1] = __ldcs(xv + 2 * (i + u * nth) + 1);
+      const int64_t v = rv + sv * (i + u * nth);
+      a[u][0] = __ldcs(xv + 2 * v);
+      a[u][1] = __ldcs(xv + 2 * v + 1);
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const uint2 lo = cast8<FMT, true>(a[u][0], sc, ov, un, m);
       const uint2 hi = cast8<FMT, true>(a[u][1], sc, ov, un, m);
-      qv[i + u * nth] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+      qv[rv + sv * (i + u * nth)] = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
   }
   for (; i < nv; i += nth) {
-    const uint2 lo = cast8<FMT, true>(__ldcs(xv + 2 * i), sc, ov, un, m);
-    const uint2 hi = cast8<FMT, true>(__ldcs(xv + 2 * i + 1), sc, ov, un, m);
-    qv[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    const int64_t v = rv + sv * i;
+    const uint2 lo = cast8<FMT, true>(__ldcs(xv + 2 * v), sc, ov, un, m);
+    const uint2 hi = cast8<FMT, true>(__ldcs(xv + 2 * v + 1), sc, ov, un, m);
+    qv[v] = make_uint4(lo.x, lo.y, hi.x, hi.y);
   }
   for (int64_t j = nv * 16 + tid; j < n; j += nth) {
     const uint16_t b = x[flat ? j : (j / cols) * ld + j % cols];
