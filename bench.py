@@ -326,10 +326,14 @@ def run_gpu(args):
     # ---- sub-records (rank 0 reports them; every rank runs the same work)
     subs = {}
     if not args.headline_only:
-        subs["finegrained_upproj_fwd_mx"] = bench_finegrained_mx(ctx, args.steps, args.warmup)
-        subs["backward_upproj"] = bench_backward(ctx, max(5, args.steps // 2), args.warmup)
-        subs["delayed_loop"] = bench_delayed_loop(ctx, max(3, args.steps // 4), args.warmup)
-        subs["gpt2s_train_step"] = bench_gpt2(ctx, args.steps, args.warmup)
+        want = set(args.records.split(",")) if args.records else None
+        runs = [("finegrained_upproj_fwd_mx", lambda: bench_finegrained_mx(ctx, args.steps, args.warmup)),
+                ("backward_upproj", lambda: bench_backward(ctx, max(5, args.steps // 2), args.warmup)),
+                ("delayed_loop", lambda: bench_delayed_loop(ctx, max(3, args.steps // 4), args.warmup)),
+                ("gpt2s_train_step", lambda: bench_gpt2(ctx, args.steps, args.warmup))]
+        for name, run in runs:
+            if want is None or name in want:
+                subs[name] = run()
         for k, v in subs.items():
             if k in cpu:
                 v["cpu_baseline"] = cpu[k]
@@ -1163,6 +1167,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true", help="time the headline step only (no sub-records)")
+    ap.add_argument("--records", default="", help="comma-separated sub-records to time (default: all of them)")
     ap.add_argument("--sweep", action="store_true", help="time every workload's GEMM and cast shapes instead")
     ap.add_argument("--only", default="", help="comma-separated sweep entries")
     ap.add_argument("--cpu-leg", default="", help=argparse.SUPPRESS)
