@@ -4,7 +4,9 @@ Reduced size (all layers and steps, fewer tokens and a narrower d): every layer-
 scaling state (history, count, scale, scale_inv, amax, counters) and codes bit-exact;
 GEMM outputs within the bound at a few steps. Full size: the loop's shapes for two of
 the twelve layers, the weight's state and codes every step, the x and dy states every
-step, sampled outputs at the last step."""
+step, sampled outputs at the first and last steps. Odd layers (and layer 11 at full size)
+run the backward with the wgrad reading x_q and dy_q MN-major, the others with the
+transposed copies."""
 import numpy as np
 import pytest
 import torch
@@ -29,8 +31,12 @@ def assert_close(got, ref, mag):
 
 
 class Layer:
-    def __init__(self, g, w_bits, M, K, N, hist):
-        self.g, self.M, self.K, self.N = g, M, K, N
+    """One layer's step through the library. mn: the backward through fp8_linear_bwd_mn (the
+    wgrad reads x_q and dy_q MN-major, split K through a workspace, as bench.py times it);
+    otherwise fp8_linear_bwd with the transposed copies."""
+
+    def __init__(self, g, w_bits, M, K, N, hist, mn=False):
+        self.g, self.M, self.K, self.N, self.mn = g, M, K, N, mn
         self.w = dev_bf16(w_bits)
         self.wst, self.xst, self.gst = g.TensorState(hist), g.TensorState(hist), g.TensorState(hist)
         self.wq, self.wqT = empty_u8(K, N), empty_u8(N, K)
@@ -38,16 +44,22 @@ class Layer:
         self.dyq, self.dyqT = empty_u8(M, N), empty_u8(N, M)
         bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
         self.y, self.dx, self.dw = bf(M, N), bf(M, K), bf(K, N)
+        self.wsb = g.fp8_linear_bwd_workspace_bytes(M, K, N)
+        self.ws = torch.zeros(max(self.wsb, 16), dtype=torch.uint8, device="cuda")
 
     def step(self, x, dy, delta):
         g, D, T = self.g, self.g.FP8_SCALE_DELAYED, self.g.FP8_GRAN_TENSOR
         if delta is not None:  # simulated optimizer step (harness, not the library)
             self.w.copy_((self.w.float() + delta).to(torch.bfloat16))
         g.fp8_requantize_weights(self.w, self.K, self.N, T, D, self.wst, self.wq, self.wqT)
-        g.fp8_linear_fwd(x, self.M, self.K, self.N, self.wqT, self.wst, None, self.xst, T, D, self.xq, self.xqT,
-                         None, self.y)
-        g.fp8_linear_bwd(dy, self.M, self.K, self.N, self.xqT, self.xst, self.wq, self.wst, self.gst, D, self.dyq,
-                         self.dyqT, self.dx, self.dw)
+        g.fp8_linear_fwd(x, self.M, self.K, self.N, self.wqT, self.wst, None, self.xst, T, D, self.xq,
+                         None if self.mn else self.xqT, None, self.y)
+        if self.mn:
+            g.fp8_linear_bwd_mn(dy, self.M, self.K, self.N, self.xq, self.xst, self.wq, self.wst, self.gst, D,
+                                self.dyq, self.dx, self.dw, self.ws, self.wsb)
+        else:
+            g.fp8_linear_bwd(dy, self.M, self.K, self.N, self.xqT, self.xst, self.wq, self.wst, self.gst, D,
+                             self.dyq, self.dyqT, self.dx, self.dw)
         for st in (self.wst, self.xst, self.gst):
             g.fp8_history_commit(st)
 
@@ -68,7 +80,7 @@ def test_delayed_loop_reduced_trajectory(g):
     w_b = [normal_bf16(5100 + l, (K, N), 0.02) for l in range(L)]
     delta = lambda l, t: perturbation_f32(15000 + 100 * t + l, (K, N), 1e-3)
     x, dy = dev_bf16(x_b), dev_bf16(dy_b)
-    layers = [Layer(g, w_b[l], M, K, N, H) for l in range(L)]
+    layers = [Layer(g, w_b[l], M, K, N, H, mn=(l % 2 == 1)) for l in range(L)]  # both backward paths
     recs = {}
 
     def on_step(t, l, rec):
@@ -91,7 +103,9 @@ def test_delayed_loop_reduced_trajectory(g):
             assert np.array_equal(host_u8(lay.dyq), r["dy"]["q"])
             if t in check_gemm_at:
                 wo, xo, go = r["w"], r["x"], r["dy"]
-                assert np.array_equal(host_u8(lay.xqT), xo["qT"]) and np.array_equal(host_u8(lay.dyqT), go["qT"])
+                assert np.array_equal(host_u8(lay.xq), xo["q"])
+                if not lay.mn:
+                    assert np.array_equal(host_u8(lay.xqT), xo["qT"]) and np.array_equal(host_u8(lay.dyqT), go["qT"])
                 yr, ym, _ = gemm.scaled_mm(xo["q"], fp8.E4M3, wo["qT"], fp8.E4M3, xo["d"], wo["d"])
                 dxr, dxm, _ = gemm.scaled_mm(go["q"], fp8.E5M2, wo["q"], fp8.E4M3, go["d"], wo["d"])
                 dwr, dwm, _ = gemm.scaled_mm(xo["qT"], fp8.E4M3, go["qT"], fp8.E5M2, xo["d"], go["d"])
@@ -120,8 +134,8 @@ def test_delayed_loop_full_size(g):
     ox0 = quant.quantize_tensor(x_b, fp8.E4M3)
     og0 = quant.quantize_tensor(dy_b, fp8.E5M2)
     rng = np.random.default_rng(9)
-    for l in (0, 11):
-        lay = Layer(g, wl["w"][l], M, K, N, H)
+    for l in (0, 11):  # layer 11 through the MN-major backward, as the bench runs it
+        lay = Layer(g, wl["w"][l], M, K, N, H, mn=(l == 11))
         ws = quant.DelayedState(H)
         w_host = wl["w"][l].copy()
         for t in range(T):
