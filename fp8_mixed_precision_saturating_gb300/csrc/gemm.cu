@@ -73,7 +73,7 @@ constexpr int QSTG_BYTES = 32 * 64;  // one staging buffer of FP8 output: 32 row
 template <int BN, int QF, bool PAIR = false, bool MX = false>
 struct Cfg {
   static_assert(BN == 128 || BN == 192 || BN == 256, "tile width");
-  static_assert(!MX || (QF < 0 && !PAIR && BN != 192), "MX: single CTAs, tiles of whole scale atoms, bf16 out");
+  static_assert(!MX || (QF < 0 && BN != 192 && (!PAIR || BN == 256)), "MX: tiles of whole scale atoms, bf16 out");
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;   // B rows this CTA loads per stage
   static constexpr int B_BYTES = B_ROWS * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -87,12 +87,12 @@ struct Cfg {
   static constexpr int STG = MX ? STG_BYTES / 2 : STG_BYTES;
   static constexpr int STAGES_FIT = (230000 - EPI_WARPS * (STG + QSTG_PER_WARP)) / (STAGE_BYTES + SF_BYTES);
   static constexpr int STAGES = STAGES_FIT < (192 * 1024) / STAGE_BYTES ? STAGES_FIT : (192 * 1024) / STAGE_BYTES;
-  // TMEM: ACC accumulator buffers, then (MX) 4 columns of A's scales and 4 per atom of B's
+  // TMEM: ACC accumulator buffers, then (MX) the K block's scale columns: 4 of A's scales and
+  // 4 per atom of B's
   static constexpr int SF_COLS = MX ? 4 * (1 + SFB_ATOMS) : 0;
   static constexpr int ACC = (512 - SF_COLS) / BN;
   static constexpr int SFA_COL = ACC * BN;
-  static constexpr int SFB_COL = SFA_COL + 4;
-  static_assert(!MX || SFB_COL + 4 * SFB_ATOMS <= 512, "TMEM columns");
+  static_assert(!MX || SFA_COL + SF_COLS <= 512, "TMEM columns");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int STG_PER_WARP = 1;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(Cfg<BN, QF, PAIR, MX>::THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
-    if (p.nprob > 1) {
+    if (p.nprob > 1 || (MX && PAIR)) {  // (MX pairs: A's and B's scale maps)
       tma_prefetch_desc(&tmA1);
       tma_prefetch_desc(&tmB1);
       tma_prefetch_desc(&tmC1);
@@ -351,7 +351,18 @@ __global__ void __launch_bounds__(Cfg<BN, QF, PAIR, MX>::THREADS, 1)
           if (i == 0 && kb == un.kb0) FP8GB_STAMP(7);
 #endif
           const uint32_t sa = sbase + stage * STAGE_BYTES;
-          if constexpr (PAIR) {
+          if constexpr (PAIR && MX) {
+            // both CTAs' operand and scale bytes land on rank 0's barrier; each CTA holds its
+            // own 128 rows of A's scales and the scales of all the tile's columns of B (its
+            // tensor core computes every column of the tile); the scale atoms come through
+            // tensor maps (tmA1: A's atoms as rows of 512 bytes; tmB1: B's, [atom][kb][512 B])
+            const uint32_t sfs = sbase + C::OFF_SF + stage * C::SF_BYTES;
+            if (rank == 0) mbar_arrive_expect_tx(fb, 2 * (STAGE_BYTES + C::SF_BYTES));
+            tma_load_2d_pair(sa, tA, full_lead + 8 * stage, kb * BK, arow);
+            tma_load_2d_pair(sa + A_BYTES, tB, full_lead + 8 * stage, kb * BK, brow);
+            tma_load_2d_pair(sfs, &tmA1, full_lead + 8 * stage, 0, (arow / BM) * p.pr[0].sf_nkb + kb);
+            tma_load_3d_pair(sfs + 512, &tmB1, full_lead + 8 * stage, 0, kb, un.nb * C::SFB_ATOMS);
+          } else if constexpr (PAIR) {
             // both CTAs' bytes land on rank 0's barrier, which alone expects them
             if (rank == 0) mbar_arrive_expect_tx(fb, 2 * STAGE_BYTES);
             if (q.mn) {  // (a CTA's half of B is one 128-column box)
@@ -416,6 +427,24 @@ __global__ void __launch_bounds__(Cfg<BN, QF, PAIR, MX>::THREADS, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       const int nmine = slot_units(p, tile0, tile_step);
+      // MX: a stage's scale atoms into TMEM (a CTA pair's copy moves each CTA's shared memory
+      // into its own tensor memory). The copies and the MMAs after them execute in issue order;
+      // measured, they cost ~80 ns of tensor-pipe time per K block (the MMAs alone ran the
+      // 16384 x 14336 x 4096 GEMM in 0.48 ms), and issuing them one block ahead into a second
+      // slot, or from a second thread, made it slower
+      auto copy_scales = [&](int st) {
+        const uint32_t sfs = sbase + C::OFF_SF + st * C::SF_BYTES;
+        const uint32_t col = tmem_base + C::SFA_COL;
+        if constexpr (PAIR) {
+          tmem_cp_32x128b_x4_pair(col, smem_desc_plain128(sfs));
+#pragma unroll
+          for (int a = 0; a < C::SFB_ATOMS; ++a) tmem_cp_32x128b_x4_pair(col + 4 + 4 * a, smem_desc_plain128(sfs + 512 * (1 + a)));
+        } else {
+          tmem_cp_32x128b_x4(col, smem_desc_plain128(sfs));
+#pragma unroll
+          for (int a = 0; a < C::SFB_ATOMS; ++a) tmem_cp_32x128b_x4(col + 4 + 4 * a, smem_desc_plain128(sfs + 512 * (1 + a)));
+        }
+      };
       for (int i = 0; ok && i < nmine; ++i) {
         const int u = slot_unit(p, tile0, tile_step, i);
         KProb q;
@@ -439,18 +468,22 @@ __global__ void __launch_bounds__(Cfg<BN, QF, PAIR, MX>::THREADS, 1)
           const uint64_t bdesc = q.mn ? smem_desc_sw128_mn(sa + A_BYTES) : smem_desc_sw128(sa + A_BYTES);
           const uint64_t kstep = q.mn ? (32 * 128) >> 4 : 32 >> 4;
           if constexpr (MX) {
-            // this K block's scales into TMEM (the copies and the MMAs below execute in issue
-            // order), then four MMAs of 32 K, each taking byte k of every row's scale word
-            const uint32_t sfs = sbase + C::OFF_SF + stage * C::SF_BYTES;
-            tmem_cp_32x128b_x4(tmem_base + C::SFA_COL, smem_desc_plain128(sfs));
+            // the block's scales, then four MMAs of 32 K, each taking byte k of every row's
+            // scale word
+            copy_scales(stage);
+            const uint32_t sfa = tmem_base + C::SFA_COL, sfb = sfa + 4;
+            if constexpr (PAIR) {
 #pragma unroll
-            for (int a = 0; a < C::SFB_ATOMS; ++a)
-              tmem_cp_32x128b_x4(tmem_base + C::SFB_COL + 4 * a, smem_desc_plain128(sfs + 512 * (1 + a)));
+              for (int k = 0; k < BK / 32; ++k)
+                mma_mxf8_pair(d, adesc + 2 * k, bdesc + 2 * k, q.idesc | idesc_sf_ids(k, k), sfa, sfb,
+                              (kb != kb0 || k != 0));
+              mma_commit_pair(bar_empty + 8 * stage, 0x3);
+            } else {
 #pragma unroll
-            for (int k = 0; k < BK / 32; ++k)
-              mma_mxf8(d, adesc + 2 * k, bdesc + 2 * k, q.idesc | idesc_sf_ids(k, k), tmem_base + C::SFA_COL,
-                       tmem_base + C::SFB_COL, (kb != kb0 || k != 0));
-            mma_commit(bar_empty + 8 * stage);
+              for (int k = 0; k < BK / 32; ++k)
+                mma_mxf8(d, adesc + 2 * k, bdesc + 2 * k, q.idesc | idesc_sf_ids(k, k), sfa, sfb, (kb != kb0 || k != 0));
+              mma_commit(bar_empty + 8 * stage);
+            }
           } else {
 #pragma unroll
             for (int k = 0; k < BK / 32; ++k) {
@@ -1565,6 +1598,19 @@ bool encode_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t d0, uint64_t d1, uint64_t d2,
+                    uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   const TileChoice c = choose_tile(M, N, K, num_sms(), pair_capacity(), 2);
@@ -1577,10 +1623,16 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why
   // one row block
   TileChoice choice{g.N > 128 ? 256 : 128, false, 1};
   if (g.mx) {
-    // single CTAs, whole scale atoms per tile: 256 wide (one accumulator, the next tile's MMAs
-    // wait for this tile's TMEM loads) or 128 wide (three accumulators)
+    // whole scale atoms per tile: 256 wide (one accumulator, the next tile's MMAs wait for this
+    // tile's TMEM loads), on CTA pairs when M has more than one row block, or 128 wide on
+    // single CTAs (three accumulators)
 #ifdef FP8GB_MX_FORCE_BN
     choice.bn = FP8GB_MX_FORCE_BN;
+#endif
+#ifdef FP8GB_MX_FORCE_PAIR  // compile-time override, for tuning builds
+    choice.pair = FP8GB_MX_FORCE_PAIR != 0 && choice.bn == 256 && g.M > BM;
+#else
+    choice.pair = choice.bn == 256 && g.M > BM && pair_capacity() > 0;
 #endif
   } else if (g.block_scaled) {
 #ifdef FP8GB_BLK_FORCE_PAIR  // compile-time override, for tuning builds
@@ -1627,6 +1679,22 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream, const char** why
       return cudaErrorInvalidValue;
     }
     p.cst = g.cst;
+  }
+  if (g.mx && choice.pair) {
+    // the scale atoms through tensor maps (a CTA pair's loads signal the even CTA's barrier):
+    // A's as rows of 512 bytes (128 words), B's as [column block][K block][512 bytes], whose
+    // box takes a 256-wide tile's two column blocks
+    Maps msf = m0;
+    const uint64_t nkb = static_cast<uint64_t>(g.K / 128);
+    const uint64_t atoms_a = static_cast<uint64_t>((g.M + 127) / 128) * nkb;
+    const uint64_t blocks_b = static_cast<uint64_t>((g.N + 127) / 128);
+    if (!encode_tmap_2d(&msf.a, g.sfa8, CU_TENSOR_MAP_DATA_TYPE_UINT32, 128, atoms_a, 512, 128, 1, 0) ||
+        !encode_tmap_3d(&msf.b, g.sfb8, CU_TENSOR_MAP_DATA_TYPE_UINT32, 128, nkb, blocks_b, 512, nkb * 512, 128, 1,
+                        2)) {
+      *why = "cuTensorMapEncodeTiled failed for the MX scale atoms";
+      return cudaErrorInvalidValue;
+    }
+    return launch_kernel<256, -1, true, true>(m0, msf, tq, p, stream);
   }
   if (g.mx) return choice.bn == 256 ? launch_kernel<256, -1, false, true>(m0, m0, tq, p, stream)
                                     : launch_kernel<128, -1, false, true>(m0, m0, tq, p, stream);

@@ -50,6 +50,10 @@ struct QuantStates {
 // rows, row_bytes = leading dimension in bytes; swizzle 128 = 128-byte swizzle, 0 = none.
 bool encode_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t inner, uint64_t outer,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, int swizzle);
+// 3-D tiled tensor map (no swizzle): dims d0 (contiguous) x d1 x d2, strides of dims 1 and 2
+// in bytes, box b0 x b1 x b2.
+bool encode_tmap_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t d0, uint64_t d1, uint64_t d2,
+                    uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
 
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
