@@ -368,8 +368,9 @@ fp8_status_t fp8_scaled_mm_quant(const void* A, fp8_format_t fa, const void* B, 
   if (lda < K || ldb < K) return fail(FP8_ERR_INVALID_ARG, "%s: lda or ldb < K", who);
   if (!aligned16(A) || !aligned16(B) || lda % 16 != 0 || ldb % 16 != 0)
     return fail(FP8_ERR_ALIGNMENT, "%s: A and B must be 16-byte aligned with lda, ldb multiples of 16", who);
-  cudaError_t e = cudaMemsetAsync(c_st->amax_cur, 0, sizeof(float), s);
-  if (e != cudaSuccess) return cuda_fail(e, who);
+  // delayed scaling: the epilogue (or, before the history holds an entry, the bootstrap cast)
+  // adds the output's amax to amax_cur, the running maximum since the last history commit
+  cudaError_t e;
   GemmArgs g{A, B, C_bf16, M, N, K, lda, ldb, ldc, (int)fa, (int)fb, scale_inv_a, scale_inv_b, false};
   g.qf = (int)fc;
   g.Cq = Cq;

@@ -172,15 +172,20 @@ __device__ __forceinline__ void store_patch(const uint2 (&c)[8], bool in, int64_
 }
 
 // ---------------------------------------------------------------------------------------
-// per-tensor quantise: one cooperative launch (every CTA resident, grid-wide syncs)
+// per-tensor quantise
 // ---------------------------------------------------------------------------------------
-//   1. CTA 0 zeroes amax_cur. If the call needs the tensor's own amax (current scaling, or
-//      delayed scaling before the history holds an entry) every CTA reduces max |x| over its
-//      share; sync; the CTA maxima go into amax_cur with atomicMax; sync. Otherwise one sync
-//      orders the zeroing before the cast's own atomicMax.
-//   2. s and d from amax_cur or from the history; CTA 0 stores them.
-//   3. every CTA casts its share (the second read of x comes from L2 when x fits in it),
-//      counts, and in delayed scaling past bootstrap accumulates the current amax.
+// One cooperative launch (every CTA resident). amax_cur holds the running maximum of the
+// delayed-scaling casts of the tensor since the last history commit, which pushes it into the
+// history and resets it to 0; a current-scaling cast sets it to its own tensor's amax.
+//   current scaling: CTA 0 zeroes amax_cur; every CTA reduces max|x| over its share; grid
+//     sync; atomicMax; grid sync; scale from amax_cur; cast.
+//   delayed scaling: before the history holds an entry (bootstrap) the same amax pass onto
+//     amax_cur as it stands, then the scale from it; past bootstrap, one pass with the
+//     history's scale that adds its amax to amax_cur with atomicMax at the end. That pass has
+//     no grid-wide sync (measured: dropping the one that used to order CTA 0's zeroing of
+//     amax_cur before the atomics saved ~2 us per cast, GPT-2-small to the loop's sizes; a
+//     separate bootstrap-amax kernel ahead of a plain launch cost ~4 us more instead).
+// The cast pass after an amax pass gets its second read of x from L2 where x fits.
 __device__ __forceinline__ bool needs_amax_pass(const QuantState& st, int delayed) {
   return !delayed || *st.hist_count == 0;
 }
@@ -269,7 +274,7 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(uint16_t* 
   const uint32_t tiles_x = static_cast<uint32_t>((cols + 127) / 128);
   const uint32_t ntiles = tiles_x * static_cast<uint32_t>((rows + 127) / 128);
   const bool pass = needs_amax_pass(st, delayed);
-  if (blockIdx.x == 0 && threadIdx.x == 0) *st.amax_cur = 0.0f;
+  if (!delayed && blockIdx.x == 0 && threadIdx.x == 0) *st.amax_cur = 0.0f;
   if (pass) {
     uint32_t m = 0;
     for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
@@ -281,9 +286,9 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(uint16_t* 
       for (int i = 0; i < 8; ++i) m = absmax_v(m, v[i]);
     }
     const uint32_t b = block_max_u32(fold2(m), red);
-    grid.sync();  // amax_cur is zero
+    grid.sync();  // (current scaling) amax_cur is zero
     if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
-    grid.sync();  // amax_cur is the tensor's amax
+    grid.sync();  // amax_cur holds the tensor's amax
   }
   float s, d;
   scales_from_amax(call_amax(st, delayed), Fmt<FMT>::kMax, s, d);
@@ -313,9 +318,8 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_tiles_kernel(uint16_t* 
     store_patch(c, in, rows, cols, ty, tx, q, qT, tT[it++ & 1]);
   }
   block_add_counters(ov, un, st.counters, red);
-  if (!pass) {  // delayed scaling past bootstrap: this cast measures the current amax
+  if (!pass) {  // delayed scaling: this cast's amax onto the running maximum
     const uint32_t b = block_max_u32(fold2(m), red);
-    grid.sync();  // block 0 has zeroed amax_cur
     if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
   }
 }
@@ -354,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 4) quant_tiles_many_kernel(const __g
 #pragma unroll
   for (int j = 0; j < kMaxJobs; ++j)
     if (j < J.n && (!J.j[j].delayed || s_hn[j] == 0)) passmask |= 1u << j;
-  if (blockIdx.x == 0 && threadIdx.x < J.n) *J.j[threadIdx.x].st.amax_cur = 0.0f;
+  // current scaling restarts amax_cur; delayed scaling adds to the running maximum
+  if (blockIdx.x == 0 && threadIdx.x < J.n && !J.j[threadIdx.x].delayed) *J.j[threadIdx.x].st.amax_cur = 0.0f;
   if (passmask) {
 #pragma unroll
     for (int j = 0; j < kMaxJobs; ++j) {
@@ -375,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 4) quant_tiles_many_kernel(const __g
       const uint32_t b = block_max_u32(fold2(m), red);
       if (threadIdx.x == 0) s_max[j] = b;
     }
-    grid.sync();  // every job's amax_cur is zero
+    grid.sync();  // every current-scaling job's amax_cur is zero
     if (threadIdx.x < J.n && ((passmask >> threadIdx.x) & 1u) && s_max[threadIdx.x] != 0)
       atomic_max_amax(J.j[threadIdx.x].st.amax_cur, s_max[threadIdx.x]);
     grid.sync();  // amax_cur holds each such job's tensor amax
@@ -428,8 +433,8 @@ __global__ void __launch_bounds__(kThreads, 4) quant_tiles_many_kernel(const __g
       if (threadIdx.x == 0) s_max[j] = b;
     }
   }
-  if (any_delayed) {  // delayed casts past bootstrap record their current amax
-    grid.sync();      // block 0 has zeroed every amax_cur
+  if (any_delayed) {  // delayed casts past bootstrap add their amax to the running maximum
+    __syncthreads();  // thread 0's s_max entries
     if (threadIdx.x < J.n && !((passmask >> threadIdx.x) & 1u) && s_max[threadIdx.x] != 0)
       atomic_max_amax(J.j[threadIdx.x].st.amax_cur, s_max[threadIdx.x]);
   }
@@ -454,7 +459,7 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_flat_kernel(const uint1
   const int64_t nv = flat ? n / 16 : 0;  // 16 elements per step: 2 x 16 B in, 16 B out
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   const bool pass = needs_amax_pass(st, delayed);
-  if (blockIdx.x == 0 && threadIdx.x == 0) *st.amax_cur = 0.0f;
+  if (!delayed && blockIdx.x == 0 && threadIdx.x == 0) *st.amax_cur = 0.0f;
   if (pass) {
     uint32_t m = 0;
     // read with normal L2 priority: the cast pass below walks the tensor backwards, so its
@@ -462,9 +467,9 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_flat_kernel(const uint1
     for (int64_t i = tid; i < nv; i += nth) m = absmax_v(absmax_v(m, __ldcg(xv + 2 * i)), __ldcg(xv + 2 * i + 1));
     for (int64_t j = nv * 16 + tid; j < n; j += nth) m = absmax_h2(m, x[flat ? j : (j / cols) * ld + j % cols]);
     const uint32_t b = block_max_u32(fold2(m), red);
-    grid.sync();  // amax_cur is zero
+    grid.sync();  // (current scaling) amax_cur is zero
     if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
-    grid.sync();  // amax_cur is the tensor's amax
+    grid.sync();  // amax_cur holds the tensor's amax
   }
   float s, d;
   scales_from_amax(call_amax(st, delayed), Fmt<FMT>::kMax, s, d);
@@ -507,12 +512,12 @@ __global__ void __launch_bounds__(kThreads) quant_tensor_flat_kernel(const uint1
     q[j] = cast1<FMT>(b, s, ov, un);
   }
   block_add_counters(ov, un, st.counters, red);
-  if (!pass) {
+  if (!pass) {  // delayed scaling: this cast's amax onto the running maximum
     const uint32_t b = block_max_u32(fold2(m), red);
-    grid.sync();  // block 0 has zeroed amax_cur
     if (threadIdx.x == 0) atomic_max_amax(st.amax_cur, b);
   }
 }
+
 
 // ---------------------------------------------------------------------------------------
 // 128 x 128 block scales: one CTA per block, amax of the block, then its cast
@@ -777,6 +782,7 @@ __global__ void history_commit_kernel(QuantStates sts) {
     const int n = *st.hist_count;
     st.hist[n % st.hist_len] = *st.amax_cur;
     *st.hist_count = n + 1;
+    *st.amax_cur = 0.0f;  // the next step's delayed casts start a new running maximum
   }
 }
 
@@ -847,6 +853,7 @@ cudaError_t launch_coop(void (*kernel)(KArgs...), int grid, cudaStream_t stream,
   return launch_coop_smem(kernel, grid, stream, 0, std::forward<Args>(args)...);
 }
 
+
 }  // namespace
 
 cudaError_t launch_quant_tensor(int fmt, bool delayed, bool tiled, const void* x, int64_t rows, int64_t cols,
@@ -855,15 +862,16 @@ cudaError_t launch_quant_tensor(int fmt, bool delayed, bool tiled, const void* x
   auto* qp = static_cast<uint8_t*>(q);
   auto* tp = static_cast<uint8_t*>(qT);
   const int dl = delayed ? 1 : 0;
+  auto go = [&](auto k, int grid, auto... args) { return launch_coop(k, grid, stream, args...); };
   if (tiled) {
     auto k = fmt == 0 ? quant_tensor_tiles_kernel<0, false> : quant_tensor_tiles_kernel<1, false>;
     const int64_t ntiles = ((cols + 127) / 128) * ((rows + 127) / 128);
-    return launch_coop(k, coop_grid(k, ntiles), stream, const_cast<uint16_t*>(xp), rows, cols, ld, qp, tp, st, dl,
-                       static_cast<const float*>(nullptr));
+    return go(k, coop_grid(k, ntiles), const_cast<uint16_t*>(xp), rows, cols, ld, qp, tp, st, dl,
+              static_cast<const float*>(nullptr));
   }
   auto k = fmt == 0 ? quant_tensor_flat_kernel<0> : quant_tensor_flat_kernel<1>;
-  return launch_coop(k, coop_grid(k, (rows * cols + 4095) / 4096), stream, xp, rows, cols, ld, qp, st, dl,
-                     static_cast<const int32_t*>(nullptr));
+  return go(k, coop_grid(k, (rows * cols + 4095) / 4096), xp, rows, cols, ld, qp, st, dl,
+            static_cast<const int32_t*>(nullptr));
 }
 
 cudaError_t launch_quant_many(int fmt, const TileJobs& jobs, cudaStream_t stream) {
@@ -877,7 +885,7 @@ cudaError_t launch_quant_tensor_if_empty_history(int fmt, const void* x, int64_t
                                                  void* q, const QuantState& st, cudaStream_t stream) {
   auto k = fmt == 0 ? quant_tensor_flat_kernel<0> : quant_tensor_flat_kernel<1>;
   return launch_coop(k, coop_grid(k, (rows * cols + 4095) / 4096), stream, static_cast<const uint16_t*>(x), rows,
-                     cols, ld, static_cast<uint8_t*>(q), st, 0, static_cast<const int32_t*>(st.hist_count));
+                     cols, ld, static_cast<uint8_t*>(q), st, 1, static_cast<const int32_t*>(st.hist_count));
 }
 
 cudaError_t launch_update_quant_tensor(bool delayed, void* w, const float* delta, int64_t rows, int64_t cols,

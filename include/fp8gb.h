@@ -101,7 +101,9 @@ typedef enum { FP8_SCALE_CURRENT = 0, FP8_SCALE_DELAYED = 1 } fp8_scaling_t;
  *                                 amax_history[hist_count % hist_len]
  *   scale        fp32             s = FP8_MAX / amax_eff of the most recent cast
  *   scale_inv    fp32             d = amax_eff / FP8_MAX (what the GEMM multiplies by)
- *   amax_cur     fp32             max |x| of the tensor of the most recent cast
+ *   amax_cur     fp32             delayed scaling: the running maximum of max |x| over the
+ *                                 casts since the last history commit (which resets it to
+ *                                 0); current scaling: max |x| of the most recent cast
  *   counters     uint64 [2]       [0] saturated elements, [1] non-zero elements flushed to
  *                                 zero; both accumulate until the caller clears them
  * If amax_eff is zero or not finite, s = d = 1. */
@@ -121,8 +123,10 @@ typedef struct {
  *  its scale (multiplied by s = FP8_MAX / amax) before the cast.
  *  gran = FP8_GRAN_TENSOR: one scale for the whole tensor, from x's own amax (mode
  *    CURRENT; two passes over x) or from st's history (mode DELAYED; bootstrap with the
- *    current amax while hist_count == 0). `st` is required; the call writes st->amax_cur,
- *    st->scale, st->scale_inv and adds to st->counters. `unit_scale_inv` is ignored.
+ *    current amax while hist_count == 0). `st` is required; the call writes st->scale and
+ *    st->scale_inv, adds to st->counters, and sets st->amax_cur to x's amax (CURRENT) or
+ *    raises it to x's amax when below (DELAYED; the bootstrap scale then comes from that
+ *    running maximum). `unit_scale_inv` is ignored.
  *  gran = FP8_GRAN_TILE_1x128: cols % 128 == 0; one scale per (row, 128 columns), the
  *    inverse scales written to unit_scale_inv [rows, cols/128] (fp32, row-major). Mode
  *    must be CURRENT. `st` may be NULL; if given, st->amax_cur receives the tensor amax and
@@ -255,8 +259,9 @@ int64_t fp8_scaled_mm_grouped_workspace_bytes(const fp8_mm_problem_t* problems, 
  * backward), so the bf16 result is not read back by a separate cast.
  *  [GUARD] "Real products...": delayed scaling with amax history. The codes use the output's
  *  delayed scale: Cq = cast_fc( fl32( bf16(C) * s_c ) ), s_c from c_st's history (required,
- *  delayed mode); the call records c_st->amax_cur = max |bf16(C)|, scale, scale_inv and adds
- *  to the counters, exactly as fp8_quantize of the bf16 output with FP8_SCALE_DELAYED would.
+ *  delayed mode); the call raises c_st->amax_cur to max |bf16(C)|, records scale and
+ *  scale_inv and adds to the counters, exactly as fp8_quantize of the bf16 output with
+ *  FP8_SCALE_DELAYED would.
  *  While the history is empty (the bootstrap call) the scale needs the output's own amax, so
  *  the epilogue writes only C_bf16 and a second kernel, launched every call and returning at
  *  once when the history is non-empty, casts it from its current amax.
@@ -402,7 +407,8 @@ fp8_status_t fp8_linear_bwd_noalloc(const void* dy_bf16, int64_t M, int64_t K, i
                                     void* dx_bf16, void* dw_bf16, void* stream);
 
 /* Push st->amax_cur into the history: amax_history[hist_count % hist_len] = amax_cur;
- * hist_count += 1. [GUARD] "Real products...": amax history tracking. */
+ * hist_count += 1; amax_cur = 0 (the next step's delayed casts start a new running maximum).
+ * [GUARD] "Real products...": amax history tracking. */
 fp8_status_t fp8_history_commit(const fp8_tensor_state_t* st, void* stream);
 
 /* The same push for n distinct states (0 <= n <= 32) in one launch: states points to a

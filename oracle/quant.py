@@ -21,8 +21,13 @@ Definitions (readings where the pages leave a step open):
 * overflow = number of non-NaN inputs with |fl32(x * s)| > FP8_MAX (infinite inputs
   included); underflow = number of non-zero non-NaN inputs whose code is +-0.
 * delayed scaling: a ring of ``hist_len`` fp32 amaxes and a push count n.  A cast uses
-  amax_eff = max of the filled entries when n > 0, else (bootstrap) the current amax.
-  Each cast records its own current amax; ``commit`` pushes it at index n % hist_len.
+  amax_eff = max of the filled entries when n > 0.  The state's amax_cur is the running
+  maximum of the delayed casts since the last ``commit``; ``commit`` pushes it at index
+  n % hist_len and resets it to 0.  In bootstrap (n == 0) a cast takes its scale from
+  amax_cur after adding its own amax (its own amax when it is the first cast since the
+  commit).  A current-scaling cast sets amax_cur to its own amax.  The pages record one amax
+  per tensor per step; with one cast of each tensor per step, this reading and "each cast
+  records its own amax" give the same history and scales.
 
 * MX units (hardware block scaling): 32 consecutive elements along the contraction
   dimension share a power-of-two scale 2^e, stored as one UE8M0 byte e + 127.  e is the
@@ -201,13 +206,19 @@ class DelayedState:
         return np.float32(self.hist[:n].max())
 
     def quantize(self, x_bits: np.ndarray, fmt: str, delayed: bool = True):
-        """Cast with the delayed scale (or the current one in bootstrap / current mode)."""
+        """Cast with the delayed scale; in bootstrap with the running maximum including this
+        tensor's amax; in current mode with this tensor's own amax."""
         cur = amax(x_bits)
-        eff = self.amax_eff() if delayed else None
-        a = cur if eff is None else eff
+        if delayed:
+            self.amax_cur = np.float32(max(self.amax_cur, cur))
+            eff = self.amax_eff()
+            a = self.amax_cur if eff is None else eff
+        else:
+            self.amax_cur = cur
+            a = cur
         s, d = scales_from_amax(a, fmt)
         q, ov, un = cast_with_scale(x_bits, s, fmt)
-        self.scale, self.scale_inv, self.amax_cur = s, d, cur
+        self.scale, self.scale_inv = s, d
         self.overflow += ov
         self.underflow += un
         out = dict(q=q, s=s, d=d, amax=cur, overflow=ov, underflow=un)
@@ -218,6 +229,7 @@ class DelayedState:
     def commit(self):
         self.hist[self.count % self.hist_len] = self.amax_cur
         self.count += 1
+        self.amax_cur = np.float32(0.0)
 
     def snapshot(self):
         return dict(hist=self.hist.copy(), count=self.count, scale=self.scale, scale_inv=self.scale_inv,

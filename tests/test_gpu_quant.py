@@ -236,6 +236,33 @@ def test_delayed_bootstrap_and_commit(g):
         assert snap["overflow"] == o["overflow"] and snap["underflow"] == o["underflow"]
 
 
+@pytest.mark.parametrize("tiled", [False, True])
+def test_delayed_running_max_and_commit_reset(g, tiled):
+    """amax_cur is the running maximum of the delayed casts since the last commit, the bootstrap
+    scale included (the bootstrap amax kernel, then the cast as a plain launch), and the commit
+    resets it; a current-scaling cast sets it to its own amax. Against the oracle's state."""
+    st, ost = g.TensorState(hist_len=2), quant.DelayedState(hist_len=2)
+    R, C = 64, 128
+    for t, (scale, mode) in enumerate([(3.0, 1), (0.5, 1), (6.0, 1), (None, "commit"), (0.25, 1), (2.0, 1),
+                                        (0.125, 0), (None, "commit"), (9.0, 1)]):
+        if mode == "commit":
+            g.fp8_history_commit(st)
+            ost.commit()
+        else:
+            x = bf16_bits_from_f32(quant.widen_bf16(normal_bf16(600 + t, (R, C))) * np.float32(scale))
+            q, qT = empty_u8(R, C), (empty_u8(C, R) if tiled else None)
+            g.fp8_quantize(dev_bf16(x), R, C, C, 1, g.FP8_GRAN_TENSOR, mode, st, q, qT)
+            ref = ost.quantize(x, fp8.E5M2, delayed=(mode == 1))
+            assert np.array_equal(host_u8(q), ref["q"]), t
+            if tiled:
+                assert np.array_equal(host_u8(qT), ref["qT"]), t
+        snap, o = st.snapshot(), ost.snapshot()
+        assert np.float32(snap["amax_cur"]) == o["amax_cur"], t
+        assert np.float32(snap["scale"]) == o["scale"] and snap["count"] == o["count"], t
+        assert np.array_equal(snap["hist"], o["hist"]), t
+        assert snap["overflow"] == o["overflow"] and snap["underflow"] == o["underflow"], t
+
+
 def test_empty_tensor_writes_unit_scales(g):
     st = g.TensorState()
     st.scale.fill_(5.0)

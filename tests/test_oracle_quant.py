@@ -126,6 +126,26 @@ def test_delayed_state_hand_trajectory():
     assert st.count == 6 and st.hist.tolist() == [0.5, 0.25, 8.0]
 
 
+def test_delayed_running_max_and_commit_reset():
+    """amax_cur: the running maximum of the delayed casts since the last commit (the bootstrap
+    scale included), reset by the commit; a current-scaling cast sets it to its own amax."""
+    st = quant.DelayedState(hist_len=2)
+    r1 = st.quantize(bits([3.0, -1.0]), fp8.E4M3, delayed=True)  # bootstrap: amax 3
+    assert st.amax_cur == 3.0 and r1["s"] == np.float32(448.0 / 3.0)
+    r2 = st.quantize(bits([1.5]), fp8.E4M3, delayed=True)  # still bootstrap: the running max 3
+    assert st.amax_cur == 3.0 and r2["s"] == r1["s"] and r2["amax"] == 1.5
+    r3 = st.quantize(bits([-6.0]), fp8.E4M3, delayed=True)
+    assert st.amax_cur == 6.0 and r3["s"] == np.float32(448.0 / 6.0)
+    st.commit()
+    assert st.amax_cur == 0.0 and st.hist.tolist() == [6.0, 0.0] and st.count == 1
+    r4 = st.quantize(bits([0.5]), fp8.E4M3, delayed=True)  # past bootstrap: the history's 6
+    assert st.amax_cur == 0.5 and r4["s"] == np.float32(448.0 / 6.0)
+    st.quantize(bits([0.25]), fp8.E4M3, delayed=False)  # current scaling: its own amax
+    assert st.amax_cur == 0.25
+    st.commit()
+    assert st.hist.tolist() == [6.0, 0.25] and st.amax_cur == 0.0
+
+
 def test_delayed_saturation_is_counted():
     st = quant.DelayedState(hist_len=4)
     st.quantize(bits([1.0, 0.5]), fp8.E4M3)
