@@ -1079,7 +1079,7 @@ def leg_gpt2(rows: int):
 
 
 # leg name -> (function, slab rows with all cores, slab rows on one core)
-CPU_LEGS = {"finegrained": (leg_finegrained, 128, 64), "finegrained_upproj_fwd_mx": (leg_finegrained_mx, 16, 8), "backward_upproj": (leg_backward, 1024, 256),
+CPU_LEGS = {"finegrained": (leg_finegrained, 1024, 256), "finegrained_upproj_fwd_mx": (leg_finegrained_mx, 128, 32), "backward_upproj": (leg_backward, 1024, 256),
             "delayed_loop": (leg_delayed_loop, 1024, 256), "gpt2s_train_step": (leg_gpt2, 2048, 512)}
 
 
