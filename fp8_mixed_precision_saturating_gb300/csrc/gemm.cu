@@ -430,9 +430,8 @@ __global__ void __launch_bounds__(Cfg<BN, QF, PAIR, MX>::THREADS, 1)
       // MX: a stage's scale atoms into TMEM (a CTA pair's copy moves each CTA's shared memory
       // into its own tensor memory). The copies and the MMAs after them execute in issue order;
       // measured, they cost ~80 ns of tensor-pipe time per K block (the MMAs alone ran the
-      // 16384 x 14336 x 4096 GEMM in 0.48 ms); the cost is per copy (issuing each twice added
-      // ~75 us), and issuing them one block ahead into a second slot, or from a second thread,
-      // made it slower, while alternating two or four sets of columns changed nothing
+      // 16384 x 14336 x 4096 GEMM in 0.48 ms), and issuing them one block ahead into a second
+      // slot, or from a second thread, made it slower
       auto copy_scales = [&](int st) {
         const uint32_t sfs = sbase + C::OFF_SF + st * C::SF_BYTES;
         const uint32_t col = tmem_base + C::SFA_COL;
