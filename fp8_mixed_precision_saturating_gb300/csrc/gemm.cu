@@ -114,6 +114,29 @@ struct Cfg {
   static_assert(OFF_STG % 1024 == 0 && STG % 1024 == 0 && OFF_QSTG % 512 == 0, "staging on swizzle atoms");
 };
 
+// floor(n / d) for 0 <= n < 2^31 and 1 <= d < 2^31 as (n * m) >> (32 + s), with
+// s = ceil(log2 d) and m = floor(2^(32+s) / d) + 1 (division by invariant integers using
+// multiplication, Granlund and Montgomery, 1994): m = (2^(32+s) + e) / d with 0 < e <= d, so
+// n m / 2^(32+s) exceeds n / d by less than n / 2^(32+s) < 1 / (2 d), which never reaches the
+// next integer. The work-unit mapping runs at every tile and first at each CTA's start, where
+// five integer divisions (a long dependent sequence each) cost ~0.5 us before the first load.
+struct DivBy {
+  uint64_t m;
+  uint32_t s;
+};
+
+inline DivBy make_div(uint32_t d) {
+  DivBy r{0, 0};
+  if (d == 0) return r;
+  while ((uint64_t(1) << r.s) < d) ++r.s;
+  r.m = ((uint64_t(1) << (32 + r.s)) / d) + 1;
+  return r;
+}
+
+__host__ __device__ __forceinline__ uint32_t div_by(uint32_t n, const DivBy& d) {
+  return static_cast<uint32_t>((static_cast<uint64_t>(n) * d.m) >> (32 + d.s));
+}
+
 // One GEMM problem of a launch. A launch runs one problem, or two independent ones (the
 // backward pass's dgrad and wgrad) whose work units share the persistent grid.
 struct KProb {
@@ -137,6 +160,11 @@ struct KProb {
   // operands stored contraction-major (A as [K, M], B as [K, N], row-major) and read MN-major
   // by the tensor cores: tiles arrive as boxes of 128 MN x 128 K
   int mn;
+  // K blocks of a tile's first split unit (num_kb / 2; unused without split K)
+  int kb_half;
+  // the tile raster's divisors as multipliers (see DivBy): tiles per raster group, rows of a
+  // group, rows of the last (shorter) group
+  DivBy div_group, div_gm, div_glast;
 };
 
 constexpr int kMaxSlots = 160;         // CTAs (or CTA pairs) of a persistent grid
@@ -155,11 +183,12 @@ struct KParams {
   int sched_len;
   uint16_t sched_off[kMaxSlots + 1];
   uint16_t sched_unit[kMaxSchedUnits];
+  DivBy div_slots;  // the grid's CTA (pair) slots
 };
 
 __device__ __forceinline__ int slot_units(const KParams& p, int slot, int slots) {
   if (p.sched_len > 0) return p.sched_off[slot + 1] - p.sched_off[slot];
-  return slot < p.units ? (p.units - slot + slots - 1) / slots : 0;
+  return slot < p.units ? static_cast<int>(div_by(static_cast<uint32_t>(p.units - slot + slots - 1), p.div_slots)) : 0;
 }
 
 __device__ __forceinline__ int slot_unit(const KParams& p, int slot, int slots, int i) {
@@ -192,17 +221,21 @@ __device__ __forceinline__ KProb prob_of(const KParams& p, int pi) {
   q.sf_nkb = pi ? b.sf_nkb : a.sf_nkb;
   q.sfb_atoms = pi ? b.sfb_atoms : a.sfb_atoms;
   q.mn = pi ? b.mn : a.mn;
+  q.kb_half = pi ? b.kb_half : a.kb_half;
+  q.div_group = pi ? b.div_group : a.div_group;
+  q.div_gm = pi ? b.div_gm : a.div_gm;
+  q.div_glast = pi ? b.div_glast : a.div_glast;
   return q;
 }
 
-__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m, int& mb, int& nb) {
-  const int per_group = group_m * num_n;
-  const int g = t / per_group;
+__device__ __forceinline__ void tile_coords(int t, const KProb& q, int group_m, int& mb, int& nb) {
+  const int g = static_cast<int>(div_by(static_cast<uint32_t>(t), q.div_group));
   const int first_m = g * group_m;
-  const int gsize = min(group_m, num_m - first_m);
-  const int local = t - g * per_group;
-  mb = first_m + local % gsize;
-  nb = local / gsize;
+  const bool last = q.num_m - first_m < group_m;  // the last group may hold fewer row blocks
+  const int gsize = last ? q.num_m - first_m : group_m;
+  const int local = t - g * group_m * q.num_n;
+  nb = static_cast<int>(div_by(static_cast<uint32_t>(local), last ? q.div_glast : q.div_gm));
+  mb = first_m + (local - nb * gsize);
 }
 
 // Work unit u of the launch -> its problem, output tile (row and column block), split and
@@ -216,11 +249,12 @@ __device__ __forceinline__ Unit unit_at(int u, const KParams& p, KProb& q) {
   r.pi = (p.nprob > 1 && u >= p.pr[1].unit0) ? 1 : 0;
   q = prob_of(p, r.pi);
   const int v = u - q.unit0;
-  r.t = v / q.splits;
+  // one or two units per tile; with two, the first takes K blocks [0, num_kb / 2)
+  r.t = q.splits > 1 ? v >> 1 : v;
   r.split = v - r.t * q.splits;
-  r.kb0 = r.split * q.num_kb / q.splits;
-  r.kb1 = (r.split + 1) * q.num_kb / q.splits;
-  tile_coords(r.t, q.num_m, q.num_n, p.group_m, r.mb, r.nb);
+  r.kb0 = r.split ? q.kb_half : 0;
+  r.kb1 = (q.splits > 1 && r.split == 0) ? q.kb_half : q.num_kb;
+  tile_coords(r.t, q, p.group_m, r.mb, r.nb);
   return r;
 }
 
@@ -878,7 +912,7 @@ __global__ void __launch_bounds__(BlkCfg<BN, PAIR>::THREADS, 1)
       const uint32_t full_lead = PAIR ? mapa_shared(bar_full, 0) : bar_full;
       for (int t = tile0; ok && t < pb.num_tiles; t += tile_step) {
         int mb, nb;
-        tile_coords(t, pb.num_m, pb.num_n, p.group_m, mb, nb);
+        tile_coords(t, pb, p.group_m, mb, nb);
         const int arow = mb * TILE_M + static_cast<int>(rank) * BM;
         const int brow = nb * BN + static_cast<int>(rank) * C::B_ROWS;
         for (int kb = 0; kb < pb.num_kb; ++kb) {
@@ -977,7 +1011,7 @@ __global__ void __launch_bounds__(BlkCfg<BN, PAIR>::THREADS, 1)
     bool ok = true;
     for (int t = tile0; ok && t < pb.num_tiles; t += tile_step) {
       int mb, nb;
-      tile_coords(t, pb.num_m, pb.num_n, p.group_m, mb, nb);
+      tile_coords(t, pb, p.group_m, mb, nb);
       const int row0 = mb * TILE_M + static_cast<int>(rank) * BM + q * 32;  // this warp's 32 rows
       const int row = row0 + lane;
       const int nblk = (nb * BN + col0) / 128;
@@ -1432,9 +1466,24 @@ void make_schedule(KParams& p, int slots) {
   for (size_t i = 0; i < sc.unit.size(); ++i) p.sched_unit[i] = sc.unit[i];
 }
 
+// The kernel's division-free work-unit mapping (DivBy): per problem the tile raster's
+// divisors and the first split unit's K blocks, and the grid's slot count.
+void set_divisors(KParams& p, int slots) {
+  for (KProb* q : {&p.pr[0], &p.pr[1]}) {
+    const int gm = p.group_m;
+    q->kb_half = q->num_kb / 2;
+    q->div_group = make_div(static_cast<uint32_t>(gm * q->num_n));
+    q->div_gm = make_div(static_cast<uint32_t>(gm));
+    const int glast = q->num_m - ((q->num_m + gm - 1) / gm - 1) * gm;  // rows of the last group
+    q->div_glast = make_div(static_cast<uint32_t>(glast > 0 ? glast : gm));
+  }
+  p.div_slots = make_div(static_cast<uint32_t>(slots));
+}
+
 template <int BN, int QF, bool PAIR, bool MX = false>
 cudaError_t launch_kernel(const Maps& m0, const Maps& m1, const CUtensorMap& tq, KParams& p, cudaStream_t stream) {
   using C = Cfg<BN, QF, PAIR, MX>;
+  if (p.pr[0].splits > 2 || p.pr[1].splits > 2) return cudaErrorInvalidValue;  // (unit_at: one or two)
   int clusters = 0;
   cudaError_t e = prepare_kernel<BN, QF, PAIR, MX>(&clusters);
   if (e != cudaSuccess) return e;
@@ -1443,6 +1492,7 @@ cudaError_t launch_kernel(const Maps& m0, const Maps& m1, const CUtensorMap& tq,
   if (slots > kMaxSlots) slots = kMaxSlots;
   if (p.units < slots) slots = p.units;
   make_schedule(p, slots);
+  set_divisors(p, slots);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? 2 * slots : slots));
   cfg.blockDim = dim3(C::THREADS);
@@ -1538,6 +1588,7 @@ cudaError_t launch_blk(const Maps& m, KParams& p, cudaStream_t stream, const cha
   if (e != cudaSuccess) return e;
   if (slots <= 0) return cudaErrorInvalidConfiguration;
   if (slots > p.pr[0].num_tiles) slots = p.pr[0].num_tiles;
+  set_divisors(p, slots);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? 2 * slots : slots));
   cfg.blockDim = dim3(C::THREADS);
